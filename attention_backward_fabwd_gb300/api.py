@@ -1,0 +1,143 @@
+"""torch-facing call with the argument list of the page "CANN ops-transformer FlashAttnGrad 算子详解"
+(discosf.com/news/4863418), §4.2 function prototype, over the libfabwd C ABI.
+
+torch provides device memory and the stream only; every step of the backward runs in libfabwd's
+CUDA kernels.  The outputs and the workspace are allocated here (caller-owned in the C ABI).
+"""
+from __future__ import annotations
+
+import enum
+from typing import Optional, Tuple, Union
+
+import torch
+
+from . import fabwd as F
+
+
+class MaskMode(enum.IntEnum):
+    """mask_mode values ([FAG] §4.3 lists an IntEnum whose table was lost; this is the reading
+    the library implements): 0 none, 1 causal (bottom-right aligned), 2 band (windows)."""
+
+    NONE = 0
+    CAUSAL = 1
+    BAND = 2
+
+
+_DTYPES = {torch.bfloat16: F.FABWD_BF16, torch.float16: F.FABWD_FP16}
+_LAYOUTS = {"BSND": F.FABWD_BSND, "TND": F.FABWD_TND, "BNSD": F.FABWD_BNSD}
+
+
+def mask_mode_value(mask_mode: Union[int, str, MaskMode]) -> int:
+    """Accept an IntEnum, an int or the enum name as a case-insensitive string ([FAG] §4.3)."""
+    if isinstance(mask_mode, str):
+        try:
+            return int(MaskMode[mask_mode.strip().upper()])
+        except KeyError:
+            raise ValueError(f"unknown mask_mode name {mask_mode!r}") from None
+    return int(mask_mode)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, *, cu_seqlens_q=None, cu_seqlens_kv=None,
+                softmax_scale=0.0, mask_mode=0, win_left=-1, win_right=-1, max_seqlen_q=-1, max_seqlen_kv=-1,
+                layout="BSND") -> F.fabwd_params:
+    """Fill fabwd_params from tensors (shapes give B, S1, S2, N1, N2, D, Dv, T1, T2)."""
+    if layout not in _LAYOUTS:
+        raise ValueError(f"layout must be one of {sorted(_LAYOUTS)}, got {layout!r}")
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"q must be bfloat16 or float16, got {q.dtype}")
+    p = F.fabwd_params()
+    p.dtype = _DTYPES[q.dtype]
+    p.layout = _LAYOUTS[layout]
+    if layout == "TND":
+        if cu_seqlens_q is None or cu_seqlens_kv is None:
+            raise ValueError("the TND layout needs cu_seqlens_q and cu_seqlens_kv")
+        p.B = cu_seqlens_q.numel() - 1
+        p.T1, p.N1, p.D = q.shape
+        p.T2, p.N2, _ = k.shape
+        p.Dv = v.shape[-1]
+        if max_seqlen_q < 0 or max_seqlen_kv < 0:
+            cq, ck = cu_seqlens_q.to("cpu", torch.int64), cu_seqlens_kv.to("cpu", torch.int64)   # synchronises
+            if max_seqlen_q < 0:
+                max_seqlen_q = int((cq[1:] - cq[:-1]).max()) if p.B > 0 else 0
+            if max_seqlen_kv < 0:
+                max_seqlen_kv = int((ck[1:] - ck[:-1]).max()) if p.B > 0 else 0
+        p.S1, p.S2 = max_seqlen_q, max_seqlen_kv
+    elif layout == "BSND":
+        p.B, p.S1, p.N1, p.D = q.shape
+        _, p.S2, p.N2, _ = k.shape
+        p.Dv = v.shape[-1]
+    else:
+        p.B, p.N1, p.S1, p.D = q.shape
+        _, p.N2, p.S2, _ = k.shape
+        p.Dv = v.shape[-1]
+    p.q, p.k, p.v, p.dout, p.attn_out = (_ptr(t) for t in (q, k, v, dout, attn_out))
+    p.softmax_lse = _ptr(softmax_lse)
+    p.cu_seqlens_q, p.cu_seqlens_kv = _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv)
+    p.softmax_scale = float(softmax_scale)
+    p.mask_mode = mask_mode_value(mask_mode)
+    p.win_left, p.win_right = int(win_left), int(win_right)
+    p.dq, p.dk, p.dv = _ptr(dq), _ptr(dk), _ptr(dv)
+    return p
+
+
+def _check_tensors(q, k, v, dout, attn_out, softmax_lse, cu_q, cu_kv):
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("libfabwd runs on CUDA tensors only")
+    for name, t in (("k", k), ("v", v), ("dout", dout), ("attn_out", attn_out)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must have q's dtype {q.dtype} ([FAG] §4.6), got {t.dtype}")
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, q on {dev}")
+    if softmax_lse.dtype != torch.float32:
+        raise TypeError("softmax_lse must be float32 ([FAG] §4.6)")
+    for name, t in (("cu_seqlens_q", cu_q), ("cu_seqlens_kv", cu_kv)):
+        if t is not None and t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+
+
+def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_seqlens_kv=None, seqused_q=None,
+                    seqused_kv=None, sinks=None, attn_mask=None, metadata=None, softmax_scale=0.0, mask_mode=0,
+                    win_left=-1, win_right=-1, max_seqlen_q=-1, max_seqlen_kv=-1, layout_q="BSND",
+                    layout_kv="BSND", layout_out="BSND", *, check_status=False,
+                    return_workspace=False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Gradients (dq, dk, dv) of attention from the saved attn_out and softmax_lse.
+
+    Arguments follow [FAG] §4.2.  Differences: seqused_q/kv, sinks and attn_mask are not
+    supported (their semantics are not stated) and raise; `metadata` (an Ascend core-split plan)
+    is accepted and ignored, the GPU schedule is derived from the shapes.  The three layouts must
+    agree ([FAG] §4.6).  Non-contiguous inputs are made contiguous.  With TND and
+    max_seqlen_* = -1 the lengths are read from cu_seqlens on the host (a synchronisation).
+    check_status=True synchronises and raises if the kernels reported a device-side problem.
+    """
+    if seqused_q is not None or seqused_kv is not None or sinks is not None or attn_mask is not None:
+        raise NotImplementedError("seqused_q/seqused_kv/sinks/attn_mask are not supported")
+    if not (layout_q == layout_kv == layout_out):
+        raise ValueError("layout_q, layout_kv and layout_out must be the same ([FAG] §4.6)")
+    q, k, v, dout, attn_out, softmax_lse = (t.contiguous() for t in (q, k, v, dout, attn_out, softmax_lse))
+    if cu_seqlens_q is not None:
+        cu_seqlens_q = cu_seqlens_q.contiguous()
+    if cu_seqlens_kv is not None:
+        cu_seqlens_kv = cu_seqlens_kv.contiguous()
+    _check_tensors(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q, cu_seqlens_kv)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    p = make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, cu_seqlens_q=cu_seqlens_q,
+                    cu_seqlens_kv=cu_seqlens_kv, softmax_scale=softmax_scale, mask_mode=mask_mode,
+                    win_left=win_left, win_right=win_right, max_seqlen_q=max_seqlen_q,
+                    max_seqlen_kv=max_seqlen_kv, layout=layout_q)
+    nbytes = F.fabwd_workspace_size(p)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    F.fabwd_preprocess(p, ws.data_ptr(), ws.numel(), stream)
+    F.fabwd_run(p, ws.data_ptr(), ws.numel(), stream)
+    if check_status:
+        s, bits = F.fabwd_read_device_status(ws.data_ptr(), ws.numel(), stream)
+        if s != F.FABWD_OK:
+            raise F.FabwdError(s, f"device status 0x{bits:x}")
+    if return_workspace:
+        return dq, dk, dv, (p, ws)
+    return dq, dk, dv

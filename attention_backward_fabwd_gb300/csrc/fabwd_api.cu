@@ -1,0 +1,301 @@
+// libfabwd host side: argument validation, workspace planning, TMA descriptors and launches.
+// The argument rules are those of the page "CANN ops-transformer FlashAttnGrad 算子详解"
+// (discosf.com/news/4863418), §4.6 constraints; the two-phase workspace protocol follows the
+// page "CANN Floyd注意力梯度算子" (jsqmd.com/news/783980), §函数原型.
+#include "../../include/fabwd.h"
+#include "fabwd_internal.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+namespace {
+
+using namespace fabwd;
+
+uint64_t g_wait_ns = 2000000000ull;
+int g_inject_timeout = 0;
+
+struct Plan {
+  long long S1p = 0;       // padded rows per (sequence, q-head)
+  long long rowsQ = 0;     // q rows over all batches/sequences
+  long long rowsK = 0;
+  size_t off_status = 0, off_lse2 = 0, off_sfmg = 0, off_dqacc = 0, total = 0;
+  double scale = 0.0;
+  long long dq_elems = 0;
+};
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
+  if (!p) return FABWD_ERR_NULLPTR;
+  if (p->dtype != FABWD_BF16 && p->dtype != FABWD_FP16) return FABWD_ERR_INVALID;
+  if (p->layout != FABWD_BSND && p->layout != FABWD_TND && p->layout != FABWD_BNSD) return FABWD_ERR_INVALID;
+  if (p->mask_mode < 0 || p->mask_mode > 2) return FABWD_ERR_INVALID;
+  // [FAG] §4.6: B in (0, 65536); N1 a multiple of N2; 0 < Dv <= D <= 192
+  if (p->B <= 0 || p->B >= 65536) return FABWD_ERR_INVALID;
+  if (p->N1 <= 0 || p->N2 <= 0 || p->N1 % p->N2 != 0) return FABWD_ERR_INVALID;
+  if (p->D <= 0 || p->Dv <= 0 || p->Dv > p->D || p->D > 192) return FABWD_ERR_INVALID;
+  if (p->S1 < 0 || p->S2 < 0 || p->S1 >= (1ll << 30) || p->S2 >= (1ll << 30)) return FABWD_ERR_INVALID;
+  if (p->N1 > 65535 || p->N2 > 65535) return FABWD_ERR_INVALID;
+  // windows: -1 = unbounded; the dense preset (mode 0) takes none ([FAG] §4.6)
+  if (p->win_left < -1 || p->win_right < -1 || p->win_left >= (1ll << 30) || p->win_right >= (1ll << 30))
+    return FABWD_ERR_INVALID;
+  if (p->mask_mode == FABWD_MASK_NONE && (p->win_left >= 0 || p->win_right >= 0)) return FABWD_ERR_INVALID;
+  if (!(p->softmax_scale == p->softmax_scale) || std::isinf(p->softmax_scale)) return FABWD_ERR_INVALID;
+  // TND requires cu_seqlens; the other layouts forbid them ([FAG] §4.6)
+  const bool tnd = p->layout == FABWD_TND;
+  if (tnd) {
+    if (!p->cu_seqlens_q || !p->cu_seqlens_kv) return FABWD_ERR_INVALID;
+    if (p->T1 < 0 || p->T2 < 0 || p->T1 >= (1ll << 31) || p->T2 >= (1ll << 31)) return FABWD_ERR_INVALID;
+    if ((p->T1 > 0 && p->S1 == 0) || (p->T2 > 0 && p->S2 == 0)) return FABWD_ERR_INVALID;
+  } else {
+    if (p->cu_seqlens_q || p->cu_seqlens_kv) return FABWD_ERR_INVALID;
+    if (p->B * p->S1 >= (1ll << 31) || p->B * p->S2 >= (1ll << 31)) return FABWD_ERR_INVALID;
+  }
+  if (!main_supported((int)p->D, (int)p->Dv)) return FABWD_ERR_UNSUPPORTED;
+
+  pl->rowsQ = tnd ? p->T1 : p->B * p->S1;
+  pl->rowsK = tnd ? p->T2 : p->B * p->S2;
+  pl->S1p = (p->S1 + kRowPad - 1) / kRowPad * kRowPad;
+  pl->scale = p->softmax_scale != 0.0 ? p->softmax_scale : 1.0 / std::sqrt((double)p->D);
+  pl->dq_elems = pl->rowsQ * p->N1 * p->D;
+  pl->off_status = 0;
+  pl->off_lse2 = 256;
+  const size_t rowbytes = round_up((size_t)p->B * p->N1 * pl->S1p * sizeof(float), 256);
+  pl->off_sfmg = pl->off_lse2 + rowbytes;
+  pl->off_dqacc = pl->off_sfmg + rowbytes;
+  pl->total = pl->off_dqacc + round_up((size_t)pl->dq_elems * sizeof(float), 256);
+
+  if (check_ptrs) {
+    const bool q_nonempty = pl->rowsQ > 0, k_nonempty = pl->rowsK > 0;
+    if (q_nonempty && (!p->q || !p->dout || !p->attn_out || !p->softmax_lse || !p->dq)) return FABWD_ERR_NULLPTR;
+    if (k_nonempty && (!p->k || !p->v || !p->dk || !p->dv)) return FABWD_ERR_NULLPTR;
+    if (q_nonempty && (!aligned16(p->q) || !aligned16(p->dout) || !aligned16(p->attn_out) || !aligned16(p->dq) ||
+                       (reinterpret_cast<uintptr_t>(p->softmax_lse) & 3u)))
+      return FABWD_ERR_INVALID;
+    if (k_nonempty && (!aligned16(p->k) || !aligned16(p->v) || !aligned16(p->dk) || !aligned16(p->dv)))
+      return FABWD_ERR_INVALID;
+  }
+  return FABWD_OK;
+}
+
+fabwd_status check_ws(const Plan& pl, const void* ws, size_t ws_bytes) {
+  if (!ws || ws_bytes < pl.total) return FABWD_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return FABWD_ERR_WORKSPACE;
+  return FABWD_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 4-D map over a q/k/v/dout tensor with a {64, 1, rows, 1} box (BSND, TND) or {64, rows, 1, 1}
+// box (BNSD), 128-byte swizzle.  Coordinates: (d, head, row, batch) for BSND/TND and
+// (d, row, head, batch) for BNSD; TND is a single batch of T rows.
+bool make_map(CUtensorMap* m, const void* base, bool fp16, int layout, long long dim, long long N, long long S,
+              long long Bn, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  const long long e = 2;
+  cuuint64_t gdim[4], gstr[3];
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  if (layout == kBNSD) {
+    gdim[0] = dim; gdim[1] = S; gdim[2] = N; gdim[3] = Bn;
+    gstr[0] = dim * e; gstr[1] = S * dim * e; gstr[2] = N * S * dim * e;
+    box[1] = box_rows;
+    box[2] = 1;
+  } else {
+    gdim[0] = dim; gdim[1] = N; gdim[2] = S; gdim[3] = Bn;
+    gstr[0] = dim * e; gstr[1] = N * dim * e; gstr[2] = S * N * dim * e;
+  }
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  std::memset(m, 0, sizeof(*m));
+  CUresult r = enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   const_cast<void*>(base), gdim, gstr, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+namespace fabwd {
+bool main_supported(int D, int Dv) { return (D == 64 && Dv == 64) || (D == 128 && Dv == 128); }
+}  // namespace fabwd
+
+extern "C" {
+
+fabwd_status fabwd_workspace_size(const fabwd_params* p, size_t* bytes) {
+  if (!p || !bytes) return FABWD_ERR_NULLPTR;
+  Plan pl;
+  fabwd_status s = plan_and_check(p, &pl, false);
+  if (s != FABWD_OK) return s;
+  *bytes = pl.total;
+  return FABWD_OK;
+}
+
+fabwd_status fabwd_workspace_layout(const fabwd_params* p, size_t* off_sfmg, size_t* off_lse2, size_t* off_dq_accum,
+                                    int64_t* row_stride) {
+  if (!p || !off_sfmg || !off_lse2 || !off_dq_accum || !row_stride) return FABWD_ERR_NULLPTR;
+  Plan pl;
+  fabwd_status s = plan_and_check(p, &pl, false);
+  if (s != FABWD_OK) return s;
+  *off_sfmg = pl.off_sfmg;
+  *off_lse2 = pl.off_lse2;
+  *off_dq_accum = pl.off_dqacc;
+  *row_stride = pl.S1p;
+  return FABWD_OK;
+}
+
+fabwd_status fabwd_preprocess(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
+  Plan pl;
+  fabwd_status s = plan_and_check(p, &pl, true);
+  if (s != FABWD_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != FABWD_OK) return s;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PreArgs a;
+  a.layout = p->layout;
+  a.B = (int)p->B;
+  a.N1 = (int)p->N1;
+  a.D = (int)p->D;
+  a.Dv = (int)p->Dv;
+  a.S1 = p->S1;
+  a.S2 = p->S2;
+  a.T1 = p->T1;
+  a.T2 = p->T2;
+  a.S1p = (int)pl.S1p;
+  a.dout = p->dout;
+  a.attn_out = p->attn_out;
+  a.lse = p->softmax_lse;
+  a.cu_q = p->cu_seqlens_q;
+  a.cu_kv = p->cu_seqlens_kv;
+  a.lse2 = reinterpret_cast<float*>(w + pl.off_lse2);
+  a.sfmg = reinterpret_cast<float*>(w + pl.off_sfmg);
+  a.dq_acc = reinterpret_cast<float*>(w + pl.off_dqacc);
+  a.dq_acc_elems = pl.dq_elems;
+  a.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+  cudaError_t e = launch_preprocess(a, p->dtype == FABWD_FP16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
+}
+
+fabwd_status fabwd_run(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
+  Plan pl;
+  fabwd_status s = plan_and_check(p, &pl, true);
+  if (s != FABWD_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != FABWD_OK) return s;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool fp16 = p->dtype == FABWD_FP16;
+  const bool tnd = p->layout == FABWD_TND;
+  const int inject = g_inject_timeout;
+  g_inject_timeout = 0;
+
+  if (pl.rowsQ > 0 && pl.rowsK > 0 && p->S1 > 0 && p->S2 > 0) {
+    MainMaps maps;
+    const long long Sq = tnd ? p->T1 : p->S1, Sk = tnd ? p->T2 : p->S2, Bn = tnd ? 1 : p->B;
+    if (!make_map(&maps.q, p->q, fp16, p->layout, p->D, p->N1, Sq, Bn, kBlockQ) ||
+        !make_map(&maps.dout, p->dout, fp16, p->layout, p->Dv, p->N1, Sq, Bn, kBlockQ) ||
+        !make_map(&maps.k, p->k, fp16, p->layout, p->D, p->N2, Sk, Bn, kBlockKV) ||
+        !make_map(&maps.v, p->v, fp16, p->layout, p->Dv, p->N2, Sk, Bn, kBlockKV))
+      return FABWD_ERR_CUDA;
+    MainArgs a;
+    a.layout = p->layout;
+    a.B = (int)p->B;
+    a.N1 = (int)p->N1;
+    a.N2 = (int)p->N2;
+    a.G = (int)(p->N1 / p->N2);
+    a.S1 = (int)p->S1;
+    a.S2 = (int)p->S2;
+    a.T1 = p->T1;
+    a.T2 = p->T2;
+    a.cu_q = p->cu_seqlens_q;
+    a.cu_kv = p->cu_seqlens_kv;
+    a.mask_mode = p->mask_mode;
+    a.win_left = (int)p->win_left;
+    a.win_right = (int)p->win_right;
+    a.scale = (float)pl.scale;
+    a.scale_log2 = (float)(pl.scale * 1.4426950408889634);
+    a.S1p = (int)pl.S1p;
+    a.lse2 = reinterpret_cast<const float*>(w + pl.off_lse2);
+    a.sfmg = reinterpret_cast<const float*>(w + pl.off_sfmg);
+    a.dq_acc = reinterpret_cast<float*>(w + pl.off_dqacc);
+    a.dk = p->dk;
+    a.dv = p->dv;
+    a.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+    a.wait_ns = g_wait_ns;
+    a.inject_timeout = inject;
+    const int grid_x = (int)((p->S2 + kBlockKV - 1) / kBlockKV);
+    cudaError_t e = fp16 ? launch_main_fp16(a, maps, (int)p->D, (int)p->Dv, grid_x, st)
+                         : launch_main_bf16(a, maps, (int)p->D, (int)p->Dv, grid_x, st);
+    if (e != cudaSuccess) return FABWD_ERR_CUDA;
+  } else if (pl.rowsK > 0) {
+    // no visible pair at all: dk = dv = 0 (the convert kernel below writes dq = 0)
+    if (launch_zero(p->dk, pl.rowsK * p->N2 * p->D * 2, st) != cudaSuccess ||
+        launch_zero(p->dv, pl.rowsK * p->N2 * p->Dv * 2, st) != cudaSuccess)
+      return FABWD_ERR_CUDA;
+  }
+  ConvArgs c;
+  c.dq_acc = reinterpret_cast<const float*>(w + pl.off_dqacc);
+  c.dq = p->dq;
+  c.elems = pl.dq_elems;
+  c.scale = (float)pl.scale;
+  cudaError_t e = launch_convert(c, fp16, st);
+  return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
+}
+
+fabwd_status fabwd_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32_t* device_status) {
+  if (!ws || !device_status) return FABWD_ERR_NULLPTR;
+  if (ws_bytes < 256) return FABWD_ERR_WORKSPACE;
+  uint32_t v = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return FABWD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FABWD_ERR_CUDA;
+  *device_status = v;
+  if (v & FABWD_DEV_TIMEOUT) return FABWD_ERR_TIMEOUT;
+  if (v) return FABWD_ERR_DEVICE;
+  return FABWD_OK;
+}
+
+uint64_t fabwd_set_wait_limit_ns(uint64_t ns) {
+  const uint64_t old = g_wait_ns;
+  g_wait_ns = ns ? ns : 2000000000ull;
+  return old;
+}
+
+int fabwd_debug_inject_timeout(int on) {
+  const int old = g_inject_timeout;
+  g_inject_timeout = on ? 1 : 0;
+  return old;
+}
+
+const char* fabwd_status_string(fabwd_status s) {
+  switch (s) {
+    case FABWD_OK: return "ok";
+    case FABWD_ERR_NULLPTR: return "a required pointer is NULL";
+    case FABWD_ERR_INVALID: return "invalid argument (dtype, shape, layout, mask, window or alignment)";
+    case FABWD_ERR_UNSUPPORTED: return "valid but unsupported (no kernel built for this head-dim pair)";
+    case FABWD_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case FABWD_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case FABWD_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up (device status)";
+    case FABWD_ERR_DEVICE: return "the kernels found inconsistent cu_seqlens (device status)";
+  }
+  return "unknown status";
+}
+
+int fabwd_version(void) { return 100; }
+
+}  // extern "C"

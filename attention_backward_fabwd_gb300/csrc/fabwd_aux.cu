@@ -1,0 +1,165 @@
+// HBM-bound kernels around the main backward kernel:
+//   preprocess: sfmg = rowsum(dout ⊙ attn_out) (the V1 "softmaxGradFront" stage of the page
+//               "CANN ops-transformer FlashAttnGrad 算子详解", §5.2 data flow), lse · log2(e)
+//               into padded rows, the fp32 dQ accumulator zeroed, device status cleared and
+//               the cu_seqlens checked;
+//   convert:    dq = cast(scale · dQ accumulator) (the fp32-workspace dQ of the same page's
+//               bn2gs1s2 template, §5.2).
+#include "fabwd_internal.cuh"
+#include "fabwd_ptx.cuh"
+#include "../../include/fabwd.h"
+
+#include <cmath>
+
+namespace fabwd {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <bool FP16, int DV>
+__global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    unsigned st = 0;
+    if (a.layout == kTND) {
+      if (a.cu_q[0] != 0 || a.cu_kv[0] != 0) st |= FABWD_DEV_BAD_SEQLENS;
+      for (int s = 0; s < a.B; ++s) {
+        const long long lq = (long long)a.cu_q[s + 1] - a.cu_q[s];
+        const long long lk = (long long)a.cu_kv[s + 1] - a.cu_kv[s];
+        if (lq < 0 || lq > a.S1 || lk < 0 || lk > a.S2) st |= FABWD_DEV_BAD_SEQLENS;
+      }
+      if (a.cu_q[a.B] != a.T1 || a.cu_kv[a.B] != a.T2) st |= FABWD_DEV_BAD_SEQLENS;
+    }
+    *a.status = st;
+  }
+
+  constexpr int LPR = DV / 8;    // lanes per row: one 16-byte chunk (8 elements) each
+  constexpr int RPW = 32 / LPR;  // rows per warp step
+  const long long nrows = (long long)a.B * a.N1 * a.S1p;
+  const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, part = lane % LPR;
+  for (long long base = gwarp * RPW; base < nrows; base += nwarp * RPW) {
+    const long long w = base + sub;
+    const bool active = w < nrows;
+    int b = 0, n1 = 0;
+    long long i = 0;
+    if (active) {
+      if (a.layout == kBNSD) {
+        i = w % a.S1p;
+        n1 = (int)((w / a.S1p) % a.N1);
+        b = (int)(w / ((long long)a.S1p * a.N1));
+      } else {
+        n1 = (int)(w % a.N1);
+        i = (w / a.N1) % a.S1p;
+        b = (int)(w / ((long long)a.N1 * a.S1p));
+      }
+    }
+    long long q0 = 0, L1 = a.S1;
+    if (active && a.layout == kTND) {
+      q0 = a.cu_q[b];
+      L1 = (long long)a.cu_q[b + 1] - q0;
+      if (q0 < 0 || q0 > a.T1) L1 = 0;                 // bad cu_seqlens: touch nothing
+      L1 = L1 < 0 ? 0 : (L1 > a.S1 ? a.S1 : L1);
+      if (q0 + L1 > a.T1) L1 = a.T1 - q0 < 0 ? 0 : a.T1 - q0;
+    }
+    const bool valid = active && i < L1;
+    float acc = 0.f;
+    if (valid) {
+      const long long r = row_index(a.layout, b, q0 + i, n1, a.N1, a.S1);
+      const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * DV + part * 8);
+      const uint4 y = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.attn_out) + r * DV + part * 8);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 xf = unpack2<FP16>(xs[e]), yf = unpack2<FP16>(ys[e]);
+        acc = fmaf(xf.x, yf.x, acc);
+        acc = fmaf(xf.y, yf.y, acc);
+      }
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (active && part == 0) {
+      const long long o = ((long long)b * a.N1 + n1) * a.S1p + i;
+      float l2 = INFINITY;
+      if (valid) {
+        const long long li = a.layout == kTND ? (long long)n1 * a.T1 + q0 + i : ((long long)b * a.N1 + n1) * a.S1 + i;
+        l2 = a.lse[li] * kLog2e;
+      }
+      a.lse2[o] = l2;
+      a.sfmg[o] = valid ? acc : 0.f;
+    }
+  }
+
+  float4* z = reinterpret_cast<float4*>(a.dq_acc);
+  const long long n4 = a.dq_acc_elems / 4;
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n4; x += (long long)gridDim.x * blockDim.x)
+    z[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+template <bool FP16>
+__global__ void __launch_bounds__(256) convert_kernel(ConvArgs a) {
+  const long long n8 = a.elems / 8;
+  const float4* src = reinterpret_cast<const float4*>(a.dq_acc);
+  uint4* dst = reinterpret_cast<uint4*>(a.dq);
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n8; x += (long long)gridDim.x * blockDim.x) {
+    const float4 u = __ldcs(src + 2 * x), v = __ldcs(src + 2 * x + 1);
+    uint4 o;
+    o.x = pack2<FP16>(u.x * a.scale, u.y * a.scale);
+    o.y = pack2<FP16>(u.z * a.scale, u.w * a.scale);
+    o.z = pack2<FP16>(v.x * a.scale, v.y * a.scale);
+    o.w = pack2<FP16>(v.z * a.scale, v.w * a.scale);
+    dst[x] = o;
+  }
+}
+
+__global__ void __launch_bounds__(256) zero_kernel(uint4* p, long long n16) {
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n16; x += (long long)gridDim.x * blockDim.x)
+    p[x] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+int grid_for(long long work_items, int per_block) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long want = (work_items + per_block - 1) / per_block;
+  long long cap = (long long)sms * 8;
+  if (want > cap) want = cap;
+  if (want < 1) want = 1;
+  return (int)want;
+}
+
+}  // namespace
+
+cudaError_t launch_zero(void* p, long long bytes, cudaStream_t st) {
+  if (bytes <= 0) return cudaSuccess;
+  const long long n16 = bytes / 16;
+  zero_kernel<<<grid_for(n16, 256), 256, 0, st>>>(static_cast<uint4*>(p), n16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st) {
+  const long long rows = (long long)a.B * a.N1 * a.S1p;
+  const long long work = rows * (a.Dv / 8) > a.dq_acc_elems / 4 ? rows * (a.Dv / 8) : a.dq_acc_elems / 4;
+  const int grid = grid_for(work, 256);
+  if (a.Dv == 128) {
+    if (fp16) preprocess_kernel<true, 128><<<grid, 256, 0, st>>>(a);
+    else preprocess_kernel<false, 128><<<grid, 256, 0, st>>>(a);
+  } else if (a.Dv == 64) {
+    if (fp16) preprocess_kernel<true, 64><<<grid, 256, 0, st>>>(a);
+    else preprocess_kernel<false, 64><<<grid, 256, 0, st>>>(a);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const ConvArgs& a, bool fp16, cudaStream_t st) {
+  if (a.elems <= 0) return cudaSuccess;
+  const int grid = grid_for(a.elems / 8, 256);
+  if (fp16) convert_kernel<true><<<grid, 256, 0, st>>>(a);
+  else convert_kernel<false><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace fabwd

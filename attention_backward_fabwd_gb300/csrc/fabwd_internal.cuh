@@ -1,0 +1,80 @@
+// Internal kernel arguments and launchers shared by the libfabwd translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fabwd {
+
+constexpr int kBlockKV = 128;  // kv rows per CTA of the main kernel (M of the kv-side MMAs)
+constexpr int kBlockQ = 128;   // q rows per main-loop step (N of S^T / dP^T, M of dQ)
+constexpr int kRowPad = 128;   // padding of the per-(sequence, q-head) lse2 / sfmg rows
+
+enum Layout : int { kBSND = 0, kTND = 1, kBNSD = 2 };
+
+// Element offset of row `row` (sequence-local for BSND/BNSD, global token index for TND) of
+// head n in a [B,S,N,dim] / [T,N,dim] / [B,N,S,dim] tensor, in units of `dim`-element rows.
+__host__ __device__ __forceinline__ long long row_index(int layout, int b, long long row, int n, int N,
+                                                        long long S) {
+  if (layout == kBSND) return ((long long)b * S + row) * N + n;
+  if (layout == kBNSD) return ((long long)b * N + n) * S + row;
+  return row * N + n;
+}
+
+struct PreArgs {
+  int layout, B, N1, D, Dv;
+  long long S1, S2, T1, T2;  // S1/S2: sequence lengths (BSND/BNSD) or max_seqlen (TND)
+  int S1p;                   // padded row count per (sequence, q-head)
+  const void* dout;
+  const void* attn_out;
+  const float* lse;
+  const int* cu_q;
+  const int* cu_kv;
+  float* lse2;               // [B][N1][S1p]: lse * log2(e), +inf on padding rows
+  float* sfmg;               // [B][N1][S1p]: rowsum(dout * attn_out), 0 on padding rows
+  float* dq_acc;             // fp32, q's shape with D
+  long long dq_acc_elems;
+  unsigned* status;
+};
+
+struct ConvArgs {
+  const float* dq_acc;
+  void* dq;
+  long long elems;
+  float scale;
+};
+
+struct MainArgs {
+  int layout, B, N1, N2, G;
+  int S1, S2;                // sequence lengths (BSND/BNSD) or max_seqlen (TND)
+  long long T1, T2;
+  const int* cu_q;
+  const int* cu_kv;
+  int mask_mode, win_left, win_right;
+  float scale, scale_log2;   // scale and scale * log2(e)
+  int S1p;
+  const float* lse2;
+  const float* sfmg;
+  float* dq_acc;
+  void* dk;
+  void* dv;
+  unsigned* status;
+  unsigned long long wait_ns;
+  int inject_timeout;
+};
+
+struct MainMaps {
+  CUtensorMap q, k, v, dout;
+};
+
+cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st);
+cudaError_t launch_convert(const ConvArgs& a, bool fp16, cudaStream_t st);
+// Zero `bytes` (a multiple of 16) at a 16-byte-aligned device address.
+cudaError_t launch_zero(void* p, long long bytes, cudaStream_t st);
+// Returns cudaErrorInvalidValue when no kernel is built for (D, Dv).
+cudaError_t launch_main_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int grid_x, cudaStream_t st);
+cudaError_t launch_main_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int grid_x, cudaStream_t st);
+bool main_supported(int D, int Dv);
+
+}  // namespace fabwd

@@ -1,0 +1,162 @@
+/*
+ * libfabwd — FlashAttention backward pass for NVIDIA GB300 (sm_103a). C ABI.
+ *
+ * [FAG] below is the page "CANN ops-transformer FlashAttnGrad 算子详解" (discosf.com/news/4863418).
+ * The operation is the one [FAG] defines in §一 (equations), §二 (inputs/outputs/attributes), §4.2 (argument
+ * list) and §4.6 (constraints).  Per head, with q-head n1 reading kv-head n2 = n1 / (N1/N2):
+ *
+ *   S = scale · Q Kᵀ,  P = exp(S − softmax_lse) on visible pairs (0 elsewhere)
+ *   dV = Pᵀ dY,  dP = dY Vᵀ,  sfmg = rowsum(dY ⊙ Y),  dS = P ⊙ (dP − sfmg)
+ *   dQ = scale · dS K,  dK = scale · dSᵀ Q          (dK, dV summed over the G q-heads of n2)
+ *
+ * where Y = attn_out and dY = dout, and scale = softmax_scale, or 1/sqrt(D) when it is 0.
+ *
+ * Use is two-phase, after the aclnn two-step workspace convention on the page
+ * "CANN Floyd注意力梯度算子" (jsqmd.com/news/783980), §函数原型:
+ *   1. fabwd_workspace_size(&p, &bytes)     host only, no CUDA call
+ *   2. caller allocates `bytes` of device memory (the workspace) and the outputs dq, dk, dv
+ *   3. fabwd_preprocess(&p, ws, bytes, stream)   sfmg + padded lse + dq accumulator zeroing
+ *   4. fabwd_run(&p, ws, bytes, stream)          main backward kernel + dq convert kernel
+ * Steps 3 and 4 must see the same params and workspace and run on the same stream, in order.
+ *
+ * Ownership: the caller owns every buffer.  The library allocates nothing, never synchronises
+ * (except fabwd_read_device_status, which exists to read a result back), and only enqueues work
+ * on the stream it is given.  No entry point is thread-unsafe except that concurrent calls on
+ * different streams must not share a workspace.
+ *
+ * Errors: every argument problem the host can see is reported before anything is enqueued.
+ * Problems only the device can see (cu_seqlens that disagree with T1/T2 or the max sequence
+ * lengths; a bounded wait inside a kernel that gave up) set bits in a status word inside the
+ * workspace, which fabwd_read_device_status returns.  No kernel traps or spins without limit.
+ */
+#ifndef FABWD_H
+#define FABWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (host side).  The numbering follows the null-pointer / invalid-argument /
+ * unsupported split of the error table on the page "CANN Floyd注意力梯度算子", §返回值. */
+typedef enum {
+  FABWD_OK = 0,
+  FABWD_ERR_NULLPTR = 1,     /* a required pointer is NULL */
+  FABWD_ERR_INVALID = 2,     /* a dtype / shape / layout / mask argument breaks a stated rule */
+  FABWD_ERR_UNSUPPORTED = 3, /* valid per the statement, but no kernel is built for it */
+  FABWD_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than fabwd_workspace_size */
+  FABWD_ERR_CUDA = 5,        /* a CUDA runtime/driver call or kernel launch failed */
+  FABWD_ERR_TIMEOUT = 6,     /* device status: a bounded wait inside a kernel gave up */
+  FABWD_ERR_DEVICE = 7       /* device status: the kernels found bad cu_seqlens */
+} fabwd_status;
+
+/* io dtype of q, k, v, dout, attn_out, dq, dk, dv ([FAG] §4.4: float16 and bfloat16, all one). */
+typedef enum { FABWD_BF16 = 0, FABWD_FP16 = 1 } fabwd_dtype;
+
+/* One layout for q/kv/out ([FAG] §4.6).  Shapes (row-major, innermost last):
+ *   BSND: q [B,S1,N1,D]  k [B,S2,N2,D]  v [B,S2,N2,Dv]  dout/attn_out [B,S1,N1,Dv]
+ *   BNSD: q [B,N1,S1,D]  k [B,N2,S2,D]  v [B,N2,S2,Dv]  dout/attn_out [B,N1,S1,Dv]
+ *   TND:  q [T1,N1,D]    k [T2,N2,D]    v [T2,N2,Dv]    dout/attn_out [T1,N1,Dv]
+ * softmax_lse (fp32): [B,N1,S1] for BSND/BNSD, [N1,T1] for TND ([FAG] §4.6). */
+typedef enum { FABWD_BSND = 0, FABWD_TND = 1, FABWD_BNSD = 2 } fabwd_layout;
+
+/* mask_mode (the enum table of [FAG] §4.3 did not survive; this library's reading):
+ *   0 none (the dense preset: windows must both be -1, [FAG] §4.6),
+ *   1 causal, bottom-right aligned: key j is visible to query i iff j <= i + (S2 - S1),
+ *   2 band.
+ * In modes 1 and 2, win_left >= 0 also requires j >= i + (S2 - S1) - win_left and
+ * win_right >= 0 requires j <= i + (S2 - S1) + win_right; -1 means unbounded.  The rules
+ * intersect.  S1/S2 here are the lengths of the sequence the pair belongs to. */
+typedef enum { FABWD_MASK_NONE = 0, FABWD_MASK_CAUSAL = 1, FABWD_MASK_BAND = 2 } fabwd_mask;
+
+/* Device status bits (fabwd_read_device_status). */
+#define FABWD_DEV_TIMEOUT 0x1u     /* a bounded mbarrier wait gave up; outputs are not valid */
+#define FABWD_DEV_BAD_SEQLENS 0x2u /* cu_seqlens not non-decreasing from 0, or beyond T / max */
+
+typedef struct {
+  int32_t dtype;   /* fabwd_dtype */
+  int32_t layout;  /* fabwd_layout */
+  /* Sizes ([FAG] §一 notation).  BSND/BNSD: S1, S2 are the sequence lengths.  TND: B is the
+   * number of sequences, S1/S2 are max_seqlen_q/max_seqlen_kv (upper bounds of every
+   * sequence's length) and T1/T2 the total token counts.  S1 = 0 or S2 = 0 (and empty TND
+   * sequences) are accepted: no pair is visible, so dq = dk = dv = 0. */
+  int64_t B, S1, S2, N1, N2, D, Dv;
+  int64_t T1, T2;
+  /* Inputs: device pointers, io dtype, contiguous in the layout above, 16-byte aligned. */
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;
+  const void* attn_out;
+  const float* softmax_lse;      /* device, fp32, natural-log lse of the scaled scores */
+  const int32_t* cu_seqlens_q;   /* device, B+1 entries, TND only (NULL otherwise) */
+  const int32_t* cu_seqlens_kv;  /* device, B+1 entries, TND only (NULL otherwise) */
+  double softmax_scale;          /* 0 -> 1/sqrt(D) ([FAG] §一 scale rule) */
+  int32_t mask_mode;             /* fabwd_mask */
+  int32_t reserved0;
+  int64_t win_left, win_right;   /* -1 = unbounded */
+  /* Outputs: device pointers, caller-allocated, shapes of q/k/v, io dtype ([FAG] §2.2). */
+  void* dq;
+  void* dk;
+  void* dv;
+} fabwd_params;
+
+/* Host only.  Validates p (the same checks as fabwd_run, pointers excepted) and returns in
+ * *bytes the workspace size fabwd_preprocess/fabwd_run need.  The workspace holds a status
+ * word, the fp32 sfmg and log2-scaled lse rows padded per (sequence, q-head) to a multiple of
+ * 128, and the fp32 dq accumulator (q's shape with D).  Errors: NULLPTR (p or bytes NULL),
+ * INVALID, UNSUPPORTED. */
+fabwd_status fabwd_workspace_size(const fabwd_params* p, size_t* bytes);
+
+/* Enqueue on `stream` (a cudaStream_t; NULL = the legacy default stream) the preprocess kernel
+ * ([FAG] §5.2 V1 softmaxGradFront): sfmg = rowsum(dout ⊙ attn_out) and lse·log2(e) into the
+ * workspace, the dq accumulator set to 0, the device status word cleared and the cu_seqlens
+ * checked.  Errors: NULLPTR, INVALID, UNSUPPORTED, WORKSPACE, CUDA (launch failure). */
+fabwd_status fabwd_preprocess(const fabwd_params* p, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* Enqueue on `stream` the main backward kernel (dK, dV written to dk/dv; dQ partial sums
+ * added into the workspace accumulator) and the convert kernel (dq = scale · accumulator, cast
+ * to the io dtype).  Must follow fabwd_preprocess with the same p and workspace on the same
+ * stream.  Errors: as fabwd_preprocess.  A TIMEOUT or bad-seqlens condition found on the
+ * device shows up in fabwd_read_device_status, not here. */
+fabwd_status fabwd_run(const fabwd_params* p, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* Synchronising read of the device status word: enqueues a 4-byte device-to-host copy on
+ * `stream`, waits for the stream, and stores the FABWD_DEV_* bits in *device_status.  Returns
+ * OK when the bits are 0, TIMEOUT when FABWD_DEV_TIMEOUT is set, DEVICE for any other bit,
+ * CUDA when the copy or the wait fails, NULLPTR/WORKSPACE for bad arguments. */
+fabwd_status fabwd_read_device_status(const void* workspace, size_t workspace_bytes, void* stream,
+                                      uint32_t* device_status);
+
+/* Bounded-wait limit in nanoseconds used by the kernels' mbarrier waits (default 2e9).  A value
+ * of 0 restores the default.  Returns the previous value.  Process-wide, not thread-safe. */
+uint64_t fabwd_set_wait_limit_ns(uint64_t ns);
+
+/* Fault-injection switch for tests of the failure path: when non-zero, the next fabwd_run
+ * launches its main kernel so that every CTA first waits on an mbarrier that nothing signals.
+ * The wait gives up after the wait limit, the CTA records FABWD_DEV_TIMEOUT, frees its tensor
+ * memory and returns.  The switch resets itself after one fabwd_run.  Returns the old value. */
+int fabwd_debug_inject_timeout(int on);
+
+/* Host only.  Byte offsets inside the workspace of the fp32 sfmg rows, the fp32 lse·log2(e)
+ * rows (both [B][N1][row_stride], row_stride = S1 rounded up to 128; for TND, B counts sequences
+ * and rows are sequence-local) and the fp32 dq accumulator (q's layout with D).  Lets callers
+ * inspect the intermediate sfmg (the V1 output of [FAG] §5.2).  Errors as fabwd_workspace_size. */
+fabwd_status fabwd_workspace_layout(const fabwd_params* p, size_t* off_sfmg, size_t* off_lse2,
+                                    size_t* off_dq_accum, int64_t* row_stride);
+
+/* Static description of a status code. */
+const char* fabwd_status_string(fabwd_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fabwd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FABWD_H */
