@@ -192,7 +192,7 @@ fabwd_status fabwd_preprocess(const fabwd_params* p, void* ws, size_t ws_bytes, 
   return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
 }
 
-fabwd_status fabwd_run(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
+fabwd_status fabwd_run_main(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
   Plan pl;
   fabwd_status s = plan_and_check(p, &pl, true);
   if (s != FABWD_OK) return s;
@@ -243,18 +243,33 @@ fabwd_status fabwd_run(const fabwd_params* p, void* ws, size_t ws_bytes, void* s
                          : launch_main_bf16(a, maps, (int)p->D, (int)p->Dv, grid_x, st);
     if (e != cudaSuccess) return FABWD_ERR_CUDA;
   } else if (pl.rowsK > 0) {
-    // no visible pair at all: dk = dv = 0 (the convert kernel below writes dq = 0)
+    // no visible pair at all: dk = dv = 0 (the convert kernel writes dq = 0)
     if (launch_zero(p->dk, pl.rowsK * p->N2 * p->D * 2, st) != cudaSuccess ||
         launch_zero(p->dv, pl.rowsK * p->N2 * p->Dv * 2, st) != cudaSuccess)
       return FABWD_ERR_CUDA;
   }
+  return FABWD_OK;
+}
+
+fabwd_status fabwd_run_convert(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
+  Plan pl;
+  fabwd_status s = plan_and_check(p, &pl, true);
+  if (s != FABWD_OK) return s;
+  if ((s = check_ws(pl, ws, ws_bytes)) != FABWD_OK) return s;
+  uint8_t* w = static_cast<uint8_t*>(ws);
   ConvArgs c;
   c.dq_acc = reinterpret_cast<const float*>(w + pl.off_dqacc);
   c.dq = p->dq;
   c.elems = pl.dq_elems;
   c.scale = (float)pl.scale;
-  cudaError_t e = launch_convert(c, fp16, st);
+  cudaError_t e = launch_convert(c, p->dtype == FABWD_FP16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
+}
+
+fabwd_status fabwd_run(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
+  fabwd_status s = fabwd_run_main(p, ws, ws_bytes, stream);
+  if (s != FABWD_OK) return s;
+  return fabwd_run_convert(p, ws, ws_bytes, stream);
 }
 
 fabwd_status fabwd_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32_t* device_status) {

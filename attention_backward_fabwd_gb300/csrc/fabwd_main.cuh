@@ -1,23 +1,32 @@
-// Main FlashAttention backward kernel for sm_103a (tcgen05 + TMEM + TMA).
+// Main FlashAttention backward kernel for sm_103a: warp-specialised tcgen05 + TMEM + TMA.
 //
 // What it computes is the backward of the page "CANN ops-transformer FlashAttnGrad 算子详解"
-// (discosf.com/news/4863418), §一: per kv-block of 128 keys of kv-head n2, over the G q-heads of
-// the group and the q-blocks that can see the block,
-//     Sᵀ  = K·Qᵀ               (tcgen05, M=128 keys, N=128 queries, K=D)
-//     dPᵀ = V·dOᵀ              (tcgen05, K=Dv)
-//     Pᵀ  = exp2(Sᵀ·scale·log2e − lse·log2e), masked pairs -> 0          (registers)
-//     dSᵀ = Pᵀ ⊙ (dPᵀ − sfmg)                                            (registers)
-//     dV += Pᵀ·dO,  dK += dSᵀ·Q  (TMEM accumulators, summed over q-blocks and the G heads)
-//     dQ_partial = dS·K  -> added in fp32 into the workspace accumulator (red.global.add)
-// The five products are §5.2's MM2, MM1, MM5, MM4, MM3; P/dS are its V2-V4 stages.  Unlike the
-// page's Ascend design, K serves as both a K-major (for Sᵀ) and an MN-major (for dQ) operand
-// from one shared-memory copy by descriptor choice, and dSᵀ likewise serves dK and dQ.
+// (discosf.com/news/4863418), §一.  One CTA owns a block of 128 keys of one kv-head and loops
+// over the G q-heads of the group and the 128-row q-blocks that can see the block:
+//     Sᵀ  = K·Qᵀ                 tcgen05 (M = 128 keys, N = 128 queries, K = D)
+//     dPᵀ = V·dOᵀ                tcgen05 (K = Dv)
+//     Pᵀ  = exp2(Sᵀ·scale·log2e − lse·log2e), masked pairs -> 0, written back to TMEM (bf16/fp16)
+//     dSᵀ = Pᵀ ⊙ (dPᵀ − sfmg)    -> shared memory (bf16/fp16)
+//     dV += Pᵀ·dO                tcgen05, A operand read from TMEM
+//     dK += dSᵀ·Q                tcgen05, accumulated over q-blocks and the G q-heads
+//     dQᵀ = Kᵀ·dSᵀ               tcgen05, M = 128 head-dim rows -> fp32 reduce-add into the
+//                                workspace accumulator, one coalesced 128-byte line per warp
+// The five products are §5.2's MM2, MM1, MM5, MM4, MM3 and the elementwise steps its V2-V4.
+// K is used K-major (Sᵀ) and MN-major (dQᵀ) from one shared-memory copy, Q and dO likewise
+// serve two products each, and dSᵀ serves dK (K-major) and dQᵀ (MN-major): the layout choices
+// are descriptor bits, not copies.
 //
-// Shared-memory tiles are 128-byte-swizzled [64-element column block][rows][64] arrays, the
-// layout TMA's SWIZZLE_128B writes for a {64, 1, rows, 1} box.
+// Warp roles (320 threads): warps 0-7 compute (warp w reads TMEM lanes 32·(w%4)..+31; warps
+// 0-3 take query columns 0-63 and warps 4-7 columns 64-127), warp 8 issues TMA loads (K, V once;
+// Q, dO, lse, sfmg double-buffered), warp 9 allocates TMEM and issues the MMAs.
 //
-// Every mbarrier wait is bounded (MainArgs::wait_ns); on give-up the CTA records
-// FABWD_DEV_TIMEOUT, drains what it has in flight (bounded as well), frees TMEM and returns.
+// TMEM columns: dK [0, D), dV [D, D+Dv), Sᵀ/Pᵀ [D+Dv, +128), dPᵀ/dQᵀ [D+Dv+128, +128).
+// Shared memory: K (padded to 128 head-dim columns), V, 2×Q, 2×dO, dSᵀ, 2×lse, 2×sfmg.  Tiles
+// are 128-byte-swizzled [64-column block][rows][64] arrays (TMA SWIZZLE_128B, box {64,1,rows,1}).
+//
+// Every mbarrier wait is bounded (MainArgs::wait_ns).  A wait that gives up sets a CTA abort
+// flag and FABWD_DEV_TIMEOUT; the other roles see the flag and leave their loops, the MMA
+// issuer drains its MMAs, TMA loads in flight get a bounded grace period, and TMEM is freed.
 #pragma once
 
 #include "fabwd_internal.cuh"
@@ -26,30 +35,31 @@
 
 namespace fabwd {
 
-constexpr unsigned long long kDrainNs = 200ull * 1000ull * 1000ull;  // 200 ms
+constexpr unsigned long long kDrainNs = 100ull * 1000ull * 1000ull;  // 100 ms
+constexpr unsigned long long kGraceNs = 2ull * 1000ull * 1000ull;    // 2 ms
+constexpr int kMainThreads = 320;
 
 template <int D, int DV>
-struct MainSmem {
+struct MainCfg {
   static constexpr int BR = kBlockQ, BC = kBlockKV;
-  static constexpr uint32_t oK = 0;
-  static constexpr uint32_t oV = oK + D * BC * 2;
-  static constexpr uint32_t oQ = oV + DV * BC * 2;
-  static constexpr uint32_t odO = oQ + D * BR * 2;
-  static constexpr uint32_t oP = odO + DV * BR * 2;
-  static constexpr uint32_t odS = oP + BC * BR * 2;
-  static constexpr uint32_t oL = odS + BC * BR * 2;
-  static constexpr uint32_t oF = oL + BR * 4;
-  static constexpr uint32_t oBar = oF + BR * 4;
-  static constexpr uint32_t oTm = oBar + 64;
-  static constexpr uint32_t bytes = oTm + 64 + 1024;  // + alignment slack
-  // TMEM columns (fp32 accumulators, lane = row)
-  static constexpr uint32_t cDK = 0;
-  static constexpr uint32_t cDV = D;
-  static constexpr uint32_t cS = D + DV;
-  static constexpr uint32_t cP = cS + BR;
-  static constexpr uint32_t cDQ = (cP + BR + D <= 512) ? cP + BR : cS;  // alias Sᵀ when full
+  static constexpr int DK = D < 128 ? 128 : D;  // K rows padded so dQᵀ = Kᵀ·dSᵀ has M = 128
+  static constexpr uint32_t kK = DK * BC * 2, kV = DV * BC * 2, kQ = D * BR * 2, kdO = DV * BR * 2;
+  static constexpr uint32_t kdS = BC * BR * 2;
+  static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + 2 * kQ, odS = odO + 2 * kdO;
+  static constexpr uint32_t oL = odS + kdS;          // [2][BR] fp32 lse·log2(e)
+  static constexpr uint32_t oF = oL + 2 * BR * 4;    // [2][BR] fp32 sfmg
+  static constexpr uint32_t oBar = oF + 2 * BR * 4;  // mbarriers
+  static constexpr uint32_t oMisc = oBar + 32 * 8;   // TMEM base holder, abort flag
+  static constexpr uint32_t bytes = oMisc + 64;
+  static constexpr uint32_t cDK = 0, cDV = D, cS = D + DV, cP = cS + BR;
+  static_assert(D % 64 == 0 && DV % 64 == 0 && D <= 128 && DV <= 128, "head dims");
   static_assert(cP + BR <= 512, "TMEM budget");
-  static_assert(cS + D <= 512, "TMEM budget for dQ");
+  static_assert(bytes <= 232448, "shared memory budget");
+};
+
+enum Bar : int {
+  kKvFull = 0, kQFull0 = 1, kQFull1 = 2, kQEmpty0 = 3, kQEmpty1 = 4, kSFull = 5, kDpFull = 6, kPFull = 7,
+  kDsFull = 8, kDqFull = 9, kDqEmpty = 10, kAccDone = 11, kNever = 12, kDrain = 13, kNumBars = 14
 };
 
 struct SeqRange {
@@ -86,23 +96,48 @@ __device__ __forceinline__ void mask_bounds(const MainArgs& a, long long& lo, lo
   }
 }
 
+// Bounded wait shared by all roles: gives up on the CTA abort flag or after wait_ns.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, const MainArgs& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > a.wait_ns) {
+      *abort_flag = 1;
+      atomicOr(a.status, FABWD_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Warp-uniform variant: the warp proceeds only if every lane saw the phase complete.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              const MainArgs& a) {
+  const bool ok = wait_bar(bar, parity, abort_flag, a);
+  return __all_sync(0xffffffffu, ok);
+}
+
 template <int D, int DV, bool FP16>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const MainArgs a) {
-  using L = MainSmem<D, DV>;
-  constexpr int BR = L::BR, BC = L::BC;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using C = MainCfg<D, DV>;
+  constexpr int BR = C::BR, BC = C::BC;
+  extern __shared__ __align__(1024) uint8_t smem[];
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int jb = blockIdx.x, n2 = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int jb = blockIdx.x / a.N2, n2 = blockIdx.x % a.N2, b = blockIdx.y;
 
   SeqRange sq;
-  if (!seq_range(a, b, sq)) return;  // bad cu_seqlens: preprocess reports it
+  if (!seq_range(a, b, sq)) return;  // bad cu_seqlens: the preprocess kernel reports it
   const int j0 = jb * BC;
   if (j0 >= sq.L2) return;
+  if ((smem_u32(smem) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
+    if (tid == 0) atomicOr(a.status, FABWD_DEV_INTERNAL);
+    return;
+  }
   const int j1 = min(j0 + BC, sq.L2);
   const long long off = (long long)sq.L2 - sq.L1;
   long long lo, hi;
@@ -112,289 +147,307 @@ __global__ void __launch_bounds__(128, 1)
   if (ib < 0) ib = 0;
   if (ie > sq.L1 - 1) ie = sq.L1 - 1;
   const int qb_begin = ib <= ie ? (int)(ib / BR) : 0;
-  const int qb_end = ib <= ie ? (int)(ie / BR) + 1 : 0;
-  const bool has_work = qb_begin < qb_end;
+  const int nqb = ib <= ie ? (int)(ie / BR) + 1 - qb_begin : 0;
+  const int T = nqb * a.G;  // loop steps: (head in group, q-block)
 
-  uint8_t* sK = smem + L::oK;
-  uint8_t* sV = smem + L::oV;
-  uint8_t* sQ = smem + L::oQ;
-  uint8_t* sdO = smem + L::odO;
-  float* sL = reinterpret_cast<float*>(smem + L::oL);
-  float* sF = reinterpret_cast<float*>(smem + L::oF);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::oBar);
-  uint64_t* kv_bar = bars + 0;
-  uint64_t* q_bar = bars + 1;
-  uint64_t* mma_bar = bars + 2;
-  uint64_t* never_bar = bars + 3;
-  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + L::oTm);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBar);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::oMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oMisc + 16);
 
   if (tid == 0) {
-    mbar_init(kv_bar, 1);
-    mbar_init(q_bar, 1);
-    mbar_init(mma_bar, 1);
-    mbar_init(never_bar, 1);
+    mbar_init(&bars[kKvFull], 1);
+    mbar_init(&bars[kQFull0], 1);
+    mbar_init(&bars[kQFull1], 1);
+    mbar_init(&bars[kQEmpty0], 1);
+    mbar_init(&bars[kQEmpty1], 1);
+    mbar_init(&bars[kSFull], 1);
+    mbar_init(&bars[kDpFull], 1);
+    mbar_init(&bars[kPFull], 8);
+    mbar_init(&bars[kDsFull], 8);
+    mbar_init(&bars[kDqFull], 1);
+    mbar_init(&bars[kDqEmpty], 8);
+    mbar_init(&bars[kAccDone], 1);
+    mbar_init(&bars[kNever], 1);
+    mbar_init(&bars[kDrain], 1);
+    *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (warp == 8 && lane == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_do);
   }
+  if (D < C::DK && warp < 8) {  // zero the K padding columns (read by the dQᵀ product only)
+    uint4* z = reinterpret_cast<uint4*>(smem + C::oK + (D / 64) * BC * 128);
+    const int n16 = (C::DK - D) / 64 * BC * 128 / 16;
+    for (int x = tid; x < n16; x += 256) z[x] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   __syncwarp();
-  if (warp == 0) tmem_alloc(tm_holder, 512);
+  if (warp == 9) tmem_alloc(tm_holder, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tm_holder;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
 
-  const int kv_row0 = a.layout == kTND ? sq.k0 + j0 : j0;
-  const int q_rowbase = a.layout == kTND ? sq.q0 : 0;
-  const int bcoord = a.layout == kTND ? 0 : b;
-  const bool bnsd = a.layout == kBNSD;  // BNSD maps order their coordinates (d, row, head, batch)
-
-  bool failed = false;
-  bool kv_pending = false, q_pending = false, mma_pending = false;
-  uint32_t q_parity = 0, mma_parity = 0;
-
-  if (a.inject_timeout) {
-    const bool ok = mbar_wait(never_bar, 0, a.wait_ns);
-    failed = __syncthreads_or(!ok);
+  if (a.inject_timeout) {  // fault injection for tests: a wait that nothing completes
+    if (lane == 0) wait_bar(&bars[kNever], 0, abort_flag, a);
+    __syncwarp();
   }
+  __syncthreads();
 
-  if (!failed && has_work) {
-    if (tid == 0) {
-      mbar_arrive_expect_tx(kv_bar, (D + DV) * BC * 2);
+  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
+  const int kv_row0 = tnd ? sq.k0 + j0 : j0;
+  const int q_rowbase = tnd ? sq.q0 : 0;
+  const int bcoord = tnd ? 0 : b;
+  constexpr bool kBF16 = !FP16;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && T > 0 && !*abort_flag) {
+      mbar_arrive_expect_tx(&bars[kKvFull], (D + DV) * BC * 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
-        tma_load_4d(sK + c * BC * 128, &tm_k, kv_bar, c * 64, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
+        tma_load_4d(smem + C::oK + c * BC * 128, &tm_k, &bars[kKvFull], c * 64, bnsd ? kv_row0 : n2,
+                    bnsd ? n2 : kv_row0, bcoord);
 #pragma unroll
       for (int c = 0; c < DV / 64; ++c)
-        tma_load_4d(sV + c * BC * 128, &tm_v, kv_bar, c * 64, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
-    }
-    kv_pending = true;
-    {
-      const bool ok = mbar_wait(kv_bar, 0, a.wait_ns);
-      failed = __syncthreads_or(!ok);
-      if (!failed) kv_pending = false;
-    }
-  }
-
-  // per-thread key row (lane of Sᵀ/dPᵀ/dK/dV) and its visible q-row interval
-  const int jr = j0 + tid;
-  const bool j_valid = jr < sq.L2;
-  long long vlo = (long long)jr - off - hi, vhi = (long long)jr - off - lo;
-  const int i_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
-  const int i_vis_hi = (int)(vhi < -1 ? -1 : (vhi > (1 << 30) ? (1 << 30) : vhi));
-
-  constexpr bool kBF16 = !FP16;
-  constexpr uint32_t ID_S = idesc_f16(BC, BR, kBF16, false, false);
-  constexpr uint32_t ID_DV = idesc_f16(BC, DV, kBF16, false, true);
-  constexpr uint32_t ID_DK = idesc_f16(BC, D, kBF16, false, true);
-  constexpr uint32_t ID_DQ = idesc_f16(BR, D, kBF16, true, true);
-
-  const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
-  const uint32_t aP = smem_u32(smem + L::oP), adS = smem_u32(smem + L::odS);
-
-  bool any_acc = false;  // dK/dV accumulators hold data
-  for (int h = 0; h < a.G && !failed && has_work; ++h) {
-    const int n1 = n2 * a.G + h;
-    const float* lse2_row = a.lse2 + ((long long)b * a.N1 + n1) * a.S1p;
-    const float* sfmg_row = a.sfmg + ((long long)b * a.N1 + n1) * a.S1p;
-    for (int qb = qb_begin; qb < qb_end && !failed; ++qb) {
-      const int i0 = qb * BR;
-      // ---- load Q, dO, lse2, sfmg tiles
-      if (tid == 0) {
-        mbar_arrive_expect_tx(q_bar, (D + DV) * BR * 2 + 2 * BR * 4);
+        tma_load_4d(smem + C::oV + c * BC * 128, &tm_v, &bars[kKvFull], c * 64, bnsd ? kv_row0 : n2,
+                    bnsd ? n2 : kv_row0, bcoord);
+      for (int t = 0; t < T; ++t) {
+        const int s = t & 1;
+        const int h = t / nqb, qb = qb_begin + t % nqb;
+        const int n1 = n2 * a.G + h, i0 = qb * BR;
+        if (t >= 2 && !wait_bar(&bars[kQEmpty0 + s], ((t >> 1) - 1) & 1, abort_flag, a)) break;
+        uint64_t* full = &bars[kQFull0 + s];
+        mbar_arrive_expect_tx(full, (D + DV) * BR * 2 + 2 * BR * 4);
+        const int row = q_rowbase + i0;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sQ + c * BR * 128, &tm_q, q_bar, c * 64, bnsd ? q_rowbase + i0 : n1, bnsd ? n1 : q_rowbase + i0,
+          tma_load_4d(smem + C::oQ + s * C::kQ + c * BR * 128, &tm_q, full, c * 64, bnsd ? row : n1, bnsd ? n1 : row,
                       bcoord);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(sdO + c * BR * 128, &tm_do, q_bar, c * 64, bnsd ? q_rowbase + i0 : n1,
-                      bnsd ? n1 : q_rowbase + i0, bcoord);
-        bulk_load(sL, lse2_row + i0, BR * 4, q_bar);
-        bulk_load(sF, sfmg_row + i0, BR * 4, q_bar);
+          tma_load_4d(smem + C::odO + s * C::kdO + c * BR * 128, &tm_do, full, c * 64, bnsd ? row : n1,
+                      bnsd ? n1 : row, bcoord);
+        const long long rbase = ((long long)b * a.N1 + n1) * a.S1p + i0;
+        bulk_load(smem + C::oL + s * BR * 4, a.lse2 + rbase, BR * 4, full);
+        bulk_load(smem + C::oF + s * BR * 4, a.sfmg + rbase, BR * 4, full);
       }
-      q_pending = true;
-      {
-        const bool ok = mbar_wait(q_bar, q_parity, a.wait_ns);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        q_pending = false;
-        q_parity ^= 1;
-      }
-      // ---- Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
-      if (tid == 0) {
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t ID_S = idesc_f16(BC, BR, kBF16, false, false);
+      constexpr uint32_t ID_DV = idesc_f16(BC, DV, kBF16, false, true);
+      constexpr uint32_t ID_DK = idesc_f16(BC, D, kBF16, false, true);
+      constexpr uint32_t ID_DQ = idesc_f16(128, BR, kBF16, true, true);
+      const uint32_t aK = smem_u32(smem + C::oK), aV = smem_u32(smem + C::oV), adS = smem_u32(smem + C::odS);
+      bool ok = wait_bar(&bars[kKvFull], 0, abort_flag, a);
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t & 1;
+        const uint32_t aQ = smem_u32(smem + C::oQ + s * C::kQ), adO = smem_u32(smem + C::odO + s * C::kdO);
+        if (!(ok = wait_bar(&bars[kQFull0 + s], (t >> 1) & 1, abort_flag, a))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(aQ + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + L::cS, ad, bd, ID_S, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::cS, sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(aQ + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+        mma_commit(&bars[kSFull]);
+        if (t > 0 && !(ok = wait_bar(&bars[kDqEmpty], (t - 1) & 1, abort_flag, a))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(aV + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(adO + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + L::cP, ad, bd, ID_S, kk > 0);
-        }
-        mma_commit(mma_bar);
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_ss(tmem + C::cP, sdesc_sw128(aV + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(adO + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+        mma_commit(&bars[kDpFull]);
+        if (!(ok = wait_bar(&bars[kPFull], t & 1, abort_flag, a))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BR / 16; ++kk)  // Pᵀ columns: queries 0-63 at +0, 64-127 at +64
+          mma_ts(tmem + C::cDV, tmem + C::cS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                 sdesc_sw128(adO + kk * 2048, BR * 128, 1024), ID_DV, (t > 0 || kk > 0) ? 1u : 0u);
+        if (!(ok = wait_bar(&bars[kDsFull], t & 1, abort_flag, a))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BR / 16; ++kk)
+          mma_ss(tmem + C::cDK, sdesc_sw128(adS + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < BC / 16; ++kk)
+          mma_ss(tmem + C::cP, sdesc_sw128(aK + kk * 2048, BC * 128, 1024), sdesc_sw128(adS + kk * 2048, BC * 128, 1024),
+                 ID_DQ, kk > 0);
+        mma_commit(&bars[kDqFull]);
+        mma_commit(&bars[kQEmpty0 + s]);
       }
-      mma_pending = true;
-      {
-        const bool ok = mbar_wait(mma_bar, mma_parity, a.wait_ns);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        mma_pending = false;
-        mma_parity ^= 1;
+      if (ok) {
+        mma_commit(&bars[kAccDone]);
+      } else {
+        mma_commit(&bars[kDrain]);
+        mbar_wait(&bars[kDrain], 0, kDrainNs);
       }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ compute warps 0-7
+    const int q4 = warp & 3, wg = warp >> 2;
+    const int row = q4 * 32 + lane;  // TMEM lane: key row (Sᵀ, dPᵀ, dK, dV) or head-dim row (dQᵀ)
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int jr = j0 + row;
+    const bool j_valid = jr < sq.L2;
+    const long long vlo = (long long)jr - off - hi, vhi = (long long)jr - off - lo;
+    const int i_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
+    const int i_vis_hi = (int)(vhi < -1 ? -1 : (vhi > (1 << 30) ? (1 << 30) : vhi));
+    const uint32_t adS = smem_u32(smem + C::odS) + wg * BC * 128 + row * 128;
+    const long long i_stride = bnsd ? D : (long long)a.N1 * D;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int s = t & 1;
+      const int h = t / nqb, qb = qb_begin + t % nqb;
+      const int n1 = n2 * a.G + h, i0 = qb * BR;
+      const int ic0 = i0 + wg * 64;  // first query of this warp's 64 columns
+      if (!(ok = wait_bar_warp(&bars[kQFull0 + s], (t >> 1) & 1, abort_flag, a))) break;
+      if (!(ok = wait_bar_warp(&bars[kSFull], t & 1, abort_flag, a))) break;
       tc_fence_after();
-      // ---- Pᵀ and dSᵀ rows (thread = key row), written as 128B-swizzled K-major tiles
+      const float* sL = reinterpret_cast<const float*>(smem + C::oL + s * BR * 4) + wg * 64;
+      const float* sF = reinterpret_cast<const float*>(smem + C::oF + s * BR * 4) + wg * 64;
+      const long long dmin = (long long)j0 - (i0 + BR - 1) - off, dmax = (long long)(j1 - 1) - i0 - off;
+      const bool full = dmin >= lo && dmax <= hi;
+      float p[64];
       {
-        const long long dmin = (long long)j0 - (i0 + BR - 1) - off, dmax = (long long)(j1 - 1) - i0 - off;
-        const bool full = dmin >= lo && dmax <= hi;
-#pragma unroll 1
-        for (int c = 0; c < BR / 32; ++c) {
-          uint32_t sr[32], pr[32];
-          tmem_ld32(tmem + lane_off + L::cS + c * 32, sr);
-          tmem_ld32(tmem + lane_off + L::cP + c * 32, pr);
-          tmem_wait_ld();
-          reg_fence(sr);
-          reg_fence(pr);
-          uint32_t pp[16], dd[16];
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lane_off + C::cS + wg * 64, r0);
+        tmem_ld32(tmem + lane_off + C::cS + wg * 64 + 32, r1);
+        tmem_wait_ld();
+        reg_fence(r0);
+        reg_fence(r1);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int col = c * 32 + e;
-            float p0 = ex2(fmaf(__uint_as_float(sr[e]), a.scale_log2, -sL[col]));
-            float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), a.scale_log2, -sL[col + 1]));
-            if (!full) {
-              const int i = i0 + col;
-              if (i < i_vis_lo || i > i_vis_hi) p0 = 0.f;
-              if (i + 1 < i_vis_lo || i + 1 > i_vis_hi) p1 = 0.f;
-            }
-            if (!j_valid) p0 = p1 = 0.f;
-            const float d0 = p0 * (__uint_as_float(pr[e]) - sF[col]);
-            const float d1 = p1 * (__uint_as_float(pr[e + 1]) - sF[col + 1]);
-            pp[e >> 1] = pack2<FP16>(p0, p1);
-            dd[e >> 1] = pack2<FP16>(d0, d1);
-          }
-          const uint32_t chunk = (c * 32) >> 6, u0 = ((c * 32) & 63) >> 3;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t rowoff = chunk * BC * 128 + tid * 128 + (((u0 + q) ^ (tid & 7)) << 4);
-            st_shared_v4(aP + rowoff, pp[4 * q], pp[4 * q + 1], pp[4 * q + 2], pp[4 * q + 3]);
-            st_shared_v4(adS + rowoff, dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
-          }
+        for (int c = 0; c < 32; ++c) {
+          p[c] = ex2(fmaf(__uint_as_float(r0[c]), a.scale_log2, -sL[c]));
+          p[c + 32] = ex2(fmaf(__uint_as_float(r1[c]), a.scale_log2, -sL[c + 32]));
         }
+      }
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (ic0 + c < i_vis_lo || ic0 + c > i_vis_hi) p[c] = 0.f;
+      }
+      if (!j_valid) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = 0.f;
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack2<FP16>(p[2 * c], p[2 * c + 1]);
+        tmem_st32(tmem + lane_off + C::cS + wg * 64, pk);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kPFull]);
+      if (!(ok = wait_bar_warp(&bars[kDpFull], t & 1, abort_flag, a))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cP + wg * 64 + hh * 32, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t dk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float d0 = p[hh * 32 + c] * (__uint_as_float(r[c]) - sF[hh * 32 + c]);
+          const float d1 = p[hh * 32 + c + 1] * (__uint_as_float(r[c + 1]) - sF[hh * 32 + c + 1]);
+          dk[c >> 1] = pack2<FP16>(d0, d1);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(adS + ((((hh * 4 + u) ^ (row & 7))) << 4), dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
       }
       fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      // ---- dV += Pᵀ dO, dK += dSᵀ Q, dQ = dS K
-      if (tid == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BR / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(aP + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(adO + kk * 2048, BR * 128, 1024);
-          mma_ss(tmem + L::cDV, ad, bd, ID_DV, (any_acc || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < BR / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(adS + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(aQ + kk * 2048, BR * 128, 1024);
-          mma_ss(tmem + L::cDK, ad, bd, ID_DK, (any_acc || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(adS + kk * 2048, BC * 128, 1024);
-          const uint64_t bd = sdesc_sw128(aK + kk * 2048, BC * 128, 1024);
-          mma_ss(tmem + L::cDQ, ad, bd, ID_DQ, kk > 0);
-        }
-        mma_commit(mma_bar);
-      }
-      any_acc = true;
-      mma_pending = true;
-      {
-        const bool ok = mbar_wait(mma_bar, mma_parity, a.wait_ns);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        mma_pending = false;
-        mma_parity ^= 1;
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kDsFull]);
+      if (!(ok = wait_bar_warp(&bars[kDqFull], t & 1, abort_flag, a))) break;
       tc_fence_after();
-      // ---- dQ partial (thread = q row) -> fp32 accumulator
       {
-        const int ir = i0 + tid;
-        const bool i_valid = ir < sq.L1;
-        float* dst = a.dq_acc + row_index(a.layout, b, (long long)q_rowbase + (i_valid ? ir : 0), n1, a.N1, a.S1) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + L::cDQ + c * 32, r);
-          tmem_wait_ld();
-          reg_fence(r);
-          if (i_valid) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lane_off + C::cP + wg * 64, r0);
+        tmem_ld32(tmem + lane_off + C::cP + wg * 64 + 32, r1);
+        tmem_wait_ld();
+        reg_fence(r0);
+        reg_fence(r1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kDqEmpty]);
+        if (row < D) {  // lane = head-dim index d; columns = queries ic0 .. ic0 + 63
+          const int nvalid = min(64, sq.L1 - ic0);
+          float* dst = a.dq_acc +
+                       row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? ic0 : 0), n1, a.N1, a.S1) * D + row;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              red_add_v4(dst + c * 32 + e, __uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                         __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-          }
+          for (int c = 0; c < 32; ++c)
+            if (c < nvalid) red_add_f32(dst + c * i_stride, __uint_as_float(r0[c]));
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c + 32 < nvalid) red_add_f32(dst + (c + 32) * i_stride, __uint_as_float(r1[c]));
         }
       }
-      tc_fence_before();
-      __syncthreads();
+    }
+    // ---- epilogue: dK = scale · acc, dV = acc; zeros when no query sees this block
+    if (ok && T > 0) ok = wait_bar_warp(&bars[kAccDone], 0, abort_flag, a);
+    if (ok) {
+      tc_fence_after();
+      const long long krow = row_index(a.layout, b, (long long)(tnd ? sq.k0 : 0) + (j_valid ? jr : 0), n2, a.N2, a.S2);
+      uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * D;
+      uint16_t* dv = static_cast<uint16_t*>(a.dv) + krow * DV;
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = wg * (D / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cDK + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * a.scale, __uint_as_float(r[e + 1]) * a.scale) : 0u;
+        if (j_valid) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(dk + col + u * 8) = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < DV / 64; ++c) {
+        const int col = wg * (DV / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cDV + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]), __uint_as_float(r[e + 1])) : 0u;
+        if (j_valid) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(dv + col + u * 8) = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        }
+      }
     }
   }
 
-  if (!failed) {
-    // ---- epilogue: dK = scale · acc, dV = acc (zeros when no q row sees this block).
-    // The TMEM loads are warp-collective: every thread loads, only valid rows store.
-    const long long krow =
-        row_index(a.layout, b, (long long)(a.layout == kTND ? sq.k0 : 0) + (j_valid ? jr : 0), n2, a.N2, a.S2);
-    uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * D;
-    uint16_t* dv = static_cast<uint16_t*>(a.dv) + krow * DV;
-#pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_off + L::cDK + c * 32, r);
-      tmem_wait_ld();
-      reg_fence(r);
-      uint32_t o[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2)
-        o[e >> 1] = any_acc ? pack2<FP16>(__uint_as_float(r[e]) * a.scale, __uint_as_float(r[e + 1]) * a.scale) : 0u;
-      if (j_valid) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(dk + c * 32 + q * 8) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-      }
-    }
-#pragma unroll 1
-    for (int c = 0; c < DV / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_off + L::cDV + c * 32, r);
-      tmem_wait_ld();
-      reg_fence(r);
-      uint32_t o[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2)
-        o[e >> 1] = any_acc ? pack2<FP16>(__uint_as_float(r[e]), __uint_as_float(r[e + 1])) : 0u;
-      if (j_valid) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(dv + c * 32 + q * 8) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-      }
-    }
-  } else {
-    if (tid == 0) {
-      atomicOr(a.status, FABWD_DEV_TIMEOUT);
-      if (kv_pending) mbar_wait(kv_bar, 0, kDrainNs);
-      if (q_pending) mbar_wait(q_bar, q_parity, kDrainNs);
-      if (mma_pending) mbar_wait(mma_bar, mma_parity, kDrainNs);
-    }
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (*abort_flag && tid == 0) {  // bounded grace period for TMA loads still in flight
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kGraceNs) {
+    }
+  }
+  __syncthreads();
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -402,24 +455,27 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 template <int D, int DV, bool FP16>
-cudaError_t launch_main_t(const MainArgs& a, const MainMaps& m, int grid_x, cudaStream_t st) {
-  using L = MainSmem<D, DV>;
+cudaError_t launch_main_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
+  using C = MainCfg<D, DV>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fabwd_main_kernel<D, DV, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L::bytes);
+                                         (int)C::bytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(grid_x, a.N2, a.B);
-  fabwd_main_kernel<D, DV, FP16><<<grid, 128, L::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
+  // blockIdx.x = kv-block * N2 + kv-head: the heaviest kv-blocks (earliest keys under a causal
+  // mask) of every head launch first.
+  dim3 grid(n_kv_blocks * a.N2, a.B);
+  fabwd_main_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
   return cudaGetLastError();
 }
 
 template <bool FP16>
-cudaError_t launch_main_dispatch(const MainArgs& a, const MainMaps& m, int D, int Dv, int grid_x, cudaStream_t st) {
-  if (D == 64 && Dv == 64) return launch_main_t<64, 64, FP16>(a, m, grid_x, st);
-  if (D == 128 && Dv == 128) return launch_main_t<128, 128, FP16>(a, m, grid_x, st);
+cudaError_t launch_main_dispatch(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks,
+                                 cudaStream_t st) {
+  if (D == 64 && Dv == 64) return launch_main_t<64, 64, FP16>(a, m, n_kv_blocks, st);
+  if (D == 128 && Dv == 128) return launch_main_t<128, 128, FP16>(a, m, n_kv_blocks, st);
   return cudaErrorInvalidValue;
 }
 

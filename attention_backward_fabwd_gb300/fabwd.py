@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
                                              ctypes.POINTER(ctypes.c_int64)]
         L.fabwd_preprocess.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
+        L.fabwd_run_main.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
+        L.fabwd_run_convert.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_read_device_status.argtypes = [ctypes.c_void_p, sz, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
         L.fabwd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.fabwd_set_wait_limit_ns.restype = ctypes.c_uint64
@@ -72,7 +74,7 @@ def lib() -> ctypes.CDLL:
         L.fabwd_status_string.argtypes = [ctypes.c_int]
         L.fabwd_status_string.restype = ctypes.c_char_p
         for f in ("fabwd_workspace_size", "fabwd_workspace_layout", "fabwd_preprocess", "fabwd_run",
-                  "fabwd_read_device_status"):
+                  "fabwd_run_main", "fabwd_run_convert", "fabwd_read_device_status"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -116,6 +118,18 @@ def fabwd_run(p: fabwd_params, workspace: int, workspace_bytes: int, stream: int
     s = lib().fabwd_run(ctypes.byref(p), workspace, workspace_bytes, stream)
     if s != FABWD_OK:
         raise FabwdError(s, "fabwd_run")
+
+
+def fabwd_run_main(p: fabwd_params, workspace: int, workspace_bytes: int, stream: int) -> None:
+    s = lib().fabwd_run_main(ctypes.byref(p), workspace, workspace_bytes, stream)
+    if s != FABWD_OK:
+        raise FabwdError(s, "fabwd_run_main")
+
+
+def fabwd_run_convert(p: fabwd_params, workspace: int, workspace_bytes: int, stream: int) -> None:
+    s = lib().fabwd_run_convert(ctypes.byref(p), workspace, workspace_bytes, stream)
+    if s != FABWD_OK:
+        raise FabwdError(s, "fabwd_run_convert")
 
 
 def fabwd_read_device_status(workspace: int, workspace_bytes: int, stream: int):

@@ -1,0 +1,576 @@
+#!/usr/bin/env python
+"""Benchmark: attention-backward TFLOP/s (bf16) on one GB300 and % of dense tensor peak.
+
+One step = one pass of the whole backward path over one batch of synthetic input:
+fabwd_preprocess (sfmg, lse rows, dq accumulator zeroing) -> fabwd_run_main (tcgen05 backward
+kernel) -> fabwd_run_convert (dq cast), all libfabwd kernels on one stream.
+
+Flops follow the measurement convention: per head 2·S1·S2·(3D + 2Dv), halved under a causal
+mask; the roofline uses the algorithmic count 2·(3D + 2Dv) per visible (query, key) pair.
+
+Inputs: q, k, v, dout are the seeded draws of attention_backward_fabwd_gb300.inputs; attn_out
+and softmax_lse come from a plain torch fp32 forward on the GPU (input synthesis, untimed).
+The L2 cache (129 MB) is flushed between timed steps by writing a 256 MB buffer (untimed).
+
+`--impl reference` times the fp64 CPU oracle instead (host cores, bounded sample per step).
+Multi-GPU (torchrun): each rank runs an independent replica (no collective on the data path);
+the step time is the max over ranks and the value counts all ranks' work (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "gqa_causal_s4096_d128"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["fabwd", "reference"], default="fabwd")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------------------------
+# work counts
+# ----------------------------------------------------------------------------------------------
+
+
+def seq_lengths(pb):
+    if pb.w.layout == "TND":
+        return list(zip(np.diff(pb.cu_seqlens_q).tolist(), np.diff(pb.cu_seqlens_kv).tolist()))
+    return [(pb.S1, pb.S2)] * pb.w.B
+
+
+def visible_pairs(L1, L2, w):
+    """Number of (i, j) pairs with lo <= j - i - (L2 - L1) <= hi, 0 <= j < L2 (per head)."""
+    if L1 == 0 or L2 == 0:
+        return 0
+    lo, hi = -(1 << 40), 1 << 40
+    if w.mask_mode != 0:
+        if w.win_left >= 0:
+            lo = -w.win_left
+        if w.win_right >= 0:
+            hi = w.win_right
+        if w.mask_mode == 1:
+            hi = min(hi, 0)
+    i = np.arange(L1, dtype=np.int64)
+    off = L2 - L1
+    jlo = np.clip(i + off + lo, 0, L2)
+    jhi = np.clip(i + off + hi + 1, 0, L2)
+    return int(np.maximum(jhi - jlo, 0).sum())
+
+
+def flop_counts(pb):
+    w = pb.w
+    per_pair = 2 * (3 * w.D + 2 * w.Dv)
+    conv = alg = 0
+    for L1, L2 in seq_lengths(pb):
+        f = per_pair * L1 * L2
+        conv += f / 2 if w.mask_mode == 1 else f
+        alg += per_pair * visible_pairs(L1, L2, w)
+    return conv * w.N1, alg * w.N1
+
+
+def io_bytes(pb):
+    e = 2
+    w = pb.w
+    qn = pb.q.numel()
+    kn, vn, on = pb.k.numel(), pb.v.numel(), pb.dout.numel()
+    lse = w.N1 * pb.T1 * 4
+    h2d = e * (qn + kn + vn + 2 * on) + lse
+    d2h = e * (qn + kn + vn)
+    return h2d, d2h
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------------
+
+
+def synth_forward(pb, dev):
+    """attn_out (io dtype) and fp32 lse by a plain torch fp32 forward on the GPU (input synthesis)."""
+    import torch
+
+    w = pb.w
+    scale = w.softmax_scale if w.softmax_scale != 0 else 1.0 / math.sqrt(w.D)
+    q, k, v = (t.to(dev) for t in (pb.q, pb.k, pb.v))
+    G = w.N1 // w.N2
+    y = torch.empty(pb.dout.shape, dtype=q.dtype, device=dev)
+    if w.layout == "TND":
+        lse = torch.empty(w.N1, pb.T1, dtype=torch.float32, device=dev)
+        seqs = [(None, slice(int(pb.cu_seqlens_q[s]), int(pb.cu_seqlens_q[s + 1])),
+                 slice(int(pb.cu_seqlens_kv[s]), int(pb.cu_seqlens_kv[s + 1]))) for s in range(w.B)]
+    else:
+        lse = torch.empty(w.B, w.N1, pb.S1, dtype=torch.float32, device=dev)
+        seqs = [(b, slice(0, pb.S1), slice(0, pb.S2)) for b in range(w.B)]
+
+    def head(x, b, rows, n):
+        if w.layout == "BSND":
+            return x[b, rows, n]
+        if w.layout == "BNSD":
+            return x[b, n, rows]
+        return x[rows, n]
+
+    for b, rq, rk in seqs:
+        L1, L2 = rq.stop - rq.start, rk.stop - rk.start
+        if L1 == 0:
+            continue
+        ii = torch.arange(L1, device=dev)[:, None]
+        jj = torch.arange(L2, device=dev)[None, :]
+        d = jj - ii - (L2 - L1)
+        ok = torch.ones(L1, L2, dtype=torch.bool, device=dev)
+        if w.mask_mode == 1:
+            ok &= d <= 0
+        if w.mask_mode != 0 and w.win_left >= 0:
+            ok &= d >= -w.win_left
+        if w.mask_mode != 0 and w.win_right >= 0:
+            ok &= d <= w.win_right
+        for n1 in range(w.N1):
+            n2 = n1 // G
+            qh = head(q, b, rq, n1).float()
+            s = (qh @ head(k, b, rk, n2).float().T) * scale
+            s = s.masked_fill(~ok, float("-inf"))
+            l = torch.logsumexp(s, dim=1)
+            l = torch.where(torch.isfinite(l), l, torch.full_like(l, float("inf")))
+            p = torch.exp(s - l[:, None]).masked_fill(~ok, 0.0)
+            yh = p @ head(v, b, rk, n2).float()
+            if w.layout == "BSND":
+                y[b, rq, n1] = yh.to(y.dtype)
+                lse[b, n1, rq] = l
+            elif w.layout == "BNSD":
+                y[b, n1, rq] = yh.to(y.dtype)
+                lse[b, n1, rq] = l
+            else:
+                y[rq, n1] = yh.to(y.dtype)
+                lse[n1, rq] = l
+    return y, lse
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        if self.bus_id:
+            mine = [r for r in rows if r[1].lower().endswith(self.bus_id.lower()[-12:])]
+            rows = mine or rows
+        ids = sorted(set(r[0] for r in rows))
+        if len(ids) > 1:
+            rows = [r for r in rows if r[0] == ids[0]]
+        try:
+            sm = [float(r[2]) for r in rows]
+            smax = max(float(r[3]) for r in rows)
+        except ValueError:
+            return None
+        loaded = [x for x in sm if x > 0.5 * smax] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[6 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def profile_traffic(workload):
+    """dram bytes per main-kernel launch recorded from an ncu capture, if one is committed."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        v = d.get(workload)
+        if v and v.get("kernel_rev") == KERNEL_REV:
+            return v.get("dram_bytes_per_launch")
+    return None
+
+
+KERNEL_REV = "main-v1"
+
+
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise max of per-rank timings (every rank gets the result)."""
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+def job_tflops(flops_per_rank, world, ms):
+    """Whole-job throughput: every rank processed flops_per_rank in at most ms milliseconds."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
+def replica_workload(w, rank):
+    """Each rank draws its own batch of the same shape (independent replicas, weak scaling)."""
+    from attention_backward_fabwd_gb300 import inputs
+
+    return inputs.sized(w, seed=w.seed + 7919 * rank)
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    from attention_backward_fabwd_gb300 import api, build, fabwd, inputs
+
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = inputs.WORKLOADS[args.workload]
+    w = replica_workload(w, rank)
+    pb = inputs.make_problem(w)
+    attn_out, lse = synth_forward(pb, dev)
+    q, k, v, dout = (t.to(dev) for t in (pb.q, pb.k, pb.v, pb.dout))
+    cu_q = cu_kv = None
+    extra = {}
+    if w.layout == "TND":
+        cu_q = torch.from_numpy(pb.cu_seqlens_q).to(dev)
+        cu_kv = torch.from_numpy(pb.cu_seqlens_kv).to(dev)
+        extra = dict(max_seqlen_q=pb.S1, max_seqlen_kv=pb.S2)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    p = api.make_params(q, k, v, dout, attn_out, lse, dq, dk, dv, cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv,
+                        softmax_scale=w.softmax_scale, mask_mode=w.mask_mode, win_left=w.win_left,
+                        win_right=w.win_right, layout=w.layout, **extra)
+    nbytes = fabwd.fabwd_workspace_size(p)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+    sp = st.cuda_stream
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(st)
+        fabwd.fabwd_preprocess(p, ws.data_ptr(), nbytes, sp)
+        if evs:
+            evs[1].record(st)
+        fabwd.fabwd_run_main(p, ws.data_ptr(), nbytes, sp)
+        if evs:
+            evs[2].record(st)
+        fabwd.fabwd_run_convert(p, ws.data_ptr(), nbytes, sp)
+        if evs:
+            evs[3].record(st)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1)
+        step()
+    s_, bits = fabwd.fabwd_read_device_status(ws.data_ptr(), nbytes, sp)
+    if s_ != fabwd.FABWD_OK:
+        raise RuntimeError(f"device status {bits:#x} after warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+        bus = f"{bus:02x}" if isinstance(bus, int) else str(bus)
+    except Exception:
+        bus = None
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall0 = time.perf_counter()
+    with ClockSampler() as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+    barrier()
+    t_wall = time.perf_counter() - t_wall0
+    pre = [e[0].elapsed_time(e[1]) for e in evs]
+    main = [e[1].elapsed_time(e[2]) for e in evs]
+    conv = [e[2].elapsed_time(e[3]) for e in evs]
+    tot = [e[0].elapsed_time(e[3]) for e in evs]
+    ms_step = statistics.mean(tot)
+    ms_main = statistics.mean(main)
+    s_, bits = fabwd.fabwd_read_device_status(ws.data_ptr(), nbytes, sp)
+    if s_ != fabwd.FABWD_OK:
+        raise RuntimeError(f"device status {bits:#x} after the timed steps")
+
+    # e2e: host buffers through the C ABI, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo, hy, hl = (t.cpu().pin_memory() for t in (q, k, v, dout, attn_out, lse))
+        ho = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+        h2d, d2h = io_bytes(pb)
+        e2e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(3, args.steps // 2))]
+        for i in range(len(e2e_evs) + 2):
+            flush.fill_(i & 0xFF)
+            ev = e2e_evs[i - 2] if i >= 2 else None
+            if ev:
+                ev[0].record(st)
+            for d_, h_ in ((q, hq), (k, hk), (v, hv), (dout, hdo), (attn_out, hy), (lse, hl)):
+                d_.copy_(h_, non_blocking=True)
+            fabwd.fabwd_preprocess(p, ws.data_ptr(), nbytes, sp)
+            fabwd.fabwd_run(p, ws.data_ptr(), nbytes, sp)
+            for h_, d_ in zip(ho, (dq, dk, dv)):
+                h_.copy_(d_, non_blocking=True)
+            if ev:
+                ev[1].record(st)
+        torch.cuda.synchronize(dev)
+        e2e_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in e2e_evs)
+        e2e = {"ms": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    ms_step, ms_main, ms_pre, ms_conv, e2e_ms, t_wall = max_over_ranks(
+        [ms_step, ms_main, statistics.mean(pre), statistics.mean(conv), e2e["ms"] if e2e else 0.0, t_wall], world, dev)
+    return dict(pb=pb, w=w, ms_step=ms_step, ms_main=ms_main, ms_pre=ms_pre, ms_conv=ms_conv, e2e=e2e, e2e_ms=e2e_ms,
+                t_wall=t_wall, clocks=clk.summary(), dq_elems=dq.numel(), nbytes=nbytes)
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU oracle (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------------------------
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_head_sampler(pb):
+    """Yields (seconds, flops_convention) of the fp64 oracle backward of one head at a time."""
+    from attention_backward_fabwd_gb300 import inputs
+    from oracle import fabwd_oracle as orc
+
+    w = pb.w
+    scale = orc.resolve_scale(w.softmax_scale, w.D)
+    G = w.N1 // w.N2
+    seqs = []
+    if w.layout == "TND":
+        for s in range(w.B):
+            seqs.append((None, slice(int(pb.cu_seqlens_q[s]), int(pb.cu_seqlens_q[s + 1])),
+                         slice(int(pb.cu_seqlens_kv[s]), int(pb.cu_seqlens_kv[s + 1]))))
+    else:
+        seqs = [(b, slice(0, pb.S1), slice(0, pb.S2)) for b in range(w.B)]
+
+    def head(x, b, rows, n):
+        if w.layout == "BSND":
+            return x[b, rows, n]
+        if w.layout == "BNSD":
+            return x[b, n, rows]
+        return x[rows, n]
+
+    units = [(sq, n1) for sq in seqs for n1 in range(w.N1)]
+    per_pair = 2 * (3 * w.D + 2 * w.Dv)
+    idx = 0
+    while True:
+        (b, rq, rk), n1 = units[idx % len(units)]
+        idx += 1
+        L1, L2 = rq.stop - rq.start, rk.stop - rk.start
+        n2 = n1 // G
+        qh, kh, vh, dyh = (inputs.to_f64(head(t, b, r, n)) for t, r, n in
+                           ((pb.q, rq, n1), (pb.k, rk, n2), (pb.v, rk, n2), (pb.dout, rq, n1)))
+        ok = orc.visible(L1, L2, w.mask_mode, w.win_left, w.win_right)
+        y, lse = orc.forward_head(qh, kh, vh, scale, ok)
+        y = inputs.to_f64(inputs.round_io(y, w.dtype))
+        lse = lse.astype(np.float32).astype(np.float64)
+        t0 = time.perf_counter()
+        orc.backward_head(qh, kh, vh, dyh, y, lse, scale, ok)
+        dt = time.perf_counter() - t0
+        f = per_pair * L1 * L2
+        yield dt, (f / 2 if w.mask_mode == 1 else f), (L1, L2)
+
+
+def cpu_baseline(pb, budget_s):
+    secs = flops = 0.0
+    heads = 0
+    shape = None
+    for dt, f, shp in oracle_head_sampler(pb):
+        secs += dt
+        flops += f
+        heads += 1
+        shape = shp
+        if secs >= budget_s:
+            break
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle backward of {heads} head(s) of the workload (S1xS2 {shape[0]}x{shape[1]}), "
+                      f"{secs:.1f} s of CPU time, same flop convention"}
+
+
+def reference_arm(args, rank, world):
+    from attention_backward_fabwd_gb300 import inputs
+
+    if rank != 0:
+        return None
+    w = inputs.WORKLOADS[args.workload]
+    pb = inputs.make_problem(w)
+    gen = oracle_head_sampler(pb)
+    for _ in range(max(args.warmup, 0)):
+        next(gen)
+    secs = flops = 0.0
+    times = []
+    shape = None
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        dt, f, shape = next(gen)
+        secs += dt
+        flops += f
+        times.append(dt)
+    value = flops / secs / 1e12
+    cores = blas_threads()
+    sample = (f"each step: fp64 numpy oracle backward of one head (S1xS2 {shape[0]}x{shape[1]}) of the workload, "
+              f"same flop convention")
+    conv, _ = flop_counts(pb)
+    return {"metric": "attention-backward TFLOP/s (bf16) at 1 GB300 and % of dense tensor peak", "value": value,
+            "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": workload_config(pb, l2="n/a (CPU)"),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0, "wall_s": time.perf_counter() - t0}
+
+
+def workload_config(pb, l2):
+    w = pb.w
+    cfg = {"workload": w.name, "layout": w.layout, "B": w.B, "S1": pb.S1, "S2": pb.S2, "N1": w.N1, "N2": w.N2,
+           "D": w.D, "Dv": w.Dv, "mask_mode": w.mask_mode, "win_left": w.win_left, "win_right": w.win_right,
+           "io_dtype": w.dtype, "l2": l2}
+    if w.layout == "TND":
+        cfg["seq_lengths"] = np.diff(pb.cu_seqlens_q).tolist()
+        cfg["T1"] = pb.T1
+    return cfg
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = reference_arm(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    r = gpu_arm(args, rank, world, local_rank)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    pb, w = r["pb"], r["w"]
+    conv, alg = flop_counts(pb)
+    peak_tf, peak_hbm, peak_kind = measured_peaks()
+    value = job_tflops(conv, world, r["ms_step"])
+    achieved = alg / (r["ms_main"] * 1e-3) / 1e12
+    # HBM-bound helper kernels: algorithmic bytes per launch
+    e = 2
+    pre_bytes = e * 2 * pb.dout.numel() + 4 * w.N1 * pb.T1 + 2 * 4 * w.B * w.N1 * ((pb.S1 + 127) // 128 * 128) \
+        + 4 * r["dq_elems"]
+    conv_bytes = 4 * r["dq_elems"] + e * r["dq_elems"]
+    out = {
+        "metric": "attention-backward TFLOP/s (bf16) at 1 GB300 and % of dense tensor peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": workload_config(pb, l2="flushed: 256 MB buffer written between timed steps (untimed)"),
+        "pct_of_peak": 100.0 * value / world / peak_tf,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": profile_traffic(w.name),
+                     "kernel": "fabwd_main_kernel", "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                     "algorithmic_flops_per_launch": alg, "ms_per_launch": r["ms_main"]},
+        "kernels": {
+            "preprocess": {"ms": r["ms_pre"], "GB/s": pre_bytes / (r["ms_pre"] * 1e-3) / 1e9,
+                           "frac_of_hbm": pre_bytes / (r["ms_pre"] * 1e-3) / 1e9 / peak_hbm},
+            "main": {"ms": r["ms_main"], "TFLOP/s": achieved},
+            "convert": {"ms": r["ms_conv"], "GB/s": conv_bytes / (r["ms_conv"] * 1e-3) / 1e9,
+                        "frac_of_hbm": conv_bytes / (r["ms_conv"] * 1e-3) / 1e9 / peak_hbm},
+        },
+        "flops_convention": conv, "flops_algorithmic": alg,
+        "gpu_launches": 3 * args.steps,
+        "clocks": r["clocks"],
+        "wall_s_timed_region": r["t_wall"],
+    }
+    if r["e2e"]:
+        out["e2e"] = {"value": job_tflops(conv, world, r["e2e_ms"]), "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": r["e2e"]["h2d_bytes_per_step"],
+                      "d2h_bytes_per_step": r["e2e"]["d2h_bytes_per_step"], "ms_per_step": r["e2e_ms"]}
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(pb, args.cpu_seconds)
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

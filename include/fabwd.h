@@ -74,6 +74,7 @@ typedef enum { FABWD_MASK_NONE = 0, FABWD_MASK_CAUSAL = 1, FABWD_MASK_BAND = 2 }
 /* Device status bits (fabwd_read_device_status). */
 #define FABWD_DEV_TIMEOUT 0x1u     /* a bounded mbarrier wait gave up; outputs are not valid */
 #define FABWD_DEV_BAD_SEQLENS 0x2u /* cu_seqlens not non-decreasing from 0, or beyond T / max */
+#define FABWD_DEV_INTERNAL 0x4u    /* a kernel found its shared memory misaligned; nothing computed */
 
 typedef struct {
   int32_t dtype;   /* fabwd_dtype */
@@ -124,6 +125,14 @@ fabwd_status fabwd_preprocess(const fabwd_params* p, void* workspace, size_t wor
  * device shows up in fabwd_read_device_status, not here. */
 fabwd_status fabwd_run(const fabwd_params* p, void* workspace, size_t workspace_bytes,
                        void* stream);
+
+/* The two halves of fabwd_run, for callers that schedule or time them separately:
+ * fabwd_run_main enqueues only the main backward kernel (dk, dv written; dQ partials added into
+ * the workspace accumulator); fabwd_run_convert enqueues only the convert kernel
+ * (dq = cast(scale · accumulator)).  fabwd_run == fabwd_run_main then fabwd_run_convert.
+ * Errors: as fabwd_run. */
+fabwd_status fabwd_run_main(const fabwd_params* p, void* workspace, size_t workspace_bytes, void* stream);
+fabwd_status fabwd_run_convert(const fabwd_params* p, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronising read of the device status word: enqueues a 4-byte device-to-host copy on
  * `stream`, waits for the stream, and stores the FABWD_DEV_* bits in *device_status.  Returns

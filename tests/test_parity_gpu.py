@@ -1,0 +1,270 @@
+"""GPU parity: the libfabwd CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (the measurement statement's): per output tensor relative L2 <= 1e-2 and
+max-abs <= 2e-2 · max|ref|; the fp32 sfmg within 1e-5 relative.  Small cases compare every
+element and span several 128-row tiles with ragged tails; the full-size workloads compare
+sampled output rows that the oracle evaluates one at a time.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attention_backward_fabwd_gb300 import api, fabwd as F, inputs
+from oracle import fabwd_oracle as orc
+
+import fabwd_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+W = inputs.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from attention_backward_fabwd_gb300 import build
+
+    build.build()
+    F.lib()
+
+
+def check_all(pb, ref, dq, dk, dv, sf):
+    out = {}
+    out["dq"] = tl.assert_close("dq", dq, ref.dq)
+    out["dk"] = tl.assert_close("dk", dk, ref.dk)
+    out["dv"] = tl.assert_close("dv", dv, ref.dv)
+    e = tl.errors(sf, ref.sfmg)
+    assert e["rel_l2"] <= tl.SFMG_REL, f"sfmg rel {e['rel_l2']}"
+    return out
+
+
+SMALL = [
+    ("mha_s128_d64", W["mha_s128_d64"], None),
+    ("causal_b2_s384", inputs.sized(W["causal_b2_s2048_d128"], N1=2, N2=2, S1=384, S2=384), None),
+    ("gqa_causal_ragged", inputs.sized(W["gqa_causal_s4096_d128"], N1=4, N2=2, S1=300, S2=300, dout_std=1.0), None),
+    ("gqa8", inputs.sized(W["gqa_causal_s4096_d128"], N1=8, N2=1, S1=200, S2=200, dout_std=1.0), None),
+    ("dense_s1_lt_s2", inputs.sized(W["mha_s128_d64"], S1=200, S2=333, D=128, Dv=128), None),
+    ("causal_s1_gt_s2", inputs.sized(W["causal_b2_s2048_d128"], B=1, N1=2, N2=2, S1=300, S2=150), None),
+    ("causal_s1_lt_s2", inputs.sized(W["causal_b2_s2048_d128"], B=1, N1=2, N2=2, S1=150, S2=420), None),
+    ("band_bnsd_d64", inputs.sized(W["mha_s128_d64"], layout="BNSD", S1=190, S2=190, mask_mode=2, win_left=20,
+                                    win_right=7), None),
+    ("band_wide", inputs.sized(W["causal_b2_s2048_d128"], B=1, N1=2, N2=2, S1=520, S2=520, mask_mode=2,
+                               win_left=200, win_right=150), None),
+    ("window_left_only", inputs.sized(W["causal_b2_s2048_d128"], B=1, N1=2, N2=1, S1=400, S2=400, mask_mode=2,
+                                      win_left=64), None),
+    ("fp16_dense_d64", inputs.sized(W["mha_s128_d64"], dtype="fp16", S1=257, S2=129), None),
+    ("scale_0_3", inputs.sized(W["mha_s128_d64"], softmax_scale=0.3, S1=130, S2=260), None),
+    ("bsnd_bf16_causal_window", inputs.sized(W["causal_b2_s2048_d128"], B=1, N1=2, N2=2, S1=700, S2=700,
+                                             win_left=150, win_right=0), None),
+    ("tnd_fp16_window", inputs.sized(W["varlen_window_fp16_d128"], B=5, N1=2, N2=2, win_left=64),
+     ([130, 1, 0, 257, 64], None)),
+    ("tnd_bf16_gqa_dense", inputs.sized(W["varlen_window_fp16_d128"], dtype="bf16", B=3, N1=4, N2=2, mask_mode=0,
+                                        win_left=-1, win_right=-1), ([200, 33, 129], [90, 300, 129])),
+    ("tnd_causal_unequal", inputs.sized(W["varlen_window_fp16_d128"], B=3, N1=2, N2=1, win_left=-1),
+     ([200, 33, 300], [150, 60, 300])),
+]
+
+
+@pytest.mark.parametrize("name,w,lens", SMALL, ids=[c[0] for c in SMALL])
+def test_small_elementwise(name, w, lens):
+    pb = inputs.make_problem(w, *(lens or ()))
+    ref = tl.full_reference(pb)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref)
+    check_all(pb, ref, dq, dk, dv, sf)
+
+
+def test_page_example_shapes_gqa_fp16():
+    # The BSND GQA call of [FAG] §4.8: B=2, S1=S2=128, N1=8, N2=2, D=Dv=128, fp16, dense.
+    w = inputs.Workload("page_example", "BSND", "fp16", B=2, N1=8, N2=2, D=128, Dv=128, S1=128, S2=128,
+                        softmax_scale=1.0 / math.sqrt(128), seed=7)
+    pb = inputs.make_problem(w)
+    ref = tl.full_reference(pb)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref)
+    assert dq.shape == pb.q.shape and dk.shape == pb.k.shape and dv.shape == pb.v.shape
+    assert dq.dtype == pb.q.dtype == dk.dtype == dv.dtype
+    check_all(pb, ref, dq, dk, dv, sf)
+
+
+def test_dk_dv_deterministic_and_workspace_reuse():
+    w = inputs.sized(W["gqa_causal_s4096_d128"], N1=4, N2=2, S1=256, S2=256, dout_std=1.0)
+    pb = inputs.make_problem(w)
+    ref = tl.forward_inputs(pb)
+    dev = torch.device("cuda")
+    args = [t.to(dev) for t in (pb.q, pb.k, pb.v, pb.dout, ref.attn_out, ref.lse)]
+    dq1, dk1, dv1 = api.flash_attn_grad(*args, mask_mode=1, check_status=True)
+    dq2, dk2, dv2 = api.flash_attn_grad(*args, mask_mode=1, check_status=True)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)   # no atomics on dK/dV
+    assert (dq1.float() - dq2.float()).abs().max().item() <= 1e-2 * dq1.float().abs().max().item()
+
+
+# ---------------------------------------------------------------------------------------------
+# degenerate and edge cases
+# ---------------------------------------------------------------------------------------------
+
+
+def _gpu_call(q, k, v, do, y, lse, **kw):
+    dev = torch.device("cuda")
+    return api.flash_attn_grad(*(t.to(dev) if t is not None else None for t in (q, k, v, do, y, lse)),
+                               check_status=True, **kw)
+
+
+def test_single_key_closed_form_on_gpu():
+    # one key: P == 1 and dS = P (dY·v − dY·Y) vanishes up to the bf16 rounding of Y (attn_out),
+    # so dQ and dK are tiny next to dV = Σ_i dY_i
+    w = inputs.sized(W["mha_s128_d64"], S1=300, S2=1, N1=2, N2=2)
+    pb = inputs.make_problem(w)
+    ref = tl.full_reference(pb)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref)
+    scale = dv.float().abs().max().item()
+    assert dq.float().abs().max().item() <= 1e-4 * scale and dk.float().abs().max().item() <= 1e-4 * scale
+    tl.assert_close("dv", dv, ref.dv)
+    want = inputs.to_f64(pb.dout).sum(axis=1)[0]          # [N, Dv]: Σ_i dY_i per head
+    tl.assert_close("dv closed form", inputs.to_f64(dv)[0, 0], want)
+
+
+def test_s2_zero_gives_zero_dq():
+    w = inputs.sized(W["mha_s128_d64"], S1=130, S2=0)
+    pb = inputs.make_problem(w)
+    lse = torch.full((1, 2, 130), float("inf"))
+    dq, dk, dv = _gpu_call(pb.q, pb.k, pb.v, pb.dout, torch.zeros_like(pb.dout), lse)
+    torch.cuda.synchronize()
+    assert dk.numel() == 0 and dv.numel() == 0 and dq.abs().max().item() == 0
+
+
+def test_s1_zero_gives_zero_dk_dv():
+    w = inputs.sized(W["mha_s128_d64"], S1=0, S2=200)
+    pb = inputs.make_problem(w)
+    dq, dk, dv = _gpu_call(pb.q, pb.k, pb.v, pb.dout, pb.dout.clone(), torch.zeros(1, 2, 0), mask_mode=1)
+    torch.cuda.synchronize()
+    assert dq.numel() == 0 and dk.abs().max().item() == 0 and dv.abs().max().item() == 0
+
+
+def test_tnd_all_sequences_empty_but_one():
+    w = inputs.sized(W["varlen_window_fp16_d128"], B=4, N1=2, N2=2)
+    pb = inputs.make_problem(w, [0, 0, 5, 0], [0, 3, 7, 0])
+    ref = tl.full_reference(pb)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref)
+    check_all(pb, ref, dq, dk, dv, sf)
+
+
+def test_rows_without_keys_get_zero_dq():
+    # causal with S1 > S2: the first S1 - S2 rows see no key (lse = +inf)
+    w = inputs.sized(W["causal_b2_s2048_d128"], B=1, N1=2, N2=2, S1=260, S2=100)
+    pb = inputs.make_problem(w)
+    ref = tl.full_reference(pb)
+    assert np.isinf(ref.lse.numpy()[0, :, :160]).all()
+    dq, dk, dv, sf = tl.run_gpu(pb, ref)
+    assert dq[0, :160].abs().max().item() == 0
+    check_all(pb, ref, dq, dk, dv, sf)
+
+
+def test_bad_cu_seqlens_reported_not_faulted():
+    w = inputs.sized(W["varlen_window_fp16_d128"], B=2, N1=2, N2=2)
+    pb = inputs.make_problem(w, [100, 60])
+    ref = tl.forward_inputs(pb)
+    dev = torch.device("cuda")
+    bad = torch.tensor([0, 100, 170], dtype=torch.int32, device=dev)   # ends beyond T = 160
+    args = [t.to(dev) for t in (pb.q, pb.k, pb.v, pb.dout, ref.attn_out, ref.lse)]
+    with pytest.raises(F.FabwdError) as ei:
+        api.flash_attn_grad(*args, cu_seqlens_q=bad, cu_seqlens_kv=bad, max_seqlen_q=128, max_seqlen_kv=128,
+                            layout_q="TND", layout_kv="TND", layout_out="TND", check_status=True)
+    assert ei.value.status == F.FABWD_ERR_DEVICE
+    # the context stays usable: a correct call right after succeeds
+    cu = torch.from_numpy(pb.cu_seqlens_q).to(dev)
+    api.flash_attn_grad(*args, cu_seqlens_q=cu, cu_seqlens_kv=cu, layout_q="TND", layout_kv="TND",
+                        layout_out="TND", mask_mode=1, win_left=1024, win_right=0, check_status=True)
+
+
+def test_timeout_injection_returns_status_and_context_survives():
+    w = inputs.sized(W["gqa_causal_s4096_d128"], N1=4, N2=2, S1=256, S2=256, dout_std=1.0)
+    pb = inputs.make_problem(w)
+    ref = tl.full_reference(pb)
+    old = F.fabwd_set_wait_limit_ns(20_000_000)  # 20 ms
+    try:
+        F.fabwd_debug_inject_timeout(True)
+        with pytest.raises(F.FabwdError) as ei:
+            _gpu_call(pb.q, pb.k, pb.v, pb.dout, ref.attn_out, ref.lse, mask_mode=1)
+        assert ei.value.status == F.FABWD_ERR_TIMEOUT
+    finally:
+        F.fabwd_debug_inject_timeout(False)
+        F.fabwd_set_wait_limit_ns(old)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref)   # same process, same context: still correct
+    check_all(pb, ref, dq, dk, dv, sf)
+
+
+# ---------------------------------------------------------------------------------------------
+# full-size workloads, sampled outputs
+# ---------------------------------------------------------------------------------------------
+
+
+def _sample_rows(rng, seqs, heads, edges, n):
+    out = set()
+    for s, L in seqs:
+        if L == 0:
+            continue
+        for h in (0, heads - 1):
+            for i in edges:
+                if 0 <= i < L:
+                    out.add((s, h, i))
+                if 0 <= L - 1 - i < L:
+                    out.add((s, h, L - 1 - i))
+    nonempty = [(s, L) for s, L in seqs if L > 0]
+    while len(out) < n and nonempty:
+        s, L = nonempty[rng.integers(len(nonempty))]
+        out.add((s, int(rng.integers(heads)), int(rng.integers(L))))
+    return sorted(out)
+
+
+FULL = ["mha_s128_d64", "causal_b2_s2048_d128", "gqa_causal_s4096_d128", "varlen_window_fp16_d128"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    w = W[name]
+    pb = inputs.make_problem(w)
+    ref = tl.forward_inputs(pb)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref)
+    kw = tl.oracle_kwargs(pb)
+    if w.layout == "TND":
+        seq_q = list(enumerate(np.diff(pb.cu_seqlens_q).tolist()))
+        seq_k = list(enumerate(np.diff(pb.cu_seqlens_kv).tolist()))
+    else:
+        seq_q = [(b, pb.S1) for b in range(w.B)]
+        seq_k = [(b, pb.S2) for b in range(w.B)]
+    rng = np.random.default_rng(5)
+    edges = [0, 1, 63, 64, 127, 128, 129]
+    q_rows = _sample_rows(rng, seq_q, w.N1, edges, 48)
+    kv_rows = _sample_rows(rng, seq_k, w.N2, edges, 48)
+    q, k, v, dy = (inputs.to_f64(t) for t in (pb.q, pb.k, pb.v, pb.dout))
+    gq, gk, gv = orc.backward_sampled(q, k, v, dy, inputs.to_f64(ref.attn_out), ref.lse.numpy().astype(np.float64),
+                                      q_rows=q_rows, kv_rows=kv_rows, **kw)
+
+    def pick(t, rows, cu):
+        x = inputs.to_f64(t)
+        if w.layout == "TND":
+            return np.stack([x[cu[s] + i, n] for s, n, i in rows])
+        return np.stack([x[s, i, n] for s, n, i in rows])
+
+    tl.assert_close("dq (sampled)", pick(dq, q_rows, pb.cu_seqlens_q), np.stack(gq))
+    tl.assert_close("dk (sampled)", pick(dk, kv_rows, pb.cu_seqlens_kv), np.stack(gk))
+    tl.assert_close("dv (sampled)", pick(dv, kv_rows, pb.cu_seqlens_kv), np.stack(gv))
+    # sfmg of every row: the oracle's rowsum(dY ⊙ Y) per head
+    y = inputs.to_f64(ref.attn_out)
+    if w.layout == "TND":
+        want = np.stack([orc._sfmg(dy[:, n], y[:, n]) for n in range(w.N1)])
+    else:
+        want = np.stack([np.stack([orc._sfmg(dy[b, :, n], y[b, :, n]) for n in range(w.N1)]) for b in range(w.B)])
+    e = tl.errors(sf, want)
+    assert e["rel_l2"] <= tl.SFMG_REL
+
+
+def test_unbuilt_head_dim_pair_is_unsupported():
+    w = W["causal_s8192_d192_dv128"]
+    q = torch.zeros(1, 256, 2, 192, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(1, 256, 2, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(F.FabwdError) as ei:
+        api.flash_attn_grad(q, q, v, v, v, torch.zeros(1, 2, 256, device="cuda"), mask_mode=w.mask_mode)
+    assert ei.value.status == F.FABWD_ERR_UNSUPPORTED
