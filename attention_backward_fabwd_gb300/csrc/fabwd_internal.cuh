@@ -8,7 +8,7 @@
 namespace fabwd {
 
 constexpr int kBlockKV = 128;  // kv rows per CTA of the main kernel (M of the kv-side MMAs)
-constexpr int kBlockQ = 128;   // q rows per main-loop step (N of S^T / dP^T, M of dQ)
+constexpr int kBlockQ = 64;    // q rows per main-loop step (N of S^T / dP^T / dQ^T)
 constexpr int kRowPad = 128;   // padding of the per-(sequence, q-head) lse2 / sfmg rows
 
 enum Layout : int { kBSND = 0, kTND = 1, kBNSD = 2 };

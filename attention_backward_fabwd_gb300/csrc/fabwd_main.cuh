@@ -1,28 +1,30 @@
-// Main FlashAttention backward kernel for sm_103a: warp-specialised tcgen05 + TMEM + TMA.
+// Main FlashAttention backward kernel for sm_103a: warp-specialised tcgen05 + TMEM + TMA with two
+// ping-ponged TMEM slots.
 //
 // What it computes is the backward of the page "CANN ops-transformer FlashAttnGrad 算子详解"
 // (discosf.com/news/4863418), §一.  One CTA owns a block of 128 keys of one kv-head and loops
-// over the G q-heads of the group and the 128-row q-blocks that can see the block:
-//     Sᵀ  = K·Qᵀ                 tcgen05 (M = 128 keys, N = 128 queries, K = D)
+// over steps t = (q-head of the group, 64-row q-block that can see the block):
+//     Sᵀ  = K·Qᵀ                 tcgen05 (M = 128 keys, N = 64 queries, K = D)
 //     dPᵀ = V·dOᵀ                tcgen05 (K = Dv)
 //     Pᵀ  = exp2(Sᵀ·scale·log2e − lse·log2e), masked pairs -> 0, written back to TMEM (bf16/fp16)
 //     dSᵀ = Pᵀ ⊙ (dPᵀ − sfmg)    -> shared memory (bf16/fp16)
 //     dV += Pᵀ·dO                tcgen05, A operand read from TMEM
-//     dK += dSᵀ·Q                tcgen05, accumulated over q-blocks and the G q-heads
-//     dQᵀ = Kᵀ·dSᵀ               tcgen05, M = 128 head-dim rows -> fp32 reduce-add into the
+//     dK += dSᵀ·Q                tcgen05, accumulated over all steps (q-blocks and the G heads)
+//     dQᵀ = Kᵀ·dSᵀ               tcgen05 (M = 128 head-dim rows) -> fp32 reduce-add into the
 //                                workspace accumulator, one coalesced 128-byte line per warp
 // The five products are §5.2's MM2, MM1, MM5, MM4, MM3 and the elementwise steps its V2-V4.
-// K is used K-major (Sᵀ) and MN-major (dQᵀ) from one shared-memory copy, Q and dO likewise
-// serve two products each, and dSᵀ serves dK (K-major) and dQᵀ (MN-major): the layout choices
-// are descriptor bits, not copies.
+// K is read K-major (Sᵀ) and MN-major (dQᵀ) from one shared-memory copy; Q and dO likewise
+// serve two products each, and dSᵀ serves dK (K-major) and dQᵀ (MN-major).
 //
-// Warp roles (320 threads): warps 0-7 compute (warp w reads TMEM lanes 32·(w%4)..+31; warps
-// 0-3 take query columns 0-63 and warps 4-7 columns 64-127), warp 8 issues TMA loads (K, V once;
-// Q, dO, lse, sfmg double-buffered), warp 9 allocates TMEM and issues the MMAs.
+// Schedule.  Steps alternate between two TMEM slots (Sᵀ/Pᵀ and dPᵀ/dQᵀ per slot) and two compute
+// warpgroups: warpgroup g (warps 4g..4g+3, warp w reading TMEM lanes 32·(w%4)..+31) handles the
+// steps t ≡ g (mod 2).  The MMA warp issues, for step t, the Sᵀ/dPᵀ products of step t+1 (other
+// slot) and then dV, dK, dQᵀ of step t, so each warpgroup's softmax/dS work overlaps the other
+// slot's products.  Warp 8 streams Q, dO, lse and sfmg through a 4-stage ring (K and V once).
 //
-// TMEM columns: dK [0, D), dV [D, D+Dv), Sᵀ/Pᵀ [D+Dv, +128), dPᵀ/dQᵀ [D+Dv+128, +128).
-// Shared memory: K (padded to 128 head-dim columns), V, 2×Q, 2×dO, dSᵀ, 2×lse, 2×sfmg.  Tiles
-// are 128-byte-swizzled [64-column block][rows][64] arrays (TMA SWIZZLE_128B, box {64,1,rows,1}).
+// TMEM columns: dK [0, D), dV [D, D+Dv), slot g at D+Dv+128g: Sᵀ/Pᵀ [+0, +64), dPᵀ/dQᵀ [+64, +128).
+// Shared memory: K (padded to 128 head-dim columns), V, 4×(Q, dO, lse, sfmg), 2×dSᵀ.  Tiles are
+// 128-byte-swizzled [64-column block][rows][64] arrays (TMA SWIZZLE_128B, box {64,1,rows,1}).
 //
 // Every mbarrier wait is bounded (MainArgs::wait_ns).  A wait that gives up sets a CTA abort
 // flag and FABWD_DEV_TIMEOUT; the other roles see the flag and leave their loops, the MMA
@@ -41,26 +43,27 @@ constexpr int kMainThreads = 320;
 
 template <int D, int DV>
 struct MainCfg {
-  static constexpr int BR = kBlockQ, BC = kBlockKV;
+  static constexpr int BR = kBlockQ, BC = kBlockKV, NS = 4;
   static constexpr int DK = D < 128 ? 128 : D;  // K rows padded so dQᵀ = Kᵀ·dSᵀ has M = 128
   static constexpr uint32_t kK = DK * BC * 2, kV = DV * BC * 2, kQ = D * BR * 2, kdO = DV * BR * 2;
   static constexpr uint32_t kdS = BC * BR * 2;
-  static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + 2 * kQ, odS = odO + 2 * kdO;
-  static constexpr uint32_t oL = odS + kdS;          // [2][BR] fp32 lse·log2(e)
-  static constexpr uint32_t oF = oL + 2 * BR * 4;    // [2][BR] fp32 sfmg
-  static constexpr uint32_t oBar = oF + 2 * BR * 4;  // mbarriers
-  static constexpr uint32_t oMisc = oBar + 32 * 8;   // TMEM base holder, abort flag
+  static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + NS * kQ, odS = odO + NS * kdO;
+  static constexpr uint32_t oL = odS + 2 * kdS;       // [NS][BR] fp32 lse·log2(e)
+  static constexpr uint32_t oF = oL + NS * BR * 4;    // [NS][BR] fp32 sfmg
+  static constexpr uint32_t oBar = oF + NS * BR * 4;  // mbarriers
+  static constexpr uint32_t oMisc = oBar + 48 * 8;    // TMEM base holder, abort flag
   static constexpr uint32_t bytes = oMisc + 64;
-  static constexpr uint32_t cDK = 0, cDV = D, cS = D + DV, cP = cS + BR;
+  static constexpr uint32_t cDK = 0, cDV = D, cSlot = D + DV;  // slot g: cSlot + 128 g
+  static_assert(BR == 64, "the slot layout assumes 64-row q-blocks");
   static_assert(D % 64 == 0 && DV % 64 == 0 && D <= 128 && DV <= 128, "head dims");
-  static_assert(cP + BR <= 512, "TMEM budget");
+  static_assert(cSlot + 256 <= 512, "TMEM budget");
   static_assert(bytes <= 232448, "shared memory budget");
 };
 
-enum Bar : int {
-  kKvFull = 0, kQFull0 = 1, kQFull1 = 2, kQEmpty0 = 3, kQEmpty1 = 4, kSFull = 5, kDpFull = 6, kPFull = 7,
-  kDsFull = 8, kDqFull = 9, kDqEmpty = 10, kAccDone = 11, kNever = 12, kDrain = 13, kNumBars = 14
-};
+// mbarrier indices
+constexpr int kKvFull = 0, kQFull = 1 /*+NS*/, kQEmpty = 5 /*+NS*/, kSFull = 9 /*+2*/, kDpFull = 11 /*+2*/,
+              kDqFull = 13 /*+2*/, kPFull = 15 /*+2*/, kDsFull = 17 /*+2*/, kDqEmpty = 19 /*+2*/, kAccDone = 21,
+              kNever = 22, kDrain = 23, kNumBars = 24;
 
 struct SeqRange {
   int q0, L1, k0, L2;
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const MainArgs a) {
   using C = MainCfg<D, DV>;
-  constexpr int BR = C::BR, BC = C::BC;
+  constexpr int BR = C::BR, BC = C::BC, NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -148,27 +151,18 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   if (ie > sq.L1 - 1) ie = sq.L1 - 1;
   const int qb_begin = ib <= ie ? (int)(ib / BR) : 0;
   const int nqb = ib <= ie ? (int)(ie / BR) + 1 - qb_begin : 0;
-  const int T = nqb * a.G;  // loop steps: (head in group, q-block)
+  const int T = nqb * a.G;  // steps: (head in group, q-block)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBar);
   uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::oMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oMisc + 16);
 
   if (tid == 0) {
-    mbar_init(&bars[kKvFull], 1);
-    mbar_init(&bars[kQFull0], 1);
-    mbar_init(&bars[kQFull1], 1);
-    mbar_init(&bars[kQEmpty0], 1);
-    mbar_init(&bars[kQEmpty1], 1);
-    mbar_init(&bars[kSFull], 1);
-    mbar_init(&bars[kDpFull], 1);
-    mbar_init(&bars[kPFull], 8);
-    mbar_init(&bars[kDsFull], 8);
-    mbar_init(&bars[kDqFull], 1);
-    mbar_init(&bars[kDqEmpty], 8);
-    mbar_init(&bars[kAccDone], 1);
-    mbar_init(&bars[kNever], 1);
-    mbar_init(&bars[kDrain], 1);
+    for (int i = 0; i < kNumBars; ++i) {
+      const bool four = (i >= kPFull && i < kPFull + 2) || (i >= kDsFull && i < kDsFull + 2) ||
+                        (i >= kDqEmpty && i < kDqEmpty + 2);
+      mbar_init(&bars[i], four ? 4 : 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -216,24 +210,24 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tma_load_4d(smem + C::oV + c * BC * 128, &tm_v, &bars[kKvFull], c * 64, bnsd ? kv_row0 : n2,
                     bnsd ? n2 : kv_row0, bcoord);
       for (int t = 0; t < T; ++t) {
-        const int s = t & 1;
+        const int st = t % NS;
         const int h = t / nqb, qb = qb_begin + t % nqb;
         const int n1 = n2 * a.G + h, i0 = qb * BR;
-        if (t >= 2 && !wait_bar(&bars[kQEmpty0 + s], ((t >> 1) - 1) & 1, abort_flag, a)) break;
-        uint64_t* full = &bars[kQFull0 + s];
+        if (t >= NS && !wait_bar(&bars[kQEmpty + st], ((t / NS) - 1) & 1, abort_flag, a)) break;
+        uint64_t* full = &bars[kQFull + st];
         mbar_arrive_expect_tx(full, (D + DV) * BR * 2 + 2 * BR * 4);
         const int row = q_rowbase + i0;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(smem + C::oQ + s * C::kQ + c * BR * 128, &tm_q, full, c * 64, bnsd ? row : n1, bnsd ? n1 : row,
-                      bcoord);
+          tma_load_4d(smem + C::oQ + st * C::kQ + c * BR * 128, &tm_q, full, c * 64, bnsd ? row : n1,
+                      bnsd ? n1 : row, bcoord);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(smem + C::odO + s * C::kdO + c * BR * 128, &tm_do, full, c * 64, bnsd ? row : n1,
+          tma_load_4d(smem + C::odO + st * C::kdO + c * BR * 128, &tm_do, full, c * 64, bnsd ? row : n1,
                       bnsd ? n1 : row, bcoord);
         const long long rbase = ((long long)b * a.N1 + n1) * a.S1p + i0;
-        bulk_load(smem + C::oL + s * BR * 4, a.lse2 + rbase, BR * 4, full);
-        bulk_load(smem + C::oF + s * BR * 4, a.sfmg + rbase, BR * 4, full);
+        bulk_load(smem + C::oL + st * BR * 4, a.lse2 + rbase, BR * 4, full);
+        bulk_load(smem + C::oF + st * BR * 4, a.sfmg + rbase, BR * 4, full);
       }
     }
     __syncwarp();
@@ -244,43 +238,59 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       constexpr uint32_t ID_DV = idesc_f16(BC, DV, kBF16, false, true);
       constexpr uint32_t ID_DK = idesc_f16(BC, D, kBF16, false, true);
       constexpr uint32_t ID_DQ = idesc_f16(128, BR, kBF16, true, true);
-      const uint32_t aK = smem_u32(smem + C::oK), aV = smem_u32(smem + C::oV), adS = smem_u32(smem + C::odS);
-      bool ok = wait_bar(&bars[kKvFull], 0, abort_flag, a);
-      for (int t = 0; ok && t < T; ++t) {
-        const int s = t & 1;
-        const uint32_t aQ = smem_u32(smem + C::oQ + s * C::kQ), adO = smem_u32(smem + C::odO + s * C::kdO);
-        if (!(ok = wait_bar(&bars[kQFull0 + s], (t >> 1) & 1, abort_flag, a))) break;
+      const uint32_t aK = smem_u32(smem + C::oK), aV = smem_u32(smem + C::oV);
+      // Sᵀ(t) and dPᵀ(t) into slot t&1
+      auto issue_s_dp = [&](int t) -> bool {
+        const int g = t & 1, st = t % NS;
+        const uint32_t aQ = smem_u32(smem + C::oQ + st * C::kQ), adO = smem_u32(smem + C::odO + st * C::kdO);
+        const uint32_t slot = tmem + C::cSlot + g * 128;
+        if (!wait_bar(&bars[kQFull + st], (t / NS) & 1, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::cS, sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
+          mma_ss(slot, sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(aQ + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
-        mma_commit(&bars[kSFull]);
-        if (t > 0 && !(ok = wait_bar(&bars[kDqEmpty], (t - 1) & 1, abort_flag, a))) break;
+        mma_commit(&bars[kSFull + g]);
+        if (t >= 2 && !wait_bar(&bars[kDqEmpty + g], ((t >> 1) - 1) & 1, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
-          mma_ss(tmem + C::cP, sdesc_sw128(aV + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
+          mma_ss(slot + 64, sdesc_sw128(aV + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(adO + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
-        mma_commit(&bars[kDpFull]);
-        if (!(ok = wait_bar(&bars[kPFull], t & 1, abort_flag, a))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BR / 16; ++kk)  // Pᵀ columns: queries 0-63 at +0, 64-127 at +64
-          mma_ts(tmem + C::cDV, tmem + C::cS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                 sdesc_sw128(adO + kk * 2048, BR * 128, 1024), ID_DV, (t > 0 || kk > 0) ? 1u : 0u);
-        if (!(ok = wait_bar(&bars[kDsFull], t & 1, abort_flag, a))) break;
+        mma_commit(&bars[kDpFull + g]);
+        return true;
+      };
+      // dV, dK, dQᵀ of step t
+      auto issue_grads = [&](int t) -> bool {
+        const int g = t & 1, st = t % NS;
+        const uint32_t aQ = smem_u32(smem + C::oQ + st * C::kQ), adO = smem_u32(smem + C::odO + st * C::kdO);
+        const uint32_t adS = smem_u32(smem + C::odS + g * C::kdS);
+        const uint32_t slot = tmem + C::cSlot + g * 128;
+        const uint32_t u = (t >> 1) & 1;
+        if (!wait_bar(&bars[kPFull + g], u, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BR / 16; ++kk)
-          mma_ss(tmem + C::cDK, sdesc_sw128(adS + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::cDV, slot + kk * 8, sdesc_sw128(adO + kk * 2048, BR * 128, 1024), ID_DV,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        if (!wait_bar(&bars[kDsFull + g], u, abort_flag, a)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BR / 16; ++kk)
+          mma_ss(tmem + C::cDK, sdesc_sw128(adS + kk * 32, 16, 1024), sdesc_sw128(aQ + kk * 2048, BR * 128, 1024),
+                 ID_DK, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
-          mma_ss(tmem + C::cP, sdesc_sw128(aK + kk * 2048, BC * 128, 1024), sdesc_sw128(adS + kk * 2048, BC * 128, 1024),
+          mma_ss(slot + 64, sdesc_sw128(aK + kk * 2048, BC * 128, 1024), sdesc_sw128(adS + kk * 2048, BC * 128, 1024),
                  ID_DQ, kk > 0);
-        mma_commit(&bars[kDqFull]);
-        mma_commit(&bars[kQEmpty0 + s]);
+        mma_commit(&bars[kDqFull + g]);
+        mma_commit(&bars[kQEmpty + st]);
+        return true;
+      };
+      bool ok = wait_bar(&bars[kKvFull], 0, abort_flag, a) && issue_s_dp(0);
+      for (int t = 0; ok && t < T; ++t) {
+        if (t + 1 < T && !(ok = issue_s_dp(t + 1))) break;
+        ok = issue_grads(t);
       }
       if (ok) {
         mma_commit(&bars[kAccDone]);
@@ -291,35 +301,36 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ compute warps 0-7
-    const int q4 = warp & 3, wg = warp >> 2;
+    // ------------------------------------------------------------------ compute warpgroups 0, 1
+    const int q4 = warp & 3, g = warp >> 2;
     const int row = q4 * 32 + lane;  // TMEM lane: key row (Sᵀ, dPᵀ, dK, dV) or head-dim row (dQᵀ)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t slot = tmem + lane_off + C::cSlot + g * 128;
     const int jr = j0 + row;
     const bool j_valid = jr < sq.L2;
     const long long vlo = (long long)jr - off - hi, vhi = (long long)jr - off - lo;
     const int i_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
     const int i_vis_hi = (int)(vhi < -1 ? -1 : (vhi > (1 << 30) ? (1 << 30) : vhi));
-    const uint32_t adS = smem_u32(smem + C::odS) + wg * BC * 128 + row * 128;
+    const uint32_t adS = smem_u32(smem + C::odS + g * C::kdS) + row * 128;
     const long long i_stride = bnsd ? D : (long long)a.N1 * D;
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int s = t & 1;
+    for (int t = g; t < T; t += 2) {
+      const int st = t % NS;
+      const uint32_t u = (t >> 1) & 1;
       const int h = t / nqb, qb = qb_begin + t % nqb;
       const int n1 = n2 * a.G + h, i0 = qb * BR;
-      const int ic0 = i0 + wg * 64;  // first query of this warp's 64 columns
-      if (!(ok = wait_bar_warp(&bars[kQFull0 + s], (t >> 1) & 1, abort_flag, a))) break;
-      if (!(ok = wait_bar_warp(&bars[kSFull], t & 1, abort_flag, a))) break;
+      if (!(ok = wait_bar_warp(&bars[kQFull + st], (t / NS) & 1, abort_flag, a))) break;
+      if (!(ok = wait_bar_warp(&bars[kSFull + g], u, abort_flag, a))) break;
       tc_fence_after();
-      const float* sL = reinterpret_cast<const float*>(smem + C::oL + s * BR * 4) + wg * 64;
-      const float* sF = reinterpret_cast<const float*>(smem + C::oF + s * BR * 4) + wg * 64;
+      const float* sL = reinterpret_cast<const float*>(smem + C::oL + st * BR * 4);
+      const float* sF = reinterpret_cast<const float*>(smem + C::oF + st * BR * 4);
       const long long dmin = (long long)j0 - (i0 + BR - 1) - off, dmax = (long long)(j1 - 1) - i0 - off;
       const bool full = dmin >= lo && dmax <= hi;
       float p[64];
       {
         uint32_t r0[32], r1[32];
-        tmem_ld32(tmem + lane_off + C::cS + wg * 64, r0);
-        tmem_ld32(tmem + lane_off + C::cS + wg * 64 + 32, r1);
+        tmem_ld32(slot, r0);
+        tmem_ld32(slot + 32, r1);
         tmem_wait_ld();
         reg_fence(r0);
         reg_fence(r1);
@@ -332,7 +343,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (!full) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (ic0 + c < i_vis_lo || ic0 + c > i_vis_hi) p[c] = 0.f;
+          if (i0 + c < i_vis_lo || i0 + c > i_vis_hi) p[c] = 0.f;
       }
       if (!j_valid) {
 #pragma unroll
@@ -342,18 +353,18 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) pk[c] = pack2<FP16>(p[2 * c], p[2 * c + 1]);
-        tmem_st32(tmem + lane_off + C::cS + wg * 64, pk);
+        tmem_st32(slot, pk);
         tmem_wait_st();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kPFull]);
-      if (!(ok = wait_bar_warp(&bars[kDpFull], t & 1, abort_flag, a))) break;
+      if (lane == 0) mbar_arrive(&bars[kPFull + g]);
+      if (!(ok = wait_bar_warp(&bars[kDpFull + g], u, abort_flag, a))) break;
       tc_fence_after();
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::cP + wg * 64 + hh * 32, r);
+        tmem_ld32(slot + 64 + hh * 32, r);
         tmem_wait_ld();
         reg_fence(r);
         uint32_t dk[16];
@@ -364,28 +375,28 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           dk[c >> 1] = pack2<FP16>(d0, d1);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_shared_v4(adS + ((((hh * 4 + u) ^ (row & 7))) << 4), dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        for (int v4 = 0; v4 < 4; ++v4)
+          st_shared_v4(adS + ((((hh * 4 + v4) ^ (row & 7))) << 4), dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2],
+                       dk[4 * v4 + 3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kDsFull]);
-      if (!(ok = wait_bar_warp(&bars[kDqFull], t & 1, abort_flag, a))) break;
+      if (lane == 0) mbar_arrive(&bars[kDsFull + g]);
+      if (!(ok = wait_bar_warp(&bars[kDqFull + g], u, abort_flag, a))) break;
       tc_fence_after();
       {
         uint32_t r0[32], r1[32];
-        tmem_ld32(tmem + lane_off + C::cP + wg * 64, r0);
-        tmem_ld32(tmem + lane_off + C::cP + wg * 64 + 32, r1);
+        tmem_ld32(slot + 64, r0);
+        tmem_ld32(slot + 96, r1);
         tmem_wait_ld();
         reg_fence(r0);
         reg_fence(r1);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kDqEmpty]);
-        if (row < D) {  // lane = head-dim index d; columns = queries ic0 .. ic0 + 63
-          const int nvalid = min(64, sq.L1 - ic0);
-          float* dst = a.dq_acc +
-                       row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? ic0 : 0), n1, a.N1, a.S1) * D + row;
+        if (lane == 0) mbar_arrive(&bars[kDqEmpty + g]);
+        if (row < D) {  // lane = head-dim index d; columns = queries i0 .. i0 + 63
+          const int nvalid = min(BR, sq.L1 - i0);
+          float* dst = a.dq_acc + row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 : 0), n1, a.N1, a.S1) * D + row;
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (c < nvalid) red_add_f32(dst + c * i_stride, __uint_as_float(r0[c]));
@@ -404,7 +415,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       uint16_t* dv = static_cast<uint16_t*>(a.dv) + krow * DV;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
-        const int col = wg * (D / 2) + c * 32;
+        const int col = g * (D / 2) + c * 32;
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + C::cDK + col, r);
         tmem_wait_ld();
@@ -415,13 +426,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * a.scale, __uint_as_float(r[e + 1]) * a.scale) : 0u;
         if (j_valid) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(dk + col + u * 8) = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+          for (int v4 = 0; v4 < 4; ++v4)
+            *reinterpret_cast<uint4*>(dk + col + v4 * 8) =
+                make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
         }
       }
 #pragma unroll 1
       for (int c = 0; c < DV / 64; ++c) {
-        const int col = wg * (DV / 2) + c * 32;
+        const int col = g * (DV / 2) + c * 32;
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + C::cDV + col, r);
         tmem_wait_ld();
@@ -432,8 +444,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]), __uint_as_float(r[e + 1])) : 0u;
         if (j_valid) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(dv + col + u * 8) = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+          for (int v4 = 0; v4 < 4; ++v4)
+            *reinterpret_cast<uint4*>(dv + col + v4 * 8) =
+                make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
         }
       }
     }
