@@ -7,9 +7,9 @@
 //     Sᵀ  = K·Qᵀ                 tcgen05 (M = 128 keys, N = 64 queries, K = D)
 //     dPᵀ = V·dOᵀ                tcgen05 (K = Dv)
 //     Pᵀ  = exp2(Sᵀ·scale·log2e − lse·log2e), masked pairs -> 0, written back to TMEM (bf16/fp16)
-//     dSᵀ = Pᵀ ⊙ (dPᵀ − sfmg)    -> shared memory (bf16/fp16)
+//     dSᵀ = Pᵀ ⊙ (dPᵀ − sfmg)    -> TMEM and shared memory (bf16/fp16)
 //     dV += Pᵀ·dO                tcgen05, A operand read from TMEM
-//     dK += dSᵀ·Q                tcgen05, accumulated over all steps (q-blocks and the G heads)
+//     dK += dSᵀ·Q                tcgen05, A operand read from TMEM; accumulated over all steps
 //     dQᵀ = Kᵀ·dSᵀ               tcgen05 (M = 128 head-dim rows) -> fp32 reduce-add into the
 //                                workspace accumulator, one coalesced 128-byte line per warp
 // The five products are §5.2's MM2, MM1, MM5, MM4, MM3 and the elementwise steps its V2-V4.
@@ -22,7 +22,8 @@
 // slot) and then dV, dK, dQᵀ of step t, so each warpgroup's softmax/dS work overlaps the other
 // slot's products.  Warp 8 streams Q, dO, lse and sfmg through a 4-stage ring (K and V once).
 //
-// TMEM columns: dK [0, D), dV [D, D+Dv), slot g at D+Dv+128g: Sᵀ/Pᵀ [+0, +64), dPᵀ/dQᵀ [+64, +128).
+// TMEM columns: dK [0, D), dV [D, D+Dv), slot g at D+Dv+128g: Sᵀ [+0, +64) overwritten by Pᵀ
+// [+0, +32) and dSᵀ [+32, +64) (16-bit pairs), dPᵀ/dQᵀ [+64, +128).
 // Shared memory: K (padded to 128 head-dim columns), V, 4×(Q, dO, lse, sfmg), 2×dSᵀ.  Tiles are
 // 128-byte-swizzled [64-column block][rows][64] arrays (TMA SWIZZLE_128B, box {64,1,rows,1}).
 //
@@ -276,9 +277,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (!wait_bar(&bars[kDsFull + g], u, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BR / 16; ++kk)
-          mma_ss(tmem + C::cDK, sdesc_sw128(adS + kk * 32, 16, 1024), sdesc_sw128(aQ + kk * 2048, BR * 128, 1024),
-                 ID_DK, (t > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BR / 16; ++kk)  // dSᵀ from TMEM (next to Pᵀ)
+          mma_ts(tmem + C::cDK, slot + 32 + kk * 8, sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK,
+                 (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
           mma_ss(slot + 64, sdesc_sw128(aK + kk * 2048, BC * 128, 1024), sdesc_sw128(adS + kk * 2048, BC * 128, 1024),
@@ -322,37 +323,39 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (!(ok = wait_bar_warp(&bars[kQFull + st], (t / NS) & 1, abort_flag, a))) break;
       if (!(ok = wait_bar_warp(&bars[kSFull + g], u, abort_flag, a))) break;
       tc_fence_after();
-      const float* sL = reinterpret_cast<const float*>(smem + C::oL + st * BR * 4);
-      const float* sF = reinterpret_cast<const float*>(smem + C::oF + st * BR * 4);
+      const float4* sL4 = reinterpret_cast<const float4*>(smem + C::oL + st * BR * 4);
+      const float4* sF4 = reinterpret_cast<const float4*>(smem + C::oF + st * BR * 4);
       const long long dmin = (long long)j0 - (i0 + BR - 1) - off, dmax = (long long)(j1 - 1) - i0 - off;
       const bool full = dmin >= lo && dmax <= hi;
-      float p[64];
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(slot, r0);
-        tmem_ld32(slot + 32, r1);
-        tmem_wait_ld();
-        reg_fence(r0);
-        reg_fence(r1);
+      uint32_t p[64];  // Sᵀ row, then P (fp32 bits)
+      tmem_ld32(slot, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+      tmem_ld32(slot + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      tmem_wait_ld();
+      reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+      reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[32]));
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          p[c] = ex2(fmaf(__uint_as_float(r0[c]), a.scale_log2, -sL[c]));
-          p[c + 32] = ex2(fmaf(__uint_as_float(r1[c]), a.scale_log2, -sL[c + 32]));
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l = sL4[c4];
+        const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * c4 + e;
+          p[c] = __float_as_uint(ex2(fmaf(__uint_as_float(p[c]), a.scale_log2, -lv[e])));
         }
       }
       if (!full) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (i0 + c < i_vis_lo || i0 + c > i_vis_hi) p[c] = 0.f;
+          if (i0 + c < i_vis_lo || i0 + c > i_vis_hi) p[c] = 0u;
       }
       if (!j_valid) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = 0.f;
+        for (int c = 0; c < 64; ++c) p[c] = 0u;
       }
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack2<FP16>(p[2 * c], p[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) pk[c] = pack2<FP16>(__uint_as_float(p[2 * c]), __uint_as_float(p[2 * c + 1]));
         tmem_st32(slot, pk);
         tmem_wait_st();
       }
@@ -369,17 +372,26 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         reg_fence(r);
         uint32_t dk[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float d0 = p[hh * 32 + c] * (__uint_as_float(r[c]) - sF[hh * 32 + c]);
-          const float d1 = p[hh * 32 + c + 1] * (__uint_as_float(r[c + 1]) - sF[hh * 32 + c + 1]);
-          dk[c >> 1] = pack2<FP16>(d0, d1);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 f = sF4[hh * 8 + c4];
+          const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int c = 4 * c4 + e;
+            const float d0 = __uint_as_float(p[hh * 32 + c]) * (__uint_as_float(r[c]) - fv[e]);
+            const float d1 = __uint_as_float(p[hh * 32 + c + 1]) * (__uint_as_float(r[c + 1]) - fv[e + 1]);
+            dk[c >> 1] = pack2<FP16>(d0, d1);
+          }
         }
+        tmem_st16(slot + 32 + hh * 16, dk);  // dSᵀ (A operand of dK) next to Pᵀ
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4)
           st_shared_v4(adS + ((((hh * 4 + v4) ^ (row & 7))) << 4), dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2],
                        dk[4 * v4 + 3]);
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kDsFull + g]);
       if (!(ok = wait_bar_warp(&bars[kDqFull + g], u, abort_flag, a))) break;
@@ -396,7 +408,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kDqEmpty + g]);
         if (row < D) {  // lane = head-dim index d; columns = queries i0 .. i0 + 63
           const int nvalid = min(BR, sq.L1 - i0);
-          float* dst = a.dq_acc + row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 : 0), n1, a.N1, a.S1) * D + row;
+          float* dst = a.dq_acc +
+                       row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 : 0), n1, a.N1, a.S1) * D + row;
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (c < nvalid) red_add_f32(dst + c * i_stride, __uint_as_float(r0[c]));
