@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libfabwd.so")
 
-SOURCES = ["fabwd_api.cu", "fabwd_aux.cu", "fabwd_main_bf16.cu", "fabwd_main_fp16.cu"]
+SOURCES = ["fabwd_api.cu", "fabwd_aux.cu", "fabwd_main_bf16.cu", "fabwd_main_fp16.cu", "fabwd_static_ws.cu"]
 HEADERS = ["fabwd_ptx.cuh", "fabwd_internal.cuh", "fabwd_main.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
         L.fabwd_run.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run_main.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run_convert.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
+        L.fabwd_run_static_workspace.argtypes = [P, ctypes.c_void_p]
         L.fabwd_read_device_status.argtypes = [ctypes.c_void_p, sz, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
         L.fabwd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.fabwd_set_wait_limit_ns.restype = ctypes.c_uint64
@@ -74,7 +75,7 @@ def lib() -> ctypes.CDLL:
         L.fabwd_status_string.argtypes = [ctypes.c_int]
         L.fabwd_status_string.restype = ctypes.c_char_p
         for f in ("fabwd_workspace_size", "fabwd_workspace_layout", "fabwd_preprocess", "fabwd_run",
-                  "fabwd_run_main", "fabwd_run_convert", "fabwd_read_device_status"):
+                  "fabwd_run_main", "fabwd_run_convert", "fabwd_read_device_status", "fabwd_run_static_workspace"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -130,6 +131,13 @@ def fabwd_run_convert(p: fabwd_params, workspace: int, workspace_bytes: int, str
     s = lib().fabwd_run_convert(ctypes.byref(p), workspace, workspace_bytes, stream)
     if s != FABWD_OK:
         raise FabwdError(s, "fabwd_run_convert")
+
+
+def fabwd_run_static_workspace(p: fabwd_params, stream: int) -> None:
+    """Preprocess + main + convert with the library's fixed scratch array (no allocation)."""
+    s = lib().fabwd_run_static_workspace(ctypes.byref(p), stream)
+    if s != FABWD_OK:
+        raise FabwdError(s, "fabwd_run_static_workspace")
 
 
 def fabwd_read_device_status(workspace: int, workspace_bytes: int, stream: int):

@@ -158,6 +158,22 @@ int fabwd_debug_inject_timeout(int on);
 fabwd_status fabwd_workspace_layout(const fabwd_params* p, size_t* off_sfmg, size_t* off_lse2,
                                     size_t* off_dq_accum, int64_t* row_stride);
 
+/* Allocation-free form of fabwd_preprocess + fabwd_run (the pages have no counterpart; it is a
+ * convenience of this library).  For callers that cannot call cudaMalloc when they run the
+ * backward: code under a host framework that owns all device memory through its own pool (a
+ * foreign allocation can fail or fragment it), or a loop whose rules forbid allocation after
+ * start-up.  The caller still allocates and passes the inputs and the outputs dq, dk, dv; the
+ * scratch lives in a fixed 64 MiB array inside the library (held on every GPU that loads the
+ * library until the process exits).  A problem whose fabwd_workspace_size exceeds 64 MiB is
+ * refused with FABWD_ERR_WORKSPACE before anything is enqueued; other argument errors as
+ * fabwd_run.  Nothing is allocated: no cudaMalloc or cudaFree is called.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress, which may load the module)
+ * and caches it; make that first call before any stream capture.  Every call on a device shares
+ * the one array, which keeps the last call's contents (the kernels clear what must start at
+ * zero): calls whose work overlaps on the GPU (other streams, other threads) race and must be
+ * serialised by the caller.  Device-side status (FABWD_DEV_*) is not reported by this call. */
+fabwd_status fabwd_run_static_workspace(const fabwd_params* p, void* stream);
+
 /* Static description of a status code. */
 const char* fabwd_status_string(fabwd_status s);
 
