@@ -134,7 +134,9 @@ bool make_map(CUtensorMap* m, const void* base, bool fp16, int layout, long long
 }  // namespace
 
 namespace fabwd {
-bool main_supported(int D, int Dv) { return (D == 64 && Dv == 64) || (D == 128 && Dv == 128); }
+bool main_supported(int D, int Dv) {
+  return (D == 64 && Dv == 64) || (D == 128 && Dv == 128) || (D == 192 && Dv == 128);
+}
 }  // namespace fabwd
 
 extern "C" {

@@ -16,11 +16,14 @@
 // K is read K-major (Sᵀ) and MN-major (dQᵀ) from one shared-memory copy; Q and dO likewise
 // serve two products each, and dSᵀ serves dK (K-major) and dQᵀ (MN-major).
 //
-// Schedule.  Steps alternate between two TMEM slots (Sᵀ/Pᵀ and dPᵀ/dQᵀ per slot) and two compute
-// warpgroups: warpgroup g (warps 4g..4g+3, warp w reading TMEM lanes 32·(w%4)..+31) handles the
-// steps t ≡ g (mod 2).  The MMA warp issues, for step t, the Sᵀ/dPᵀ products of step t+1 (other
-// slot) and then dV, dK, dQᵀ of step t, so each warpgroup's softmax/dS work overlaps the other
-// slot's products.  Warp 8 streams Q, dO, lse and sfmg through a 4-stage ring (K and V once).
+// Schedule (D <= 128).  Steps alternate between two TMEM slots (Sᵀ/Pᵀ and dPᵀ/dQᵀ per slot) and
+// two compute warpgroups: warpgroup g (warps 4g..4g+3, warp w reading TMEM lanes 32·(w%4)..+31)
+// handles the steps t ≡ g (mod 2).  The MMA warp issues, for step t, the Sᵀ/dPᵀ products of step
+// t+1 (other slot) and then dV, dK, dQᵀ of step t, so each warpgroup's softmax/dS work overlaps
+// the other slot's products.  Warp 8 streams Q, dO, lse and sfmg through a 4-stage ring (K and V
+// once).  With D = 192 (dK alone takes 192 TMEM columns) there is one slot: both warpgroups work
+// on every step, 32 query columns each, and dQᵀ is two M = 128 products (head-dim rows 0..127
+// and 64..191, of which rows 128..191 are kept).
 //
 // TMEM columns: dK [0, D), dV [D, D+Dv), slot g at D+Dv+128g: Sᵀ [+0, +64) overwritten by Pᵀ
 // [+0, +32) and dSᵀ [+32, +64) (16-bit pairs), dPᵀ/dQᵀ [+64, +128).
@@ -44,20 +47,28 @@ constexpr int kMainThreads = 320;
 
 template <int D, int DV>
 struct MainCfg {
-  static constexpr int BR = kBlockQ, BC = kBlockKV, NS = 4;
+  static constexpr int BR = kBlockQ, BC = kBlockKV;
+  // Head dims up to 128 leave TMEM room for two slots (ping-pong between the warpgroups); D = 192
+  // (dK alone takes 192 columns) leaves room for one, which both warpgroups share, 32 query
+  // columns each.
+  static constexpr int NSLOT = D > 128 ? 1 : 2;
+  static constexpr int NC = NSLOT == 2 ? 64 : 32;       // query columns per compute thread per step
+  static constexpr int NS = D > 128 ? 3 : 4;            // Q/dO/lse/sfmg ring stages
+  static constexpr bool DQ2 = D > 128;                  // second dQᵀ product for head-dim rows 128..D-1
   static constexpr int DK = D < 128 ? 128 : D;  // K rows padded so dQᵀ = Kᵀ·dSᵀ has M = 128
   static constexpr uint32_t kK = DK * BC * 2, kV = DV * BC * 2, kQ = D * BR * 2, kdO = DV * BR * 2;
   static constexpr uint32_t kdS = BC * BR * 2;
   static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + NS * kQ, odS = odO + NS * kdO;
-  static constexpr uint32_t oL = odS + 2 * kdS;       // [NS][BR] fp32 lse·log2(e)
+  static constexpr uint32_t oL = odS + NSLOT * kdS;   // [NS][BR] fp32 lse·log2(e)
   static constexpr uint32_t oF = oL + NS * BR * 4;    // [NS][BR] fp32 sfmg
   static constexpr uint32_t oBar = oF + NS * BR * 4;  // mbarriers
   static constexpr uint32_t oMisc = oBar + 48 * 8;    // TMEM base holder, abort flag
   static constexpr uint32_t bytes = oMisc + 64;
   static constexpr uint32_t cDK = 0, cDV = D, cSlot = D + DV;  // slot g: cSlot + 128 g
+  static constexpr uint32_t cDQ2 = cSlot + 128 * NSLOT;       // second dQᵀ part (D = 192)
   static_assert(BR == 64, "the slot layout assumes 64-row q-blocks");
-  static_assert(D % 64 == 0 && DV % 64 == 0 && D <= 128 && DV <= 128, "head dims");
-  static_assert(cSlot + 256 <= 512, "TMEM budget");
+  static_assert(D % 64 == 0 && DV % 64 == 0 && (D <= 128 || (D == 192 && DV <= 128)) && DV <= D, "head dims");
+  static_assert(cDQ2 + (DQ2 ? 64 : 0) <= 512, "TMEM budget");
   static_assert(bytes <= 232448, "shared memory budget");
 };
 
@@ -160,9 +171,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      const bool four = (i >= kPFull && i < kPFull + 2) || (i >= kDsFull && i < kDsFull + 2) ||
-                        (i >= kDqEmpty && i < kDqEmpty + 2);
-      mbar_init(&bars[i], four ? 4 : 1);
+      const bool per_warp = (i >= kPFull && i < kPFull + 2) || (i >= kDsFull && i < kDsFull + 2) ||
+                            (i >= kDqEmpty && i < kDqEmpty + 2);
+      mbar_init(&bars[i], per_warp ? (C::NSLOT == 2 ? 4 : 8) : 1);  // one arrival per compute warp of the slot
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -240,9 +251,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       constexpr uint32_t ID_DK = idesc_f16(BC, D, kBF16, false, true);
       constexpr uint32_t ID_DQ = idesc_f16(128, BR, kBF16, true, true);
       const uint32_t aK = smem_u32(smem + C::oK), aV = smem_u32(smem + C::oV);
-      // Sᵀ(t) and dPᵀ(t) into slot t&1
+      // Sᵀ(t) and dPᵀ(t) into slot t % NSLOT
       auto issue_s_dp = [&](int t) -> bool {
-        const int g = t & 1, st = t % NS;
+        const int g = t % C::NSLOT, st = t % NS, use = t / C::NSLOT;
         const uint32_t aQ = smem_u32(smem + C::oQ + st * C::kQ), adO = smem_u32(smem + C::odO + st * C::kdO);
         const uint32_t slot = tmem + C::cSlot + g * 128;
         if (!wait_bar(&bars[kQFull + st], (t / NS) & 1, abort_flag, a)) return false;
@@ -252,7 +263,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_ss(slot, sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(aQ + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
         mma_commit(&bars[kSFull + g]);
-        if (t >= 2 && !wait_bar(&bars[kDqEmpty + g], ((t >> 1) - 1) & 1, abort_flag, a)) return false;
+        if (use >= 1 && !wait_bar(&bars[kDqEmpty + g], (use - 1) & 1, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
@@ -261,37 +272,53 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         mma_commit(&bars[kDpFull + g]);
         return true;
       };
+      // Pᵀ / dSᵀ TMEM columns of k-step kk (16 queries): with two slots one warpgroup owns all 64
+      // queries (Pᵀ at +0, dSᵀ at +32); with one slot warpgroup kk/2 owns 32 (Pᵀ at +0, dSᵀ at +16
+      // within its own 32 Sᵀ columns)
+      auto p_col = [](int kk) { return C::NSLOT == 2 ? kk * 8 : (kk >> 1) * 32 + (kk & 1) * 8; };
+      auto ds_col = [](int kk) { return C::NSLOT == 2 ? 32 + kk * 8 : (kk >> 1) * 32 + 16 + (kk & 1) * 8; };
       // dV, dK, dQᵀ of step t
       auto issue_grads = [&](int t) -> bool {
-        const int g = t & 1, st = t % NS;
+        const int g = t % C::NSLOT, st = t % NS;
         const uint32_t aQ = smem_u32(smem + C::oQ + st * C::kQ), adO = smem_u32(smem + C::odO + st * C::kdO);
         const uint32_t adS = smem_u32(smem + C::odS + g * C::kdS);
         const uint32_t slot = tmem + C::cSlot + g * 128;
-        const uint32_t u = (t >> 1) & 1;
+        const uint32_t u = (t / C::NSLOT) & 1;
         if (!wait_bar(&bars[kPFull + g], u, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BR / 16; ++kk)
-          mma_ts(tmem + C::cDV, slot + kk * 8, sdesc_sw128(adO + kk * 2048, BR * 128, 1024), ID_DV,
+          mma_ts(tmem + C::cDV, slot + p_col(kk), sdesc_sw128(adO + kk * 2048, BR * 128, 1024), ID_DV,
                  (t > 0 || kk > 0) ? 1u : 0u);
         if (!wait_bar(&bars[kDsFull + g], u, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BR / 16; ++kk)  // dSᵀ from TMEM (next to Pᵀ)
-          mma_ts(tmem + C::cDK, slot + 32 + kk * 8, sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK,
+          mma_ts(tmem + C::cDK, slot + ds_col(kk), sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK,
                  (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
           mma_ss(slot + 64, sdesc_sw128(aK + kk * 2048, BC * 128, 1024), sdesc_sw128(adS + kk * 2048, BC * 128, 1024),
                  ID_DQ, kk > 0);
+        if constexpr (C::DQ2) {  // head-dim rows 64..191 (rows 64..127 again; only 128..191 are used)
+#pragma unroll
+          for (int kk = 0; kk < BC / 16; ++kk)
+            mma_ss(tmem + C::cDQ2, sdesc_sw128(aK + BC * 128 + kk * 2048, BC * 128, 1024),
+                   sdesc_sw128(adS + kk * 2048, BC * 128, 1024), ID_DQ, kk > 0);
+        }
         mma_commit(&bars[kDqFull + g]);
         mma_commit(&bars[kQEmpty + st]);
         return true;
       };
       bool ok = wait_bar(&bars[kKvFull], 0, abort_flag, a) && issue_s_dp(0);
       for (int t = 0; ok && t < T; ++t) {
-        if (t + 1 < T && !(ok = issue_s_dp(t + 1))) break;
-        ok = issue_grads(t);
+        if (C::NSLOT == 2) {  // the other slot's Sᵀ/dPᵀ go first, overlapping this slot's dS work
+          if (t + 1 < T && !(ok = issue_s_dp(t + 1))) break;
+          ok = issue_grads(t);
+        } else {
+          if (!(ok = issue_grads(t))) break;
+          if (t + 1 < T) ok = issue_s_dp(t + 1);
+        }
       }
       if (ok) {
         mma_commit(&bars[kAccDone]);
@@ -306,35 +333,40 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const int q4 = warp & 3, g = warp >> 2;
     const int row = q4 * 32 + lane;  // TMEM lane: key row (Sᵀ, dPᵀ, dK, dV) or head-dim row (dQᵀ)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t slot = tmem + lane_off + C::cSlot + g * 128;
+    constexpr int NC = C::NC;
+    const int cb = C::NSLOT == 2 ? 0 : 32 * g;  // this warpgroup's first query column of a step
     const int jr = j0 + row;
     const bool j_valid = jr < sq.L2;
     const long long vlo = (long long)jr - off - hi, vhi = (long long)jr - off - lo;
     const int i_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
     const int i_vis_hi = (int)(vhi < -1 ? -1 : (vhi > (1 << 30) ? (1 << 30) : vhi));
-    const uint32_t adS = smem_u32(smem + C::odS + g * C::kdS) + row * 128;
+    const uint32_t adS_row = smem_u32(smem + C::odS) + row * 128;
     const long long i_stride = bnsd ? D : (long long)a.N1 * D;
     bool ok = true;
-    for (int t = g; t < T; t += 2) {
+    const int sg = C::NSLOT == 2 ? g : 0;  // the slot this warpgroup works on
+    const uint32_t slot = tmem + lane_off + C::cSlot + sg * 128;
+    const uint32_t adS = adS_row + sg * C::kdS;
+    constexpr int kTStep = C::NSLOT == 2 ? 2 : 1;
+    for (int t = C::NSLOT == 2 ? g : 0; t < T; t += kTStep) {
       const int st = t % NS;
-      const uint32_t u = (t >> 1) & 1;
+      const uint32_t u = (C::NSLOT == 2 ? (t >> 1) : t) & 1;
       const int h = t / nqb, qb = qb_begin + t % nqb;
       const int n1 = n2 * a.G + h, i0 = qb * BR;
       if (!(ok = wait_bar_warp(&bars[kQFull + st], (t / NS) & 1, abort_flag, a))) break;
-      if (!(ok = wait_bar_warp(&bars[kSFull + g], u, abort_flag, a))) break;
+      if (!(ok = wait_bar_warp(&bars[kSFull + sg], u, abort_flag, a))) break;
       tc_fence_after();
-      const float4* sL4 = reinterpret_cast<const float4*>(smem + C::oL + st * BR * 4);
-      const float4* sF4 = reinterpret_cast<const float4*>(smem + C::oF + st * BR * 4);
+      const float4* sL4 = reinterpret_cast<const float4*>(smem + C::oL + st * BR * 4 + cb * 4);
+      const float4* sF4 = reinterpret_cast<const float4*>(smem + C::oF + st * BR * 4 + cb * 4);
       const long long dmin = (long long)j0 - (i0 + BR - 1) - off, dmax = (long long)(j1 - 1) - i0 - off;
       const bool full = dmin >= lo && dmax <= hi;
-      uint32_t p[64];  // Sᵀ row, then P (fp32 bits)
-      tmem_ld32(slot, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-      tmem_ld32(slot + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
-      tmem_wait_ld();
-      reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-      reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      uint32_t p[NC];  // Sᵀ row, then P (fp32 bits)
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
+      for (int k = 0; k < NC / 32; ++k) tmem_ld32(slot + cb + 32 * k, *reinterpret_cast<uint32_t(*)[32]>(&p[32 * k]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < NC / 32; ++k) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[32 * k]));
+#pragma unroll
+      for (int c4 = 0; c4 < NC / 4; ++c4) {
         const float4 l = sL4[c4];
         const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
@@ -345,29 +377,31 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       if (!full) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (i0 + c < i_vis_lo || i0 + c > i_vis_hi) p[c] = 0u;
+        for (int c = 0; c < NC; ++c)
+          if (i0 + cb + c < i_vis_lo || i0 + cb + c > i_vis_hi) p[c] = 0u;
       }
       if (!j_valid) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = 0u;
+        for (int c = 0; c < NC; ++c) p[c] = 0u;
       }
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack2<FP16>(__uint_as_float(p[2 * c]), __uint_as_float(p[2 * c + 1]));
-        tmem_st32(slot, pk);
+        for (int c = 0; c < NC / 2; ++c) pk[c] = pack2<FP16>(__uint_as_float(p[2 * c]), __uint_as_float(p[2 * c + 1]));
+        if constexpr (NC == 64) tmem_st32(slot, pk);  // Pᵀ over this warpgroup's own Sᵀ columns
+        else tmem_st16(slot + cb, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
         tmem_wait_st();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kPFull + g]);
-      if (!(ok = wait_bar_warp(&bars[kDpFull + g], u, abort_flag, a))) break;
+      if (lane == 0) mbar_arrive(&bars[kPFull + sg]);
+      if (!(ok = wait_bar_warp(&bars[kDpFull + sg], u, abort_flag, a))) break;
       tc_fence_after();
+      const uint32_t ds_tmem = slot + (C::NSLOT == 2 ? 32 : cb + 16);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      for (int hh = 0; hh < NC / 32; ++hh) {
         uint32_t r[32];
-        tmem_ld32(slot + 64 + hh * 32, r);
+        tmem_ld32(slot + 64 + cb + hh * 32, r);
         tmem_wait_ld();
         reg_fence(r);
         uint32_t dk[16];
@@ -383,39 +417,61 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             dk[c >> 1] = pack2<FP16>(d0, d1);
           }
         }
-        tmem_st16(slot + 32 + hh * 16, dk);  // dSᵀ (A operand of dK) next to Pᵀ
+        tmem_st16(ds_tmem + hh * 16, dk);  // dSᵀ (A operand of dK) next to Pᵀ
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4)
-          st_shared_v4(adS + ((((hh * 4 + v4) ^ (row & 7))) << 4), dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2],
-                       dk[4 * v4 + 3]);
+          st_shared_v4(adS + ((((cb / 8 + hh * 4 + v4) ^ (row & 7))) << 4), dk[4 * v4], dk[4 * v4 + 1],
+                       dk[4 * v4 + 2], dk[4 * v4 + 3]);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kDsFull + g]);
-      if (!(ok = wait_bar_warp(&bars[kDqFull + g], u, abort_flag, a))) break;
+      if (lane == 0) mbar_arrive(&bars[kDsFull + sg]);
+      if (!(ok = wait_bar_warp(&bars[kDqFull + sg], u, abort_flag, a))) break;
       tc_fence_after();
       {
         uint32_t r0[32], r1[32];
-        tmem_ld32(slot + 64, r0);
-        tmem_ld32(slot + 96, r1);
+        tmem_ld32(slot + 64 + cb, r0);
+        if constexpr (NC == 64) tmem_ld32(slot + 96 + cb, r1);
         tmem_wait_ld();
         reg_fence(r0);
-        reg_fence(r1);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kDqEmpty + g]);
-        if (row < D) {  // lane = head-dim index d; columns = queries i0 .. i0 + 63
-          const int nvalid = min(BR, sq.L1 - i0);
+        if constexpr (NC == 64) reg_fence(r1);
+        if constexpr (!C::DQ2) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kDqEmpty + sg]);
+        }
+        const int nvalid = min(NC, sq.L1 - (i0 + cb));
+        if (row < D) {  // lane = head-dim index d; columns = queries i0 + cb .. + NC - 1
           float* dst = a.dq_acc +
-                       row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 : 0), n1, a.N1, a.S1) * D + row;
+                       row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 + cb : 0), n1, a.N1, a.S1) * D + row;
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (c < nvalid) red_add_f32(dst + c * i_stride, __uint_as_float(r0[c]));
+          if constexpr (NC == 64) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c + 32 < nvalid) red_add_f32(dst + (c + 32) * i_stride, __uint_as_float(r1[c]));
+            for (int c = 0; c < 32; ++c)
+              if (c + 32 < nvalid) red_add_f32(dst + (c + 32) * i_stride, __uint_as_float(r1[c]));
+          }
+        }
+        if constexpr (C::DQ2) {  // lanes 64..127 of the second part hold head-dim rows 128..191
+          if (q4 >= 2) {
+            tmem_ld32(tmem + lane_off + C::cDQ2 + cb, r0);
+            tmem_wait_ld();
+            reg_fence(r0);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kDqEmpty + sg]);
+          if (q4 >= 2) {
+            float* dst = a.dq_acc +
+                         row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 + cb : 0), n1, a.N1, a.S1) * D +
+                         64 + row;
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c < nvalid) red_add_f32(dst + c * i_stride, __uint_as_float(r0[c]));
+          }
         }
       }
     }
@@ -502,6 +558,7 @@ cudaError_t launch_main_dispatch(const MainArgs& a, const MainMaps& m, int D, in
                                  cudaStream_t st) {
   if (D == 64 && Dv == 64) return launch_main_t<64, 64, FP16>(a, m, n_kv_blocks, st);
   if (D == 128 && Dv == 128) return launch_main_t<128, 128, FP16>(a, m, n_kv_blocks, st);
+  if (D == 192 && Dv == 128) return launch_main_t<192, 128, FP16>(a, m, n_kv_blocks, st);
   return cudaErrorInvalidValue;
 }
 

@@ -102,6 +102,7 @@ def test_workspace_size_formula(lib):
     (dict(layout=F.FABWD_TND), F.FABWD_ERR_INVALID),                            # TND without cu_seqlens
     (dict(D=96, Dv=96), F.FABWD_ERR_UNSUPPORTED),    # valid per the statement, no kernel built
     (dict(D=128, Dv=64), F.FABWD_ERR_UNSUPPORTED),
+    (dict(D=192, Dv=192), F.FABWD_ERR_UNSUPPORTED),
 ])
 def test_validation_codes(lib, change, code):
     p = base_params(**change)

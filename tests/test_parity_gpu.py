@@ -65,6 +65,11 @@ SMALL = [
                                         win_left=-1, win_right=-1), ([200, 33, 129], [90, 300, 129])),
     ("tnd_causal_unequal", inputs.sized(W["varlen_window_fp16_d128"], B=3, N1=2, N2=1, win_left=-1),
      ([200, 33, 300], [150, 60, 300])),
+    ("d192_dv128_causal", inputs.sized(W["causal_s8192_d192_dv128"], N1=2, N2=2, S1=300, S2=300), None),
+    ("d192_dv128_gqa_fp16_band", inputs.sized(W["causal_s8192_d192_dv128"], dtype="fp16", N1=4, N2=2, S1=260,
+                                              S2=390, mask_mode=2, win_left=100, win_right=30), None),
+    ("d192_tnd", inputs.sized(W["varlen_window_fp16_d128"], D=192, Dv=128, B=3, N1=2, N2=2, win_left=64),
+     ([70, 1, 200], None)),
 ]
 
 
@@ -218,7 +223,8 @@ def _sample_rows(rng, seqs, heads, edges, n):
     return sorted(out)
 
 
-FULL = ["mha_s128_d64", "causal_b2_s2048_d128", "gqa_causal_s4096_d128", "varlen_window_fp16_d128"]
+FULL = ["mha_s128_d64", "causal_b2_s2048_d128", "gqa_causal_s4096_d128", "varlen_window_fp16_d128",
+        "causal_s8192_d192_dv128"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -262,9 +268,7 @@ def test_full_size_sampled(name):
 
 
 def test_unbuilt_head_dim_pair_is_unsupported():
-    w = W["causal_s8192_d192_dv128"]
-    q = torch.zeros(1, 256, 2, 192, dtype=torch.bfloat16, device="cuda")
-    v = torch.zeros(1, 256, 2, 128, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 256, 2, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(F.FabwdError) as ei:
-        api.flash_attn_grad(q, q, v, v, v, torch.zeros(1, 2, 256, device="cuda"), mask_mode=w.mask_mode)
+        api.flash_attn_grad(q, q, q, q, q, torch.zeros(1, 2, 256, device="cuda"), mask_mode=1)
     assert ei.value.status == F.FABWD_ERR_UNSUPPORTED
