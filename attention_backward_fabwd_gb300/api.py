@@ -24,6 +24,19 @@ class MaskMode(enum.IntEnum):
 
 
 _DTYPES = {torch.bfloat16: F.FABWD_BF16, torch.float16: F.FABWD_FP16}
+_DQ_MODES = {"auto": F.FABWD_DQ_AUTO, "atomic": F.FABWD_DQ_ATOMIC, "separate": F.FABWD_DQ_SEPARATE}
+
+
+def dq_mode_value(dq_mode: Union[int, str]) -> int:
+    """'auto' (0), 'atomic' (1: fp32 workspace + convert) or 'separate' (2: deterministic pass)."""
+    if isinstance(dq_mode, str):
+        try:
+            return _DQ_MODES[dq_mode.strip().lower()]
+        except KeyError:
+            raise ValueError(f"unknown dq_mode {dq_mode!r}") from None
+    return int(dq_mode)
+
+
 _LAYOUTS = {"BSND": F.FABWD_BSND, "TND": F.FABWD_TND, "BNSD": F.FABWD_BNSD}
 
 
@@ -43,7 +56,7 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 def make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, *, cu_seqlens_q=None, cu_seqlens_kv=None,
                 softmax_scale=0.0, mask_mode=0, win_left=-1, win_right=-1, max_seqlen_q=-1, max_seqlen_kv=-1,
-                layout="BSND") -> F.fabwd_params:
+                layout="BSND", dq_mode="auto") -> F.fabwd_params:
     """Fill fabwd_params from tensors (shapes give B, S1, S2, N1, N2, D, Dv, T1, T2)."""
     if layout not in _LAYOUTS:
         raise ValueError(f"layout must be one of {sorted(_LAYOUTS)}, got {layout!r}")
@@ -80,6 +93,7 @@ def make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, *, cu_seqlens_
     p.softmax_scale = float(softmax_scale)
     p.mask_mode = mask_mode_value(mask_mode)
     p.win_left, p.win_right = int(win_left), int(win_right)
+    p.dq_mode = dq_mode_value(dq_mode)
     p.dq, p.dk, p.dv = _ptr(dq), _ptr(dk), _ptr(dv)
     return p
 
@@ -103,7 +117,7 @@ def _check_tensors(q, k, v, dout, attn_out, softmax_lse, cu_q, cu_kv):
 def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_seqlens_kv=None, seqused_q=None,
                     seqused_kv=None, sinks=None, attn_mask=None, metadata=None, softmax_scale=0.0, mask_mode=0,
                     win_left=-1, win_right=-1, max_seqlen_q=-1, max_seqlen_kv=-1, layout_q="BSND",
-                    layout_kv="BSND", layout_out="BSND", *, check_status=False,
+                    layout_kv="BSND", layout_out="BSND", *, dq_mode="auto", check_status=False,
                     return_workspace=False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Gradients (dq, dk, dv) of attention from the saved attn_out and softmax_lse.
 
@@ -112,6 +126,8 @@ def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_
     is accepted and ignored, the GPU schedule is derived from the shapes.  The three layouts must
     agree ([FAG] §4.6).  Non-contiguous inputs are made contiguous.  With TND and
     max_seqlen_* = -1 the lengths are read from cu_seqlens on the host (a synchronisation).
+    dq_mode selects how dQ is formed: 'atomic' (fp32 reduce-adds into a workspace accumulator, then
+    a convert pass), 'separate' (a q-stationary pass, bitwise reproducible) or 'auto'.
     check_status=True synchronises and raises if the kernels reported a device-side problem.
     """
     if seqused_q is not None or seqused_kv is not None or sinks is not None or attn_mask is not None:
@@ -128,7 +144,7 @@ def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_
     p = make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, cu_seqlens_q=cu_seqlens_q,
                     cu_seqlens_kv=cu_seqlens_kv, softmax_scale=softmax_scale, mask_mode=mask_mode,
                     win_left=win_left, win_right=win_right, max_seqlen_q=max_seqlen_q,
-                    max_seqlen_kv=max_seqlen_kv, layout=layout_q)
+                    max_seqlen_kv=max_seqlen_kv, layout=layout_q, dq_mode=dq_mode)
     nbytes = F.fabwd_workspace_size(p)
     ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
     stream = torch.cuda.current_stream(q.device).cuda_stream

@@ -19,6 +19,7 @@ uint64_t g_wait_ns = 2000000000ull;
 int g_inject_timeout = 0;
 
 struct Plan {
+  bool separate = false;   // dQ by the q-stationary kernel (no fp32 accumulator, no atomics)
   long long S1p = 0;       // padded rows per (sequence, q-head)
   long long rowsQ = 0;     // q rows over all batches/sequences
   long long rowsK = 0;
@@ -47,6 +48,8 @@ fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
     return FABWD_ERR_INVALID;
   if (p->mask_mode == FABWD_MASK_NONE && (p->win_left >= 0 || p->win_right >= 0)) return FABWD_ERR_INVALID;
   if (!(p->softmax_scale == p->softmax_scale) || std::isinf(p->softmax_scale)) return FABWD_ERR_INVALID;
+  if (p->dq_mode != FABWD_DQ_AUTO && p->dq_mode != FABWD_DQ_ATOMIC && p->dq_mode != FABWD_DQ_SEPARATE)
+    return FABWD_ERR_INVALID;
   // TND requires cu_seqlens; the other layouts forbid them ([FAG] §4.6)
   const bool tnd = p->layout == FABWD_TND;
   if (tnd) {
@@ -63,7 +66,10 @@ fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
   pl->rowsK = tnd ? p->T2 : p->B * p->S2;
   pl->S1p = (p->S1 + kRowPad - 1) / kRowPad * kRowPad;
   pl->scale = p->softmax_scale != 0.0 ? p->softmax_scale : 1.0 / std::sqrt((double)p->D);
-  pl->dq_elems = pl->rowsQ * p->N1 * p->D;
+  // AUTO: the separate pass where it measured faster (D = 192, whose fused kernel has one TMEM
+  // slot and two dQᵀ products to reduce), the fused atomic pass otherwise
+  pl->separate = p->dq_mode == FABWD_DQ_SEPARATE || (p->dq_mode == FABWD_DQ_AUTO && p->D > 128);
+  pl->dq_elems = pl->separate ? 0 : pl->rowsQ * p->N1 * p->D;
   pl->off_status = 0;
   pl->off_lse2 = 256;
   const size_t rowbytes = round_up((size_t)p->B * p->N1 * pl->S1p * sizeof(float), 256);
@@ -194,58 +200,77 @@ fabwd_status fabwd_preprocess(const fabwd_params* p, void* ws, size_t ws_bytes, 
   return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+MainArgs main_args(const fabwd_params* p, const Plan& pl, uint8_t* w, int inject) {
+  MainArgs a;
+  a.layout = p->layout;
+  a.B = (int)p->B;
+  a.N1 = (int)p->N1;
+  a.N2 = (int)p->N2;
+  a.G = (int)(p->N1 / p->N2);
+  a.S1 = (int)p->S1;
+  a.S2 = (int)p->S2;
+  a.T1 = p->T1;
+  a.T2 = p->T2;
+  a.cu_q = p->cu_seqlens_q;
+  a.cu_kv = p->cu_seqlens_kv;
+  a.mask_mode = p->mask_mode;
+  a.win_left = (int)p->win_left;
+  a.win_right = (int)p->win_right;
+  a.scale = (float)pl.scale;
+  a.scale_log2 = (float)(pl.scale * 1.4426950408889634);
+  a.S1p = (int)pl.S1p;
+  a.lse2 = reinterpret_cast<const float*>(w + pl.off_lse2);
+  a.sfmg = reinterpret_cast<const float*>(w + pl.off_sfmg);
+  a.dq_acc = pl.separate ? nullptr : reinterpret_cast<float*>(w + pl.off_dqacc);
+  a.dq = p->dq;
+  a.dk = p->dk;
+  a.dv = p->dv;
+  a.status = reinterpret_cast<unsigned*>(w + pl.off_status);
+  a.wait_ns = g_wait_ns;
+  a.inject_timeout = inject;
+  return a;
+}
+
+bool any_pair(const fabwd_params* p, const Plan& pl) {
+  return pl.rowsQ > 0 && pl.rowsK > 0 && p->S1 > 0 && p->S2 > 0;
+}
+
+// Tensor maps with the given q-side and kv-side box heights.
+bool make_maps(const fabwd_params* p, MainMaps* maps, int q_rows, int kv_rows) {
+  const bool fp16 = p->dtype == FABWD_FP16, tnd = p->layout == FABWD_TND;
+  const long long Sq = tnd ? p->T1 : p->S1, Sk = tnd ? p->T2 : p->S2, Bn = tnd ? 1 : p->B;
+  return make_map(&maps->q, p->q, fp16, p->layout, p->D, p->N1, Sq, Bn, q_rows) &&
+         make_map(&maps->dout, p->dout, fp16, p->layout, p->Dv, p->N1, Sq, Bn, q_rows) &&
+         make_map(&maps->k, p->k, fp16, p->layout, p->D, p->N2, Sk, Bn, kv_rows) &&
+         make_map(&maps->v, p->v, fp16, p->layout, p->Dv, p->N2, Sk, Bn, kv_rows);
+}
+
+}  // namespace
+
+extern "C" {
+
 fabwd_status fabwd_run_main(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
   Plan pl;
   fabwd_status s = plan_and_check(p, &pl, true);
   if (s != FABWD_OK) return s;
   if ((s = check_ws(pl, ws, ws_bytes)) != FABWD_OK) return s;
-  uint8_t* w = static_cast<uint8_t*>(ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool fp16 = p->dtype == FABWD_FP16;
-  const bool tnd = p->layout == FABWD_TND;
   const int inject = g_inject_timeout;
   g_inject_timeout = 0;
-
-  if (pl.rowsQ > 0 && pl.rowsK > 0 && p->S1 > 0 && p->S2 > 0) {
+  if (any_pair(p, pl)) {
     MainMaps maps;
-    const long long Sq = tnd ? p->T1 : p->S1, Sk = tnd ? p->T2 : p->S2, Bn = tnd ? 1 : p->B;
-    if (!make_map(&maps.q, p->q, fp16, p->layout, p->D, p->N1, Sq, Bn, kBlockQ) ||
-        !make_map(&maps.dout, p->dout, fp16, p->layout, p->Dv, p->N1, Sq, Bn, kBlockQ) ||
-        !make_map(&maps.k, p->k, fp16, p->layout, p->D, p->N2, Sk, Bn, kBlockKV) ||
-        !make_map(&maps.v, p->v, fp16, p->layout, p->Dv, p->N2, Sk, Bn, kBlockKV))
-      return FABWD_ERR_CUDA;
-    MainArgs a;
-    a.layout = p->layout;
-    a.B = (int)p->B;
-    a.N1 = (int)p->N1;
-    a.N2 = (int)p->N2;
-    a.G = (int)(p->N1 / p->N2);
-    a.S1 = (int)p->S1;
-    a.S2 = (int)p->S2;
-    a.T1 = p->T1;
-    a.T2 = p->T2;
-    a.cu_q = p->cu_seqlens_q;
-    a.cu_kv = p->cu_seqlens_kv;
-    a.mask_mode = p->mask_mode;
-    a.win_left = (int)p->win_left;
-    a.win_right = (int)p->win_right;
-    a.scale = (float)pl.scale;
-    a.scale_log2 = (float)(pl.scale * 1.4426950408889634);
-    a.S1p = (int)pl.S1p;
-    a.lse2 = reinterpret_cast<const float*>(w + pl.off_lse2);
-    a.sfmg = reinterpret_cast<const float*>(w + pl.off_sfmg);
-    a.dq_acc = reinterpret_cast<float*>(w + pl.off_dqacc);
-    a.dk = p->dk;
-    a.dv = p->dv;
-    a.status = reinterpret_cast<unsigned*>(w + pl.off_status);
-    a.wait_ns = g_wait_ns;
-    a.inject_timeout = inject;
-    const int grid_x = (int)((p->S2 + kBlockKV - 1) / kBlockKV);
-    cudaError_t e = fp16 ? launch_main_fp16(a, maps, (int)p->D, (int)p->Dv, grid_x, st)
-                         : launch_main_bf16(a, maps, (int)p->D, (int)p->Dv, grid_x, st);
+    if (!make_maps(p, &maps, kBlockQ, kBlockKV)) return FABWD_ERR_CUDA;
+    const MainArgs a = main_args(p, pl, static_cast<uint8_t*>(ws), inject);
+    const int n_kv_blocks = (int)((p->S2 + kBlockKV - 1) / kBlockKV);
+    cudaError_t e = p->dtype == FABWD_FP16 ? launch_main_fp16(a, maps, (int)p->D, (int)p->Dv, n_kv_blocks, !pl.separate, st)
+                                           : launch_main_bf16(a, maps, (int)p->D, (int)p->Dv, n_kv_blocks, !pl.separate, st);
     if (e != cudaSuccess) return FABWD_ERR_CUDA;
   } else if (pl.rowsK > 0) {
-    // no visible pair at all: dk = dv = 0 (the convert kernel writes dq = 0)
+    // no visible pair at all: dk = dv = 0
     if (launch_zero(p->dk, pl.rowsK * p->N2 * p->D * 2, st) != cudaSuccess ||
         launch_zero(p->dv, pl.rowsK * p->N2 * p->Dv * 2, st) != cudaSuccess)
       return FABWD_ERR_CUDA;
@@ -253,25 +278,37 @@ fabwd_status fabwd_run_main(const fabwd_params* p, void* ws, size_t ws_bytes, vo
   return FABWD_OK;
 }
 
-fabwd_status fabwd_run_convert(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
+fabwd_status fabwd_run_dq(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
   Plan pl;
   fabwd_status s = plan_and_check(p, &pl, true);
   if (s != FABWD_OK) return s;
   if ((s = check_ws(pl, ws, ws_bytes)) != FABWD_OK) return s;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  ConvArgs c;
-  c.dq_acc = reinterpret_cast<const float*>(w + pl.off_dqacc);
-  c.dq = p->dq;
-  c.elems = pl.dq_elems;
-  c.scale = (float)pl.scale;
-  cudaError_t e = launch_convert(c, p->dtype == FABWD_FP16, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (!pl.separate) {
+    ConvArgs c;
+    c.dq_acc = reinterpret_cast<const float*>(w + pl.off_dqacc);
+    c.dq = p->dq;
+    c.elems = pl.dq_elems;
+    c.scale = (float)pl.scale;
+    e = launch_convert(c, p->dtype == FABWD_FP16, st);
+  } else if (any_pair(p, pl)) {
+    MainMaps maps;
+    if (!make_maps(p, &maps, kDqBlockQ, p->D > 128 ? 64 : 128)) return FABWD_ERR_CUDA;
+    const MainArgs a = main_args(p, pl, w, 0);
+    e = p->dtype == FABWD_FP16 ? launch_dq_fp16(a, maps, (int)p->D, (int)p->Dv, st)
+                               : launch_dq_bf16(a, maps, (int)p->D, (int)p->Dv, st);
+  } else if (pl.rowsQ > 0) {
+    e = launch_zero(p->dq, pl.rowsQ * p->N1 * p->D * 2, st);  // no visible pair: dq = 0
+  }
   return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
 }
 
 fabwd_status fabwd_run(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
   fabwd_status s = fabwd_run_main(p, ws, ws_bytes, stream);
   if (s != FABWD_OK) return s;
-  return fabwd_run_convert(p, ws, ws_bytes, stream);
+  return fabwd_run_dq(p, ws, ws_bytes, stream);
 }
 
 fabwd_status fabwd_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32_t* device_status) {

@@ -1,0 +1,314 @@
+// q-stationary dQ kernel for sm_103a (the deterministic dQ mode).
+//
+// What it computes is dQ of the page "CANN ops-transformer FlashAttnGrad 算子详解"
+// (discosf.com/news/4863418), §一: dQ = scale · dS · K with dS = P ⊙ (dP − sfmg),
+// P = exp(scale·QKᵀ − lse), dP = dY·Vᵀ.  One CTA owns 128 query rows of one q-head and loops
+// over the key blocks that row block can see:
+//     S  = Q·Kᵀ       tcgen05 (M = 128 queries, N = BN keys, K = D), double-buffered in TMEM
+//     dP = dO·Vᵀ      tcgen05 (K = Dv)
+//     dS = exp2(S·scale·log2e − lse·log2e) ⊙ (dP − sfmg), masked pairs -> 0, bf16/fp16 in TMEM
+//     dQ += dS·K      tcgen05, A operand read from TMEM, accumulated in TMEM over all key blocks
+// and writes dq = scale · dQ in the io dtype once.  Every dQ element is summed by one CTA in a
+// fixed order: no atomics, no fp32 workspace, bitwise reproducible.  dK and dV come from the
+// kv-stationary kernel run without its dQ product.  The lane of every TMEM accumulator is the
+// query row, so the per-row lse and sfmg are per-thread scalars.
+//
+// Warp roles (320 threads): warps 0-7 compute (warp w reads TMEM lanes 32·(w%4)..+31; warps 0-3
+// take key columns [0, BN/2), warps 4-7 [BN/2, BN)), warp 8 issues TMA loads (Q, dO once; K, V
+// through a 2-stage ring), warp 9 allocates TMEM and issues the MMAs.
+// TMEM columns: dQ [0, D), S buffer 0 [D, D+BN), S buffer 1 [D+BN, D+2BN), dP [D+2BN, D+3BN).
+// Every mbarrier wait is bounded as in the kv-stationary kernel.
+#pragma once
+
+#include "fabwd_internal.cuh"
+#include "fabwd_main.cuh"
+#include "fabwd_ptx.cuh"
+#include "../../include/fabwd.h"
+
+namespace fabwd {
+
+template <int D, int DV>
+struct DqCfg {
+  static constexpr int BM = 128;                 // query rows per CTA (TMEM lanes)
+  static constexpr int BN = D > 128 ? 64 : 128;  // keys per step
+  static constexpr int NS = 2;                   // K/V ring stages
+  static constexpr int NC = BN / 2;              // key columns per compute thread
+  static constexpr uint32_t kQ = D * BM * 2, kdO = DV * BM * 2, kK = D * BN * 2, kV = DV * BN * 2;
+  static constexpr uint32_t oQ = 0, odO = oQ + kQ, oK = odO + kdO, oV = oK + NS * kK;
+  static constexpr uint32_t oBar = oV + NS * kV;
+  static constexpr uint32_t oMisc = oBar + 32 * 8;
+  static constexpr uint32_t bytes = oMisc + 64;
+  static constexpr uint32_t cDQ = 0, cS0 = D, cP = D + 2 * BN;  // S buffer b at cS0 + b·BN
+  static_assert(cP + BN <= 512, "TMEM budget");
+  static_assert(bytes <= 232448, "shared memory budget");
+};
+
+constexpr int kDqQdoFull = 0, kDqKvFull = 1 /*+2*/, kDqKvEmpty = 3 /*+2*/, kDqSFull = 5 /*+2*/, kDqDpFull = 7,
+              kDqDsFull = 8, kDqAccDone = 9, kDqNever = 10, kDqDrain = 11, kDqNumBars = 12;
+
+template <int D, int DV, bool FP16>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    fabwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const MainArgs a) {
+  using C = DqCfg<D, DV>;
+  constexpr int BM = C::BM, BN = C::BN, NS = C::NS, NC = C::NC;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.y;
+  SeqRange sq;
+  if (!seq_range(a, b, sq)) return;  // bad cu_seqlens: the preprocess kernel reports it
+  const int nqb_all = (a.S1 + BM - 1) / BM;
+  const int qb = nqb_all - 1 - (int)(blockIdx.x / a.N1), n1 = blockIdx.x % a.N1;  // latest query blocks first
+  const int i0 = qb * BM;
+  if (i0 >= sq.L1) return;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) atomicOr(a.status, FABWD_DEV_INTERNAL);
+    return;
+  }
+  const int n2 = n1 / a.G;
+  const int i1 = min(i0 + BM, sq.L1);
+  const long long off = (long long)sq.L2 - sq.L1;
+  long long lo, hi;
+  mask_bounds(a, lo, hi);
+  // keys seen by at least one row of [i0, i1)
+  long long jb_ = (long long)i0 + off + lo, je_ = (long long)(i1 - 1) + off + hi;
+  if (jb_ < 0) jb_ = 0;
+  if (je_ > sq.L2 - 1) je_ = sq.L2 - 1;
+  const int kb_begin = jb_ <= je_ ? (int)(jb_ / BN) : 0;
+  const int T = jb_ <= je_ ? (int)(je_ / BN) + 1 - kb_begin : 0;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBar);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::oMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oMisc + 16);
+  if (tid == 0) {
+    for (int i = 0; i < kDqNumBars; ++i) mbar_init(&bars[i], i == kDqDsFull ? 8 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_do);
+  }
+  __syncwarp();
+  if (warp == 9) tmem_alloc(tm_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tm_holder;
+  if (a.inject_timeout) {
+    if (lane == 0) wait_bar(&bars[kDqNever], 0, abort_flag, a);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
+  const int q_row = (tnd ? sq.q0 : 0) + i0;
+  const int kv_rowbase = tnd ? sq.k0 : 0;
+  const int bcoord = tnd ? 0 : b;
+  constexpr bool kBF16 = !FP16;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && T > 0 && !*abort_flag) {
+      mbar_arrive_expect_tx(&bars[kDqQdoFull], (D + DV) * BM * 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_4d(smem + C::oQ + c * BM * 128, &tm_q, &bars[kDqQdoFull], c * 64, bnsd ? q_row : n1,
+                    bnsd ? n1 : q_row, bcoord);
+#pragma unroll
+      for (int c = 0; c < DV / 64; ++c)
+        tma_load_4d(smem + C::odO + c * BM * 128, &tm_do, &bars[kDqQdoFull], c * 64, bnsd ? q_row : n1,
+                    bnsd ? n1 : q_row, bcoord);
+      for (int t = 0; t < T; ++t) {
+        const int st = t % NS;
+        if (t >= NS && !wait_bar(&bars[kDqKvEmpty + st], ((t / NS) - 1) & 1, abort_flag, a)) break;
+        uint64_t* full = &bars[kDqKvFull + st];
+        mbar_arrive_expect_tx(full, (D + DV) * BN * 2);
+        const int row = kv_rowbase + (kb_begin + t) * BN;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(smem + C::oK + st * C::kK + c * BN * 128, &tm_k, full, c * 64, bnsd ? row : n2, bnsd ? n2 : row,
+                      bcoord);
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_4d(smem + C::oV + st * C::kV + c * BN * 128, &tm_v, full, c * 64, bnsd ? row : n2,
+                      bnsd ? n2 : row, bcoord);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t ID_S = idesc_f16(BM, BN, kBF16, false, false);
+      constexpr uint32_t ID_DQ = idesc_f16(BM, D, kBF16, false, true);
+      const uint32_t aQ = smem_u32(smem + C::oQ), adO = smem_u32(smem + C::odO);
+      auto issue_s = [&](int t) -> bool {
+        const int st = t % NS;
+        const uint32_t aK = smem_u32(smem + C::oK + st * C::kK);
+        if (!wait_bar(&bars[kDqKvFull + st], (t / NS) & 1, abort_flag, a)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::cS0 + (t & 1) * BN, sdesc_sw128(aQ + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(aK + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+        mma_commit(&bars[kDqSFull + (t & 1)]);
+        return true;
+      };
+      auto issue_dp = [&](int t) {
+        const uint32_t aV = smem_u32(smem + C::oV + (t % NS) * C::kV);
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_ss(tmem + C::cP, sdesc_sw128(adO + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(aV + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+        mma_commit(&bars[kDqDpFull]);
+      };
+      bool ok = wait_bar(&bars[kDqQdoFull], 0, abort_flag, a) && issue_s(0);
+      if (ok) issue_dp(0);
+      for (int t = 0; ok && t < T; ++t) {
+        // S of the next key block into the other buffer (its dS was consumed by the previous dQ product)
+        if (t + 1 < T && !(ok = issue_s(t + 1))) break;
+        if (!(ok = wait_bar(&bars[kDqDsFull], t & 1, abort_flag, a))) break;
+        tc_fence_after();
+        const uint32_t aK = smem_u32(smem + C::oK + (t % NS) * C::kK);
+        const uint32_t sb = tmem + C::cS0 + (t & 1) * BN;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)  // dS of warpgroup kk/(NC/16) sits in its own S columns
+          mma_ts(tmem + C::cDQ, sb + (kk / (NC / 16)) * NC + (kk % (NC / 16)) * 8,
+                 sdesc_sw128(aK + kk * 2048, BN * 128, 1024), ID_DQ, (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kDqKvEmpty + (t % NS)]);
+        if (t + 1 < T) issue_dp(t + 1);  // dP was read before the dS arrival awaited above
+      }
+      if (ok) {
+        mma_commit(&bars[kDqAccDone]);
+      } else {
+        mma_commit(&bars[kDqDrain]);
+        mbar_wait(&bars[kDqDrain], 0, kDrainNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ compute warpgroups 0, 1
+    const int q4 = warp & 3, g = warp >> 2;
+    const int row = q4 * 32 + lane;  // TMEM lane = query row i0 + row
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int ir = i0 + row;
+    const float* lse2_row = a.lse2 + ((long long)b * a.N1 + n1) * a.S1p;
+    const float* sfmg_row = a.sfmg + ((long long)b * a.N1 + n1) * a.S1p;
+    const float lse2 = lse2_row[ir];  // +inf beyond the sequence: P = 0 there
+    const float sf = sfmg_row[ir];
+    // keys visible to this row: j - ir - off in [lo, hi]
+    const long long vlo = (long long)ir + off + lo, vhi = (long long)ir + off + hi;
+    const int j_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
+    const int j_vis_hi = (int)min((long long)sq.L2 - 1, vhi < -1 ? -1ll : (vhi > (1 << 30) ? (long long)(1 << 30) : vhi));
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int j0 = (kb_begin + t) * BN;
+      const uint32_t sb = tmem + lane_off + C::cS0 + (t & 1) * BN + g * NC;
+      const long long dmin = (long long)j0 - (i0 + BM - 1) - off, dmax = (long long)(j0 + BN - 1) - i0 - off;
+      const bool full = j0 + BN <= sq.L2 && dmin >= lo && dmax <= hi;
+      if (!(ok = wait_bar_warp(&bars[kDqSFull + (t & 1)], (t >> 1) & 1, abort_flag, a))) break;
+      tc_fence_after();
+      uint32_t p[NC];
+      tmem_ld32(sb, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+      if constexpr (NC == 64) tmem_ld32(sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      tmem_wait_ld();
+      reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+      if constexpr (NC == 64) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+#pragma unroll
+      for (int c = 0; c < NC; ++c) p[c] = __float_as_uint(ex2(fmaf(__uint_as_float(p[c]), a.scale_log2, -lse2)));
+      if (!full) {
+        const int jc = j0 + g * NC;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          if (jc + c < j_vis_lo || jc + c > j_vis_hi) p[c] = 0u;
+      }
+      if (!(ok = wait_bar_warp(&bars[kDqDpFull], t & 1, abort_flag, a))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int hh = 0; hh < NC / 32; ++hh) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cP + g * NC + hh * 32, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t ds[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          ds[c >> 1] = pack2<FP16>(__uint_as_float(p[hh * 32 + c]) * (__uint_as_float(r[c]) - sf),
+                                   __uint_as_float(p[hh * 32 + c + 1]) * (__uint_as_float(r[c + 1]) - sf));
+        tmem_st16(sb + hh * 16, ds);  // dS over this warpgroup's own (already read) S columns
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kDqDsFull]);
+    }
+    // ---- epilogue: dq = scale · dQ (zeros when the row block sees no key)
+    if (ok && T > 0) ok = wait_bar_warp(&bars[kDqAccDone], 0, abort_flag, a);
+    if (ok) {
+      tc_fence_after();
+      const bool i_valid = ir < sq.L1;
+      const long long qrow = row_index(a.layout, b, (long long)(tnd ? sq.q0 : 0) + (i_valid ? ir : 0), n1, a.N1, a.S1);
+      uint16_t* dq = static_cast<uint16_t*>(a.dq) + qrow * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = g * (D / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cDQ + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * a.scale, __uint_as_float(r[e + 1]) * a.scale) : 0u;
+        if (i_valid) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            *reinterpret_cast<uint4*>(dq + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kGraceNs) {
+    }
+  }
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int DV, bool FP16>
+cudaError_t launch_dq_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) {
+  using C = DqCfg<D, DV>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fabwd_dq_kernel<D, DV, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::bytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B);
+  fabwd_dq_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
+  return cudaGetLastError();
+}
+
+template <bool FP16>
+cudaError_t launch_dq_dispatch(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st) {
+  if (D == 64 && Dv == 64) return launch_dq_t<64, 64, FP16>(a, m, st);
+  if (D == 128 && Dv == 128) return launch_dq_t<128, 128, FP16>(a, m, st);
+  if (D == 192 && Dv == 128) return launch_dq_t<192, 128, FP16>(a, m, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fabwd

@@ -10,6 +10,7 @@ namespace fabwd {
 constexpr int kBlockKV = 128;  // kv rows per CTA of the main kernel (M of the kv-side MMAs)
 constexpr int kBlockQ = 64;    // q rows per main-loop step (N of S^T / dP^T / dQ^T)
 constexpr int kRowPad = 128;   // padding of the per-(sequence, q-head) lse2 / sfmg rows
+constexpr int kDqBlockQ = 128; // q rows per CTA of the q-stationary dQ kernel
 
 enum Layout : int { kBSND = 0, kTND = 1, kBNSD = 2 };
 
@@ -56,7 +57,8 @@ struct MainArgs {
   int S1p;
   const float* lse2;
   const float* sfmg;
-  float* dq_acc;
+  float* dq_acc;              // fp32 accumulator (atomic dQ mode), else null
+  void* dq;                   // io-dtype dq (written by the q-stationary dQ kernel)
   void* dk;
   void* dv;
   unsigned* status;
@@ -72,9 +74,14 @@ cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st);
 cudaError_t launch_convert(const ConvArgs& a, bool fp16, cudaStream_t st);
 // Zero `bytes` (a multiple of 16) at a 16-byte-aligned device address.
 cudaError_t launch_zero(void* p, long long bytes, cudaStream_t st);
-// Returns cudaErrorInvalidValue when no kernel is built for (D, Dv).
-cudaError_t launch_main_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int grid_x, cudaStream_t st);
-cudaError_t launch_main_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int grid_x, cudaStream_t st);
+// Return cudaErrorInvalidValue when no kernel is built for (D, Dv).  fused: the kv-stationary
+// kernel also reduces dQ into the fp32 accumulator; otherwise it writes dK, dV only.
+cudaError_t launch_main_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, bool fused,
+                             cudaStream_t st);
+cudaError_t launch_main_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, bool fused,
+                             cudaStream_t st);
+cudaError_t launch_dq_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
+cudaError_t launch_dq_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
 bool main_supported(int D, int Dv);
 
 }  // namespace fabwd

@@ -45,7 +45,7 @@ constexpr unsigned long long kDrainNs = 100ull * 1000ull * 1000ull;  // 100 ms
 constexpr unsigned long long kGraceNs = 2ull * 1000ull * 1000ull;    // 2 ms
 constexpr int kMainThreads = 320;
 
-template <int D, int DV>
+template <int D, int DV, bool FUSED>
 struct MainCfg {
   static constexpr int BR = kBlockQ, BC = kBlockKV;
   // Head dims up to 128 leave TMEM room for two slots (ping-pong between the warpgroups); D = 192
@@ -54,12 +54,12 @@ struct MainCfg {
   static constexpr int NSLOT = D > 128 ? 1 : 2;
   static constexpr int NC = NSLOT == 2 ? 64 : 32;       // query columns per compute thread per step
   static constexpr int NS = D > 128 ? 3 : 4;            // Q/dO/lse/sfmg ring stages
-  static constexpr bool DQ2 = D > 128;                  // second dQᵀ product for head-dim rows 128..D-1
-  static constexpr int DK = D < 128 ? 128 : D;  // K rows padded so dQᵀ = Kᵀ·dSᵀ has M = 128
+  static constexpr bool DQ2 = FUSED && D > 128;         // second dQᵀ product for head-dim rows 128..D-1
+  static constexpr int DK = FUSED && D < 128 ? 128 : D;  // K rows padded so dQᵀ = Kᵀ·dSᵀ has M = 128
   static constexpr uint32_t kK = DK * BC * 2, kV = DV * BC * 2, kQ = D * BR * 2, kdO = DV * BR * 2;
   static constexpr uint32_t kdS = BC * BR * 2;
   static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + NS * kQ, odS = odO + NS * kdO;
-  static constexpr uint32_t oL = odS + NSLOT * kdS;   // [NS][BR] fp32 lse·log2(e)
+  static constexpr uint32_t oL = odS + (FUSED ? NSLOT * kdS : 0);  // [NS][BR] fp32 lse·log2(e)
   static constexpr uint32_t oF = oL + NS * BR * 4;    // [NS][BR] fp32 sfmg
   static constexpr uint32_t oBar = oF + NS * BR * 4;  // mbarriers
   static constexpr uint32_t oMisc = oBar + 48 * 8;    // TMEM base holder, abort flag
@@ -133,12 +133,14 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, vo
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, int DV, bool FP16>
+// FUSED: also compute dQᵀ and reduce it into the fp32 workspace accumulator (atomic dQ mode);
+// otherwise the kernel produces dK and dV only and a separate q-stationary kernel computes dQ.
+template <int D, int DV, bool FP16, bool FUSED>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const MainArgs a) {
-  using C = MainCfg<D, DV>;
+  using C = MainCfg<D, DV, FUSED>;
   constexpr int BR = C::BR, BC = C::BC, NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -263,7 +265,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_ss(slot, sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(aQ + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
         mma_commit(&bars[kSFull + g]);
-        if (use >= 1 && !wait_bar(&bars[kDqEmpty + g], (use - 1) & 1, abort_flag, a)) return false;
+        // dPᵀ reuses the slot's dPᵀ/dQᵀ columns: wait until the previous dQᵀ was read (without
+        // dQ, the compute warps read the previous dPᵀ before their dS arrival, already awaited)
+        if (FUSED && use >= 1 && !wait_bar(&bars[kDqEmpty + g], (use - 1) & 1, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
@@ -296,17 +300,19 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int kk = 0; kk < BR / 16; ++kk)  // dSᵀ from TMEM (next to Pᵀ)
           mma_ts(tmem + C::cDK, slot + ds_col(kk), sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK,
                  (t > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk)
-          mma_ss(slot + 64, sdesc_sw128(aK + kk * 2048, BC * 128, 1024), sdesc_sw128(adS + kk * 2048, BC * 128, 1024),
-                 ID_DQ, kk > 0);
-        if constexpr (C::DQ2) {  // head-dim rows 64..191 (rows 64..127 again; only 128..191 are used)
+        if constexpr (FUSED) {
 #pragma unroll
           for (int kk = 0; kk < BC / 16; ++kk)
-            mma_ss(tmem + C::cDQ2, sdesc_sw128(aK + BC * 128 + kk * 2048, BC * 128, 1024),
-                   sdesc_sw128(adS + kk * 2048, BC * 128, 1024), ID_DQ, kk > 0);
+            mma_ss(slot + 64, sdesc_sw128(aK + kk * 2048, BC * 128, 1024), sdesc_sw128(adS + kk * 2048, BC * 128, 1024),
+                   ID_DQ, kk > 0);
+          if constexpr (C::DQ2) {  // head-dim rows 64..191 (rows 64..127 again; only 128..191 are used)
+#pragma unroll
+            for (int kk = 0; kk < BC / 16; ++kk)
+              mma_ss(tmem + C::cDQ2, sdesc_sw128(aK + BC * 128 + kk * 2048, BC * 128, 1024),
+                     sdesc_sw128(adS + kk * 2048, BC * 128, 1024), ID_DQ, kk > 0);
+          }
+          mma_commit(&bars[kDqFull + g]);
         }
-        mma_commit(&bars[kDqFull + g]);
         mma_commit(&bars[kQEmpty + st]);
         return true;
       };
@@ -418,16 +424,19 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           }
         }
         tmem_st16(ds_tmem + hh * 16, dk);  // dSᵀ (A operand of dK) next to Pᵀ
+        if constexpr (FUSED) {  // dSᵀ also in shared memory: the B operand of dQᵀ
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4)
-          st_shared_v4(adS + ((((cb / 8 + hh * 4 + v4) ^ (row & 7))) << 4), dk[4 * v4], dk[4 * v4 + 1],
-                       dk[4 * v4 + 2], dk[4 * v4 + 3]);
+          for (int v4 = 0; v4 < 4; ++v4)
+            st_shared_v4(adS + ((((cb / 8 + hh * 4 + v4) ^ (row & 7))) << 4), dk[4 * v4], dk[4 * v4 + 1],
+                         dk[4 * v4 + 2], dk[4 * v4 + 3]);
+        }
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
+      if constexpr (FUSED) fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kDsFull + sg]);
+      if constexpr (!FUSED) continue;
       if (!(ok = wait_bar_warp(&bars[kDqFull + sg], u, abort_flag, a))) break;
       tc_fence_after();
       {
@@ -536,12 +545,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   }
 }
 
-template <int D, int DV, bool FP16>
+template <int D, int DV, bool FP16, bool FUSED>
 cudaError_t launch_main_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
-  using C = MainCfg<D, DV>;
+  using C = MainCfg<D, DV, FUSED>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fabwd_main_kernel<D, DV, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fabwd_main_kernel<D, DV, FP16, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::bytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -549,16 +558,16 @@ cudaError_t launch_main_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks,
   // blockIdx.x = kv-block * N2 + kv-head: the heaviest kv-blocks (earliest keys under a causal
   // mask) of every head launch first.
   dim3 grid(n_kv_blocks * a.N2, a.B);
-  fabwd_main_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
+  fabwd_main_kernel<D, DV, FP16, FUSED><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
   return cudaGetLastError();
 }
 
-template <bool FP16>
+template <bool FP16, bool FUSED>
 cudaError_t launch_main_dispatch(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks,
                                  cudaStream_t st) {
-  if (D == 64 && Dv == 64) return launch_main_t<64, 64, FP16>(a, m, n_kv_blocks, st);
-  if (D == 128 && Dv == 128) return launch_main_t<128, 128, FP16>(a, m, n_kv_blocks, st);
-  if (D == 192 && Dv == 128) return launch_main_t<192, 128, FP16>(a, m, n_kv_blocks, st);
+  if (D == 64 && Dv == 64) return launch_main_t<64, 64, FP16, FUSED>(a, m, n_kv_blocks, st);
+  if (D == 128 && Dv == 128) return launch_main_t<128, 128, FP16, FUSED>(a, m, n_kv_blocks, st);
+  if (D == 192 && Dv == 128) return launch_main_t<192, 128, FP16, FUSED>(a, m, n_kv_blocks, st);
   return cudaErrorInvalidValue;
 }
 

@@ -19,7 +19,8 @@ FABWD_ERR_WORKSPACE, FABWD_ERR_CUDA, FABWD_ERR_TIMEOUT, FABWD_ERR_DEVICE = 4, 5,
 FABWD_BF16, FABWD_FP16 = 0, 1
 FABWD_BSND, FABWD_TND, FABWD_BNSD = 0, 1, 2
 FABWD_MASK_NONE, FABWD_MASK_CAUSAL, FABWD_MASK_BAND = 0, 1, 2
-FABWD_DEV_TIMEOUT, FABWD_DEV_BAD_SEQLENS = 0x1, 0x2
+FABWD_DEV_TIMEOUT, FABWD_DEV_BAD_SEQLENS, FABWD_DEV_INTERNAL = 0x1, 0x2, 0x4
+FABWD_DQ_AUTO, FABWD_DQ_ATOMIC, FABWD_DQ_SEPARATE = 0, 1, 2
 
 HEADER = os.path.join(_build.ROOT, "include", "fabwd.h")
 
@@ -36,7 +37,7 @@ class fabwd_params(ctypes.Structure):
         ("dout", ctypes.c_void_p), ("attn_out", ctypes.c_void_p), ("softmax_lse", ctypes.c_void_p),
         ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_kv", ctypes.c_void_p),
         ("softmax_scale", ctypes.c_double),
-        ("mask_mode", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("mask_mode", ctypes.c_int32), ("dq_mode", ctypes.c_int32),
         ("win_left", ctypes.c_int64), ("win_right", ctypes.c_int64),
         ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
     ]
@@ -66,7 +67,7 @@ def lib() -> ctypes.CDLL:
         L.fabwd_preprocess.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run_main.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
-        L.fabwd_run_convert.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
+        L.fabwd_run_dq.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run_static_workspace.argtypes = [P, ctypes.c_void_p]
         L.fabwd_read_device_status.argtypes = [ctypes.c_void_p, sz, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
         L.fabwd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -75,7 +76,7 @@ def lib() -> ctypes.CDLL:
         L.fabwd_status_string.argtypes = [ctypes.c_int]
         L.fabwd_status_string.restype = ctypes.c_char_p
         for f in ("fabwd_workspace_size", "fabwd_workspace_layout", "fabwd_preprocess", "fabwd_run",
-                  "fabwd_run_main", "fabwd_run_convert", "fabwd_read_device_status", "fabwd_run_static_workspace"):
+                  "fabwd_run_main", "fabwd_run_dq", "fabwd_read_device_status", "fabwd_run_static_workspace"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -127,10 +128,10 @@ def fabwd_run_main(p: fabwd_params, workspace: int, workspace_bytes: int, stream
         raise FabwdError(s, "fabwd_run_main")
 
 
-def fabwd_run_convert(p: fabwd_params, workspace: int, workspace_bytes: int, stream: int) -> None:
-    s = lib().fabwd_run_convert(ctypes.byref(p), workspace, workspace_bytes, stream)
+def fabwd_run_dq(p: fabwd_params, workspace: int, workspace_bytes: int, stream: int) -> None:
+    s = lib().fabwd_run_dq(ctypes.byref(p), workspace, workspace_bytes, stream)
     if s != FABWD_OK:
-        raise FabwdError(s, "fabwd_run_convert")
+        raise FabwdError(s, "fabwd_run_dq")
 
 
 def fabwd_run_static_workspace(p: fabwd_params, stream: int) -> None:

@@ -3,7 +3,7 @@
 
 One step = one pass of the whole backward path over one batch of synthetic input:
 fabwd_preprocess (sfmg, lse rows, dq accumulator zeroing) -> fabwd_run_main (tcgen05 backward
-kernel) -> fabwd_run_convert (dq cast), all libfabwd kernels on one stream.
+kernel) -> fabwd_run_dq (dQ stage), all libfabwd kernels on one stream.
 
 Flops follow the measurement convention: per head 2·S1·S2·(3D + 2Dv), halved under a causal
 mask; the roofline uses the algorithmic count 2·(3D + 2Dv) per visible (query, key) pair.
@@ -43,6 +43,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["fabwd", "reference"], default="fabwd")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--dq-mode", default="auto", choices=["auto", "atomic", "separate"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -296,7 +297,7 @@ def gpu_arm(args, rank, world, local_rank):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     p = api.make_params(q, k, v, dout, attn_out, lse, dq, dk, dv, cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv,
                         softmax_scale=w.softmax_scale, mask_mode=w.mask_mode, win_left=w.win_left,
-                        win_right=w.win_right, layout=w.layout, **extra)
+                        win_right=w.win_right, layout=w.layout, dq_mode=args.dq_mode, **extra)
     nbytes = fabwd.fabwd_workspace_size(p)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     st = torch.cuda.current_stream(dev)
@@ -312,7 +313,7 @@ def gpu_arm(args, rank, world, local_rank):
         fabwd.fabwd_run_main(p, ws.data_ptr(), nbytes, sp)
         if evs:
             evs[2].record(st)
-        fabwd.fabwd_run_convert(p, ws.data_ptr(), nbytes, sp)
+        fabwd.fabwd_run_dq(p, ws.data_ptr(), nbytes, sp)
         if evs:
             evs[3].record(st)
 

@@ -71,6 +71,18 @@ typedef enum { FABWD_BSND = 0, FABWD_TND = 1, FABWD_BNSD = 2 } fabwd_layout;
  * intersect.  S1/S2 here are the lengths of the sequence the pair belongs to. */
 typedef enum { FABWD_MASK_NONE = 0, FABWD_MASK_CAUSAL = 1, FABWD_MASK_BAND = 2 } fabwd_mask;
 
+/* How dQ is produced.
+ *   FABWD_DQ_ATOMIC:   the kv-stationary kernel reduce-adds fp32 dQ partials into the workspace
+ *                      and a convert pass casts scale · accumulator (the fp32-workspace dQ of
+ *                      [FAG] §5.2's bn2gs1s2 template); summation order varies between runs.
+ *   FABWD_DQ_SEPARATE: the kv-stationary kernel produces dK and dV only; a q-stationary kernel
+ *                      recomputes S and dP per query block and accumulates dQ in tensor memory,
+ *                      without atomics: bitwise reproducible, no fp32 accumulator in the
+ *                      workspace, about 1.4x the tensor-core work.
+ *   FABWD_DQ_AUTO:     the library's choice: SEPARATE for D > 128, ATOMIC otherwise (the faster
+ *                      mode on the measured workloads). */
+typedef enum { FABWD_DQ_AUTO = 0, FABWD_DQ_ATOMIC = 1, FABWD_DQ_SEPARATE = 2 } fabwd_dq_mode;
+
 /* Device status bits (fabwd_read_device_status). */
 #define FABWD_DEV_TIMEOUT 0x1u     /* a bounded mbarrier wait gave up; outputs are not valid */
 #define FABWD_DEV_BAD_SEQLENS 0x2u /* cu_seqlens not non-decreasing from 0, or beyond T / max */
@@ -96,7 +108,7 @@ typedef struct {
   const int32_t* cu_seqlens_kv;  /* device, B+1 entries, TND only (NULL otherwise) */
   double softmax_scale;          /* 0 -> 1/sqrt(D) ([FAG] §一 scale rule) */
   int32_t mask_mode;             /* fabwd_mask */
-  int32_t reserved0;
+  int32_t dq_mode;               /* fabwd_dq_mode (0 = auto) */
   int64_t win_left, win_right;   /* -1 = unbounded */
   /* Outputs: device pointers, caller-allocated, shapes of q/k/v, io dtype ([FAG] §2.2). */
   void* dq;
@@ -107,8 +119,8 @@ typedef struct {
 /* Host only.  Validates p (the same checks as fabwd_run, pointers excepted) and returns in
  * *bytes the workspace size fabwd_preprocess/fabwd_run need.  The workspace holds a status
  * word, the fp32 sfmg and log2-scaled lse rows padded per (sequence, q-head) to a multiple of
- * 128, and the fp32 dq accumulator (q's shape with D).  Errors: NULLPTR (p or bytes NULL),
- * INVALID, UNSUPPORTED. */
+ * 128, and, in FABWD_DQ_ATOMIC mode only, the fp32 dq accumulator (q's shape with D).  Errors:
+ * NULLPTR (p or bytes NULL), INVALID, UNSUPPORTED. */
 fabwd_status fabwd_workspace_size(const fabwd_params* p, size_t* bytes);
 
 /* Enqueue on `stream` (a cudaStream_t; NULL = the legacy default stream) the preprocess kernel
@@ -118,21 +130,22 @@ fabwd_status fabwd_workspace_size(const fabwd_params* p, size_t* bytes);
 fabwd_status fabwd_preprocess(const fabwd_params* p, void* workspace, size_t workspace_bytes,
                               void* stream);
 
-/* Enqueue on `stream` the main backward kernel (dK, dV written to dk/dv; dQ partial sums
- * added into the workspace accumulator) and the convert kernel (dq = scale · accumulator, cast
- * to the io dtype).  Must follow fabwd_preprocess with the same p and workspace on the same
- * stream.  Errors: as fabwd_preprocess.  A TIMEOUT or bad-seqlens condition found on the
+/* Enqueue on `stream` the kv-stationary backward kernel (dK, dV written to dk/dv; in atomic
+ * mode also the dQ partial sums added into the workspace accumulator) and the dQ stage (atomic
+ * mode: the convert kernel, dq = cast(scale · accumulator); separate mode: the q-stationary dQ
+ * kernel).  Must follow fabwd_preprocess with the same p and workspace on the same stream.  Errors: as fabwd_preprocess.  A TIMEOUT or bad-seqlens condition found on the
  * device shows up in fabwd_read_device_status, not here. */
 fabwd_status fabwd_run(const fabwd_params* p, void* workspace, size_t workspace_bytes,
                        void* stream);
 
 /* The two halves of fabwd_run, for callers that schedule or time them separately:
- * fabwd_run_main enqueues only the main backward kernel (dk, dv written; dQ partials added into
- * the workspace accumulator); fabwd_run_convert enqueues only the convert kernel
- * (dq = cast(scale · accumulator)).  fabwd_run == fabwd_run_main then fabwd_run_convert.
+ * fabwd_run_main enqueues the kv-stationary kernel (dk, dv; atomic mode: dQ partials into the
+ * workspace accumulator); fabwd_run_dq enqueues the dQ stage (atomic mode: the convert kernel;
+ * separate mode: the q-stationary dQ kernel, which needs only the preprocess outputs and may run
+ * before, after or beside fabwd_run_main).  fabwd_run == fabwd_run_main then fabwd_run_dq.
  * Errors: as fabwd_run. */
 fabwd_status fabwd_run_main(const fabwd_params* p, void* workspace, size_t workspace_bytes, void* stream);
-fabwd_status fabwd_run_convert(const fabwd_params* p, void* workspace, size_t workspace_bytes, void* stream);
+fabwd_status fabwd_run_dq(const fabwd_params* p, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronising read of the device status word: enqueues a 4-byte device-to-host copy on
  * `stream`, waits for the stream, and stores the FABWD_DEV_* bits in *device_status.  Returns

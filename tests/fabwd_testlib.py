@@ -59,7 +59,7 @@ def full_reference(pb: inputs.Problem) -> Reference:
     return ref
 
 
-def run_gpu(pb: inputs.Problem, ref: Reference, device="cuda", check_status=True):
+def run_gpu(pb: inputs.Problem, ref: Reference, device="cuda", check_status=True, dq_mode="auto"):
     """Run the libfabwd path on the GPU; returns (dq, dk, dv, sfmg fp32 in lse's layout)."""
     from attention_backward_fabwd_gb300 import api, fabwd
 
@@ -74,7 +74,7 @@ def run_gpu(pb: inputs.Problem, ref: Reference, device="cuda", check_status=True
     dq, dk, dv, (p, ws) = api.flash_attn_grad(
         t(pb.q), t(pb.k), t(pb.v), t(pb.dout), t(ref.attn_out), t(ref.lse), cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv,
         layout_q=pb.w.layout, layout_kv=pb.w.layout, layout_out=pb.w.layout, check_status=check_status,
-        return_workspace=True, **mask_kwargs(pb.w), **extra)
+        return_workspace=True, dq_mode=dq_mode, **mask_kwargs(pb.w), **extra)
     torch.cuda.synchronize()
     lay = fabwd.fabwd_workspace_layout(p)
     B, N1, R = p.B, p.N1, lay["row_stride"]

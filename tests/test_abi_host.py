@@ -71,7 +71,7 @@ def test_version_and_status_strings(lib):
 
 
 def test_workspace_size_formula(lib):
-    p = base_params()
+    p = base_params(dq_mode=F.FABWD_DQ_ATOMIC)
     s, n = ws_size(p)
     assert s == F.FABWD_OK
     S1p = 384
@@ -81,6 +81,10 @@ def test_workspace_size_formula(lib):
     lay = F.fabwd_workspace_layout(p)
     assert lay["row_stride"] == S1p and lay["lse2"] == 256 and lay["sfmg"] == 256 + r256(rows)
     assert lay["dq_accum"] == lay["sfmg"] + r256(rows)
+    # separate dQ mode keeps no fp32 accumulator; auto picks it for D > 128 only
+    assert ws_size(base_params(dq_mode=F.FABWD_DQ_SEPARATE)) == (F.FABWD_OK, 256 + 2 * r256(rows))
+    assert ws_size(base_params(dq_mode=F.FABWD_DQ_AUTO)) == (s, n)
+    assert ws_size(base_params(dq_mode=F.FABWD_DQ_AUTO, D=192)) == (F.FABWD_OK, 256 + 2 * r256(rows))
 
 
 @pytest.mark.parametrize("change,code", [
@@ -103,11 +107,12 @@ def test_workspace_size_formula(lib):
     (dict(D=96, Dv=96), F.FABWD_ERR_UNSUPPORTED),    # valid per the statement, no kernel built
     (dict(D=128, Dv=64), F.FABWD_ERR_UNSUPPORTED),
     (dict(D=192, Dv=192), F.FABWD_ERR_UNSUPPORTED),
+    (dict(dq_mode=3), F.FABWD_ERR_INVALID),
 ])
 def test_validation_codes(lib, change, code):
     p = base_params(**change)
     assert ws_size(p)[0] == code
-    for fn in ("fabwd_preprocess", "fabwd_run", "fabwd_run_main", "fabwd_run_convert"):
+    for fn in ("fabwd_preprocess", "fabwd_run", "fabwd_run_main", "fabwd_run_dq"):
         assert F.call_status(fn, p, 0x100000, 1 << 30, None) == code
 
 

@@ -73,11 +73,12 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("dq_mode", ["separate", "atomic"])
 @pytest.mark.parametrize("name,w,lens", SMALL, ids=[c[0] for c in SMALL])
-def test_small_elementwise(name, w, lens):
+def test_small_elementwise(name, w, lens, dq_mode):
     pb = inputs.make_problem(w, *(lens or ()))
     ref = tl.full_reference(pb)
-    dq, dk, dv, sf = tl.run_gpu(pb, ref)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref, dq_mode=dq_mode)
     check_all(pb, ref, dq, dk, dv, sf)
 
 
@@ -93,16 +94,29 @@ def test_page_example_shapes_gqa_fp16():
     check_all(pb, ref, dq, dk, dv, sf)
 
 
-def test_dk_dv_deterministic_and_workspace_reuse():
-    w = inputs.sized(W["gqa_causal_s4096_d128"], N1=4, N2=2, S1=256, S2=256, dout_std=1.0)
+@pytest.mark.parametrize("dq_mode", ["separate", "atomic"])
+def test_determinism_and_workspace_reuse(dq_mode):
+    w = inputs.sized(W["gqa_causal_s4096_d128"], N1=4, N2=2, S1=700, S2=700, dout_std=1.0)
     pb = inputs.make_problem(w)
     ref = tl.forward_inputs(pb)
     dev = torch.device("cuda")
     args = [t.to(dev) for t in (pb.q, pb.k, pb.v, pb.dout, ref.attn_out, ref.lse)]
-    dq1, dk1, dv1 = api.flash_attn_grad(*args, mask_mode=1, check_status=True)
-    dq2, dk2, dv2 = api.flash_attn_grad(*args, mask_mode=1, check_status=True)
-    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)   # no atomics on dK/dV
-    assert (dq1.float() - dq2.float()).abs().max().item() <= 1e-2 * dq1.float().abs().max().item()
+    dq1, dk1, dv1 = api.flash_attn_grad(*args, mask_mode=1, dq_mode=dq_mode, check_status=True)
+    dq2, dk2, dv2 = api.flash_attn_grad(*args, mask_mode=1, dq_mode=dq_mode, check_status=True)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)   # no atomics on dK/dV in either mode
+    if dq_mode == "separate":
+        assert torch.equal(dq1, dq2)                          # one CTA sums each dQ element in order
+    else:
+        assert (dq1.float() - dq2.float()).abs().max().item() <= 1e-2 * dq1.float().abs().max().item()
+
+
+def test_modes_agree():
+    w = inputs.sized(W["varlen_window_fp16_d128"], B=3, N1=4, N2=2, win_left=100)
+    pb = inputs.make_problem(w, [300, 17, 260])
+    ref = tl.full_reference(pb)
+    outs = {m: tl.run_gpu(pb, ref, dq_mode=m) for m in ("atomic", "separate")}
+    for i, name in enumerate(("dq", "dk", "dv")):
+        tl.assert_close(f"{name} atomic vs separate", outs["atomic"][i], inputs.to_f64(outs["separate"][i]))
 
 
 # ---------------------------------------------------------------------------------------------
@@ -232,7 +246,7 @@ def test_full_size_sampled(name):
     w = W[name]
     pb = inputs.make_problem(w)
     ref = tl.forward_inputs(pb)
-    dq, dk, dv, sf = tl.run_gpu(pb, ref)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref)  # the library's default dQ mode, as the bench runs it
     kw = tl.oracle_kwargs(pb)
     if w.layout == "TND":
         seq_q = list(enumerate(np.diff(pb.cu_seqlens_q).tolist()))

@@ -47,11 +47,17 @@ def test_static_workspace_matches_caller_workspace_twice(lib):
 
 
 def test_static_workspace_refuses_oversized_problems(lib):
-    # dq accumulator alone: 8192 x 32 x 128 fp32 = 128 MiB > 64 MiB; refused before any launch
+    # The pointers below are placeholders that must never reach a kernel, so the problem is
+    # chosen to need far more than the 64 MiB array in every dQ mode (the lse/sfmg rows alone are
+    # 2 x 4 x 64 x 65536 x 4 B = 128 MiB), and the size is checked on the host before the call.
     p = F.fabwd_params()
     p.dtype, p.layout = F.FABWD_BF16, F.FABWD_BSND
-    p.B, p.S1, p.S2, p.N1, p.N2, p.D, p.Dv = 1, 8192, 8192, 32, 8, 128, 128
+    p.B, p.S1, p.S2, p.N1, p.N2, p.D, p.Dv = 4, 65536, 65536, 64, 8, 128, 128
     p.mask_mode, p.win_left, p.win_right = 1, -1, -1
     for name in ("q", "k", "v", "dout", "attn_out", "softmax_lse", "dq", "dk", "dv"):
         setattr(p, name, 0x10000)
-    assert lib.fabwd_run_static_workspace(ctypes.byref(p), None) == F.FABWD_ERR_WORKSPACE
+    for mode in (F.FABWD_DQ_AUTO, F.FABWD_DQ_ATOMIC, F.FABWD_DQ_SEPARATE):
+        p.dq_mode = mode
+        need = F.fabwd_workspace_size(p)
+        assert need >= 96 << 20, "the placeholder pointers would reach a kernel"
+        assert lib.fabwd_run_static_workspace(ctypes.byref(p), None) == F.FABWD_ERR_WORKSPACE
