@@ -66,9 +66,8 @@ fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
   pl->rowsK = tnd ? p->T2 : p->B * p->S2;
   pl->S1p = (p->S1 + kRowPad - 1) / kRowPad * kRowPad;
   pl->scale = p->softmax_scale != 0.0 ? p->softmax_scale : 1.0 / std::sqrt((double)p->D);
-  // AUTO: the separate pass where it measured faster (D = 192, whose fused kernel has one TMEM
-  // slot and two dQᵀ products to reduce), the fused atomic pass otherwise
-  pl->separate = p->dq_mode == FABWD_DQ_SEPARATE || (p->dq_mode == FABWD_DQ_AUTO && p->D > 128);
+  // AUTO: the separate pass (measured faster than the fused atomic pass on the GB300 workloads)
+  pl->separate = p->dq_mode != FABWD_DQ_ATOMIC;
   pl->dq_elems = pl->separate ? 0 : pl->rowsQ * p->N1 * p->D;
   pl->off_status = 0;
   pl->off_lse2 = 256;
@@ -262,12 +261,19 @@ fabwd_status fabwd_run_main(const fabwd_params* p, void* ws, size_t ws_bytes, vo
   const int inject = g_inject_timeout;
   g_inject_timeout = 0;
   if (any_pair(p, pl)) {
+    // separate mode with D <= 128: the dK/dV kernel with 128-row query steps; otherwise the
+    // kv-stationary kernel with 64-row steps (which also reduces dQ in atomic mode)
+    const bool kv128 = pl.separate && p->D <= 128;
     MainMaps maps;
-    if (!make_maps(p, &maps, kBlockQ, kBlockKV)) return FABWD_ERR_CUDA;
+    if (!make_maps(p, &maps, kv128 ? 128 : kBlockQ, kBlockKV)) return FABWD_ERR_CUDA;
     const MainArgs a = main_args(p, pl, static_cast<uint8_t*>(ws), inject);
     const int n_kv_blocks = (int)((p->S2 + kBlockKV - 1) / kBlockKV);
-    cudaError_t e = p->dtype == FABWD_FP16 ? launch_main_fp16(a, maps, (int)p->D, (int)p->Dv, n_kv_blocks, !pl.separate, st)
-                                           : launch_main_bf16(a, maps, (int)p->D, (int)p->Dv, n_kv_blocks, !pl.separate, st);
+    const bool fp16 = p->dtype == FABWD_FP16;
+    const int D = (int)p->D, Dv = (int)p->Dv;
+    cudaError_t e = kv128 ? (fp16 ? launch_kv_fp16(a, maps, D, Dv, n_kv_blocks, st)
+                                  : launch_kv_bf16(a, maps, D, Dv, n_kv_blocks, st))
+                          : (fp16 ? launch_main_fp16(a, maps, D, Dv, n_kv_blocks, !pl.separate, st)
+                                  : launch_main_bf16(a, maps, D, Dv, n_kv_blocks, !pl.separate, st));
     if (e != cudaSuccess) return FABWD_ERR_CUDA;
   } else if (pl.rowsK > 0) {
     // no visible pair at all: dk = dv = 0

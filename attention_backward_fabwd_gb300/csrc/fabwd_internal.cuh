@@ -81,6 +81,10 @@ cudaError_t launch_main_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv
 cudaError_t launch_main_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, bool fused,
                              cudaStream_t st);
 cudaError_t launch_dq_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
+// dK/dV-only kernel with 128-row query steps (separate dQ mode, D <= 128); needs q-side maps with
+// 128-row boxes.  Returns cudaErrorInvalidValue for other head dims.
+cudaError_t launch_kv_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
+cudaError_t launch_kv_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
 cudaError_t launch_dq_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
 bool main_supported(int D, int Dv);
 

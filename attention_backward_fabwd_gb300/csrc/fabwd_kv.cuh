@@ -1,0 +1,370 @@
+// kv-stationary dK/dV kernel with 128-row query steps (separate dQ mode, D <= 128).
+//
+// What it computes is dK and dV of the page "CANN ops-transformer FlashAttnGrad 算子详解"
+// (discosf.com/news/4863418), §一: dV = Pᵀ·dY and dK = scale·dSᵀ·Q with P = exp(scale·QKᵀ − lse)
+// and dS = P ⊙ (dY·Vᵀ − sfmg), summed over the query blocks and the G q-heads of a kv-head.
+// One CTA owns 128 keys of one kv-head; each step handles 128 query rows of one q-head:
+//     Sᵀ  = K·Qᵀ     tcgen05 M = 128 keys, N = 128 queries (a full-rate shape), TMEM slot S
+//     dPᵀ = V·dOᵀ    same shape, TMEM slot dP
+//     Pᵀ  = exp2(Sᵀ·scale·log2e − lse·log2e) -> 16-bit pairs over the warpgroup's own Sᵀ columns
+//     dSᵀ = Pᵀ ⊙ (dPᵀ − sfmg)               -> 16-bit pairs over its own dPᵀ columns
+//     dV += Pᵀ·dO, dK += dSᵀ·Q               tcgen05 with the A operand read from TMEM
+// Warpgroup g (warps 4g..4g+3) handles query columns [64g, 64g+64) of every step.  Keeping dSᵀ in
+// the dPᵀ columns frees the Sᵀ columns as soon as dV has read Pᵀ, so the MMA warp issues
+//     Sᵀ(t), dPᵀ(t), dV(t), Sᵀ(t+1), dK(t), dPᵀ(t+1), dV(t+1), ...
+// and the elementwise work of each step overlaps the previous step's dK and the next step's Sᵀ.
+// Warp 8 streams Q, dO, lse and sfmg through a 2-stage TMA ring (K and V are loaded once).
+// TMEM columns: dK [0, D), dV [D, D+Dv), Sᵀ/Pᵀ [D+Dv, +128), dPᵀ/dSᵀ [D+Dv+128, +128).
+// Bounded waits, abort flag, drain and TMEM release as in the fused kernel.
+#pragma once
+
+#include "fabwd_internal.cuh"
+#include "fabwd_main.cuh"
+#include "fabwd_ptx.cuh"
+#include "../../include/fabwd.h"
+
+namespace fabwd {
+
+template <int D, int DV>
+struct KvCfg {
+  static constexpr int BR = 128, BC = kBlockKV, NS = 2;
+  static constexpr uint32_t kK = D * BC * 2, kV = DV * BC * 2, kQ = D * BR * 2, kdO = DV * BR * 2;
+  static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + NS * kQ;
+  static constexpr uint32_t oL = odO + NS * kdO;     // [NS][BR] fp32 lse·log2(e)
+  static constexpr uint32_t oF = oL + NS * BR * 4;   // [NS][BR] fp32 sfmg
+  static constexpr uint32_t oBar = oF + NS * BR * 4;
+  static constexpr uint32_t oMisc = oBar + 32 * 8;
+  static constexpr uint32_t bytes = oMisc + 64;
+  static constexpr uint32_t cDK = 0, cDV = D, cS = D + DV, cP = cS + BR;
+  static_assert(D % 64 == 0 && DV % 64 == 0 && D <= 128 && DV <= D, "head dims");
+  static_assert(cP + BR <= 512, "TMEM budget");
+  static_assert(bytes <= 232448, "shared memory budget");
+};
+
+constexpr int kKvKvFull = 0, kKvQFull = 1 /*+2*/, kKvQEmpty = 3 /*+2*/, kKvSFull = 5, kKvDpFull = 6, kKvPFull = 7,
+              kKvDsFull = 8, kKvAccDone = 9, kKvNever = 10, kKvDrain = 11, kKvNumBars = 12;
+
+template <int D, int DV, bool FP16>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    fabwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const MainArgs a) {
+  using C = KvCfg<D, DV>;
+  constexpr int BR = C::BR, BC = C::BC, NS = C::NS;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int jb = blockIdx.x / a.N2, n2 = blockIdx.x % a.N2, b = blockIdx.y;
+  SeqRange sq;
+  if (!seq_range(a, b, sq)) return;  // bad cu_seqlens: the preprocess kernel reports it
+  const int j0 = jb * BC;
+  if (j0 >= sq.L2) return;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) atomicOr(a.status, FABWD_DEV_INTERNAL);
+    return;
+  }
+  const int j1 = min(j0 + BC, sq.L2);
+  const long long off = (long long)sq.L2 - sq.L1;
+  long long lo, hi;
+  mask_bounds(a, lo, hi);
+  long long ib = (long long)j0 - off - hi, ie = (long long)(j1 - 1) - off - lo;
+  if (ib < 0) ib = 0;
+  if (ie > sq.L1 - 1) ie = sq.L1 - 1;
+  const int qb_begin = ib <= ie ? (int)(ib / BR) : 0;
+  const int nqb = ib <= ie ? (int)(ie / BR) + 1 - qb_begin : 0;
+  const int T = nqb * a.G;  // steps: (head in group, 128-row q-block)
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBar);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::oMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oMisc + 16);
+  if (tid == 0) {
+    for (int i = 0; i < kKvNumBars; ++i) mbar_init(&bars[i], (i == kKvPFull || i == kKvDsFull) ? 8 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_do);
+  }
+  __syncwarp();
+  if (warp == 9) tmem_alloc(tm_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tm_holder;
+  if (a.inject_timeout) {
+    if (lane == 0) wait_bar(&bars[kKvNever], 0, abort_flag, a);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
+  const int kv_row0 = tnd ? sq.k0 + j0 : j0;
+  const int q_rowbase = tnd ? sq.q0 : 0;
+  const int bcoord = tnd ? 0 : b;
+  constexpr bool kBF16 = !FP16;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && T > 0 && !*abort_flag) {
+      mbar_arrive_expect_tx(&bars[kKvKvFull], (D + DV) * BC * 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_4d(smem + C::oK + c * BC * 128, &tm_k, &bars[kKvKvFull], c * 64, bnsd ? kv_row0 : n2,
+                    bnsd ? n2 : kv_row0, bcoord);
+#pragma unroll
+      for (int c = 0; c < DV / 64; ++c)
+        tma_load_4d(smem + C::oV + c * BC * 128, &tm_v, &bars[kKvKvFull], c * 64, bnsd ? kv_row0 : n2,
+                    bnsd ? n2 : kv_row0, bcoord);
+      for (int t = 0; t < T; ++t) {
+        const int st = t % NS;
+        const int h = t / nqb, qb = qb_begin + t % nqb;
+        const int n1 = n2 * a.G + h, i0 = qb * BR;
+        if (t >= NS && !wait_bar(&bars[kKvQEmpty + st], ((t / NS) - 1) & 1, abort_flag, a)) break;
+        uint64_t* full = &bars[kKvQFull + st];
+        mbar_arrive_expect_tx(full, (D + DV) * BR * 2 + 2 * BR * 4);
+        const int row = q_rowbase + i0;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(smem + C::oQ + st * C::kQ + c * BR * 128, &tm_q, full, c * 64, bnsd ? row : n1,
+                      bnsd ? n1 : row, bcoord);
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_4d(smem + C::odO + st * C::kdO + c * BR * 128, &tm_do, full, c * 64, bnsd ? row : n1,
+                      bnsd ? n1 : row, bcoord);
+        const long long rbase = ((long long)b * a.N1 + n1) * a.S1p + i0;
+        bulk_load(smem + C::oL + st * BR * 4, a.lse2 + rbase, BR * 4, full);
+        bulk_load(smem + C::oF + st * BR * 4, a.sfmg + rbase, BR * 4, full);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t ID_S = idesc_f16(BC, BR, kBF16, false, false);
+      constexpr uint32_t ID_DV = idesc_f16(BC, DV, kBF16, false, true);
+      constexpr uint32_t ID_DK = idesc_f16(BC, D, kBF16, false, true);
+      const uint32_t aK = smem_u32(smem + C::oK), aV = smem_u32(smem + C::oV);
+      // A operand columns of k-step kk (16 queries): warpgroup kk/4 holds queries 64·(kk/4)..,
+      // its 16-bit pairs at +0..31 of its own 64 columns
+      auto a_col = [](int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; };
+      auto issue_s = [&](int t) -> bool {
+        const int st = t % NS;
+        const uint32_t aQ = smem_u32(smem + C::oQ + st * C::kQ);
+        if (!wait_bar(&bars[kKvQFull + st], (t / NS) & 1, abort_flag, a)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::cS, sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(aQ + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+        mma_commit(&bars[kKvSFull]);
+        return true;
+      };
+      auto issue_dp = [&](int t) {
+        const uint32_t adO = smem_u32(smem + C::odO + (t % NS) * C::kdO);
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_ss(tmem + C::cP, sdesc_sw128(aV + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(adO + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+        mma_commit(&bars[kKvDpFull]);
+      };
+      bool ok = wait_bar(&bars[kKvKvFull], 0, abort_flag, a) && issue_s(0);
+      if (ok) issue_dp(0);
+      for (int t = 0; ok && t < T; ++t) {
+        const int st = t % NS;
+        const uint32_t aQ = smem_u32(smem + C::oQ + st * C::kQ), adO = smem_u32(smem + C::odO + st * C::kdO);
+        if (!(ok = wait_bar(&bars[kKvPFull], t & 1, abort_flag, a))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BR / 16; ++kk)
+          mma_ts(tmem + C::cDV, tmem + C::cS + a_col(kk), sdesc_sw128(adO + kk * 2048, BR * 128, 1024), ID_DV,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        // Sᵀ of the next step may overwrite the Pᵀ columns once dV (issued above) has read them
+        if (t + 1 < T && !(ok = issue_s(t + 1))) break;
+        if (!(ok = wait_bar(&bars[kKvDsFull], t & 1, abort_flag, a))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BR / 16; ++kk)
+          mma_ts(tmem + C::cDK, tmem + C::cP + a_col(kk), sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kKvQEmpty + st]);
+        if (t + 1 < T) issue_dp(t + 1);  // after dK read the dSᵀ held in the dPᵀ columns
+      }
+      if (ok) {
+        mma_commit(&bars[kKvAccDone]);
+      } else {
+        mma_commit(&bars[kKvDrain]);
+        mbar_wait(&bars[kKvDrain], 0, kDrainNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ compute warpgroups 0, 1
+    const int q4 = warp & 3, g = warp >> 2;
+    const int row = q4 * 32 + lane;  // TMEM lane = key row j0 + row
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t sS = tmem + lane_off + C::cS + g * 64, sP = tmem + lane_off + C::cP + g * 64;
+    const int jr = j0 + row;
+    const bool j_valid = jr < sq.L2;
+    const long long vlo = (long long)jr - off - hi, vhi = (long long)jr - off - lo;
+    const int i_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
+    const int i_vis_hi = (int)(vhi < -1 ? -1 : (vhi > (1 << 30) ? (1 << 30) : vhi));
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int st = t % NS;
+      const int qb = qb_begin + t % nqb;
+      const int i0 = qb * BR, ic0 = i0 + g * 64;
+      if (!(ok = wait_bar_warp(&bars[kKvQFull + st], (t / NS) & 1, abort_flag, a))) break;
+      if (!(ok = wait_bar_warp(&bars[kKvSFull], t & 1, abort_flag, a))) break;
+      tc_fence_after();
+      const float4* sL4 = reinterpret_cast<const float4*>(smem + C::oL + st * BR * 4 + g * 256);
+      const float4* sF4 = reinterpret_cast<const float4*>(smem + C::oF + st * BR * 4 + g * 256);
+      const long long dmin = (long long)j0 - (i0 + BR - 1) - off, dmax = (long long)(j1 - 1) - i0 - off;
+      const bool full = dmin >= lo && dmax <= hi;
+      uint32_t p0[32], p1[32];  // Sᵀ row (64 queries), then P (fp32 bits)
+      tmem_ld32(sS, p0);
+      tmem_ld32(sS + 32, p1);
+      tmem_wait_ld();
+      reg_fence(p0);
+      reg_fence(p1);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 l0 = sL4[c4], l1 = sL4[c4 + 8];
+        const float la[4] = {l0.x, l0.y, l0.z, l0.w}, lb[4] = {l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          p0[4 * c4 + e] = __float_as_uint(ex2(fmaf(__uint_as_float(p0[4 * c4 + e]), a.scale_log2, -la[e])));
+          p1[4 * c4 + e] = __float_as_uint(ex2(fmaf(__uint_as_float(p1[4 * c4 + e]), a.scale_log2, -lb[e])));
+        }
+      }
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (ic0 + c < i_vis_lo || ic0 + c > i_vis_hi) p0[c] = 0u;
+          if (ic0 + 32 + c < i_vis_lo || ic0 + 32 + c > i_vis_hi) p1[c] = 0u;
+        }
+      }
+      if (!j_valid) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) p0[c] = p1[c] = 0u;
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          pk[c] = pack2<FP16>(__uint_as_float(p0[2 * c]), __uint_as_float(p0[2 * c + 1]));
+          pk[16 + c] = pack2<FP16>(__uint_as_float(p1[2 * c]), __uint_as_float(p1[2 * c + 1]));
+        }
+        tmem_st32(sS, pk);  // Pᵀ over this warpgroup's own (already read) Sᵀ columns
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kKvPFull]);
+      if (!(ok = wait_bar_warp(&bars[kKvDpFull], t & 1, abort_flag, a))) break;
+      tc_fence_after();
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(sP, r0);
+        tmem_ld32(sP + 32, r1);
+        tmem_wait_ld();
+        reg_fence(r0);
+        reg_fence(r1);
+        uint32_t dk[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 f0 = sF4[c4], f1 = sF4[c4 + 8];
+          const float fa[4] = {f0.x, f0.y, f0.z, f0.w}, fb[4] = {f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int c = 4 * c4 + e;
+            dk[c >> 1] = pack2<FP16>(__uint_as_float(p0[c]) * (__uint_as_float(r0[c]) - fa[e]),
+                                     __uint_as_float(p0[c + 1]) * (__uint_as_float(r0[c + 1]) - fa[e + 1]));
+            dk[16 + (c >> 1)] = pack2<FP16>(__uint_as_float(p1[c]) * (__uint_as_float(r1[c]) - fb[e]),
+                                            __uint_as_float(p1[c + 1]) * (__uint_as_float(r1[c + 1]) - fb[e + 1]));
+          }
+        }
+        tmem_st32(sP, dk);  // dSᵀ over this warpgroup's own (already read) dPᵀ columns
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kKvDsFull]);
+    }
+    // ---- epilogue: dK = scale · acc, dV = acc; zeros when no query sees this block
+    if (ok && T > 0) ok = wait_bar_warp(&bars[kKvAccDone], 0, abort_flag, a);
+    if (ok) {
+      tc_fence_after();
+      const long long krow = row_index(a.layout, b, (long long)(tnd ? sq.k0 : 0) + (j_valid ? jr : 0), n2, a.N2, a.S2);
+      uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * D;
+      uint16_t* dv = static_cast<uint16_t*>(a.dv) + krow * DV;
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = g * (D / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cDK + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * a.scale, __uint_as_float(r[e + 1]) * a.scale) : 0u;
+        if (j_valid) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            *reinterpret_cast<uint4*>(dk + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < DV / 64; ++c) {
+        const int col = g * (DV / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cDV + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]), __uint_as_float(r[e + 1])) : 0u;
+        if (j_valid) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            *reinterpret_cast<uint4*>(dv + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kGraceNs) {
+    }
+  }
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int DV, bool FP16>
+cudaError_t launch_kv_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
+  using C = KvCfg<D, DV>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fabwd_kv_kernel<D, DV, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::bytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(n_kv_blocks * a.N2, a.B);
+  fabwd_kv_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
+  return cudaGetLastError();
+}
+
+}  // namespace fabwd

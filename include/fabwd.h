@@ -79,8 +79,8 @@ typedef enum { FABWD_MASK_NONE = 0, FABWD_MASK_CAUSAL = 1, FABWD_MASK_BAND = 2 }
  *                      recomputes S and dP per query block and accumulates dQ in tensor memory,
  *                      without atomics: bitwise reproducible, no fp32 accumulator in the
  *                      workspace, about 1.4x the tensor-core work.
- *   FABWD_DQ_AUTO:     the library's choice: SEPARATE for D > 128, ATOMIC otherwise (the faster
- *                      mode on the measured workloads). */
+ *   FABWD_DQ_AUTO:     the library's choice (currently SEPARATE, the faster mode on the measured
+ *                      workloads). */
 typedef enum { FABWD_DQ_AUTO = 0, FABWD_DQ_ATOMIC = 1, FABWD_DQ_SEPARATE = 2 } fabwd_dq_mode;
 
 /* Device status bits (fabwd_read_device_status). */

@@ -81,10 +81,9 @@ def test_workspace_size_formula(lib):
     lay = F.fabwd_workspace_layout(p)
     assert lay["row_stride"] == S1p and lay["lse2"] == 256 and lay["sfmg"] == 256 + r256(rows)
     assert lay["dq_accum"] == lay["sfmg"] + r256(rows)
-    # separate dQ mode keeps no fp32 accumulator; auto picks it for D > 128 only
+    # separate dQ mode (auto's choice) keeps no fp32 accumulator
     assert ws_size(base_params(dq_mode=F.FABWD_DQ_SEPARATE)) == (F.FABWD_OK, 256 + 2 * r256(rows))
-    assert ws_size(base_params(dq_mode=F.FABWD_DQ_AUTO)) == (s, n)
-    assert ws_size(base_params(dq_mode=F.FABWD_DQ_AUTO, D=192)) == (F.FABWD_OK, 256 + 2 * r256(rows))
+    assert ws_size(base_params(dq_mode=F.FABWD_DQ_AUTO)) == (F.FABWD_OK, 256 + 2 * r256(rows))
 
 
 @pytest.mark.parametrize("change,code", [
