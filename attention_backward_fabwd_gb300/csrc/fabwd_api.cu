@@ -168,6 +168,15 @@ fabwd_status fabwd_workspace_layout(const fabwd_params* p, size_t* off_sfmg, siz
   return FABWD_OK;
 }
 
+fabwd_status fabwd_resolve_dq_mode(const fabwd_params* p, int32_t* mode) {
+  if (!p || !mode) return FABWD_ERR_NULLPTR;
+  Plan pl;
+  fabwd_status s = plan_and_check(p, &pl, false);
+  if (s != FABWD_OK) return s;
+  *mode = pl.separate ? FABWD_DQ_SEPARATE : FABWD_DQ_ATOMIC;
+  return FABWD_OK;
+}
+
 fabwd_status fabwd_preprocess(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
   Plan pl;
   fabwd_status s = plan_and_check(p, &pl, true);

@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
         L.fabwd_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
         L.fabwd_workspace_layout.argtypes = [P, ctypes.POINTER(sz), ctypes.POINTER(sz), ctypes.POINTER(sz),
                                              ctypes.POINTER(ctypes.c_int64)]
+        L.fabwd_resolve_dq_mode.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
         L.fabwd_preprocess.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run_main.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
@@ -76,7 +77,8 @@ def lib() -> ctypes.CDLL:
         L.fabwd_status_string.argtypes = [ctypes.c_int]
         L.fabwd_status_string.restype = ctypes.c_char_p
         for f in ("fabwd_workspace_size", "fabwd_workspace_layout", "fabwd_preprocess", "fabwd_run",
-                  "fabwd_run_main", "fabwd_run_dq", "fabwd_read_device_status", "fabwd_run_static_workspace"):
+                  "fabwd_run_main", "fabwd_run_dq", "fabwd_read_device_status", "fabwd_run_static_workspace",
+                  "fabwd_resolve_dq_mode"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -108,6 +110,14 @@ def fabwd_workspace_layout(p: fabwd_params):
     if s != FABWD_OK:
         raise FabwdError(s, "fabwd_workspace_layout")
     return {"sfmg": a.value, "lse2": b.value, "dq_accum": c.value, "row_stride": r.value}
+
+
+def fabwd_resolve_dq_mode(p: fabwd_params) -> int:
+    m = ctypes.c_int32(0)
+    s = lib().fabwd_resolve_dq_mode(ctypes.byref(p), ctypes.byref(m))
+    if s != FABWD_OK:
+        raise FabwdError(s, "fabwd_resolve_dq_mode")
+    return m.value
 
 
 def fabwd_preprocess(p: fabwd_params, workspace: int, workspace_bytes: int, stream: int) -> None:

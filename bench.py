@@ -2,15 +2,20 @@
 """Benchmark: attention-backward TFLOP/s (bf16) on one GB300 and % of dense tensor peak.
 
 One step = one pass of the whole backward path over one batch of synthetic input:
-fabwd_preprocess (sfmg, lse rows, dq accumulator zeroing) -> fabwd_run_main (tcgen05 backward
-kernel) -> fabwd_run_dq (dQ stage), all libfabwd kernels on one stream.
+fabwd_preprocess (sfmg, lse rows, dq accumulator zeroing) -> fabwd_run_main (the dK/dV kernel,
+or the fused kernel in the atomic dQ mode) -> fabwd_run_dq (the dQ kernel, or the convert pass),
+all libfabwd kernels on one stream, with CUDA events between the stages.
 
-Flops follow the measurement convention: per head 2·S1·S2·(3D + 2Dv), halved under a causal
-mask; the roofline uses the algorithmic count 2·(3D + 2Dv) per visible (query, key) pair.
+`value` follows the measurement convention: per head 2·S1·S2·(3D + 2Dv), halved under a causal
+mask, over the whole step.  `roofline` is the stage kernel with the longest time, credited with
+its own algorithmic flops: 2·(inner dimensions of the products it forms) per visible (query, key)
+pair — (3D + 2Dv) for the fused kernel, (2D + 2Dv) for the dK/dV kernel, (2D + Dv) for the dQ
+kernel (which forms S and dP again).
 
 Inputs: q, k, v, dout are the seeded draws of attention_backward_fabwd_gb300.inputs; attn_out
 and softmax_lse come from a plain torch fp32 forward on the GPU (input synthesis, untimed).
 The L2 cache (129 MB) is flushed between timed steps by writing a 256 MB buffer (untimed).
+SM clocks and throttle reasons are sampled by nvidia-smi every 50 ms inside the timed region.
 
 `--impl reference` times the fp64 CPU oracle instead (host cores, bounded sample per step).
 Multi-GPU (torchrun): each rank runs an independent replica (no collective on the data path);
@@ -39,8 +44,8 @@ DEFAULT_WORKLOAD = "gqa_causal_s4096_d128"
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["fabwd", "reference"], default="fabwd")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--dq-mode", default="auto", choices=["auto", "atomic", "separate"])
@@ -167,9 +172,10 @@ def synth_forward(pb, dev):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks/throttle reasons sampled every 50 ms; summary() keeps the samples taken
+    inside the window marked by mark_start()/mark_end() (wall clock)."""
 
-    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -177,6 +183,7 @@ class ClockSampler:
         self.bus_id = bus_id
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
@@ -184,19 +191,37 @@ class ClockSampler:
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+                                          "-lms", "50"], stdout=self.out, stderr=subprocess.DEVNULL)
+            deadline = time.time() + 10.0   # nvidia-smi takes a moment to print its first sample
+            while time.time() < deadline and os.path.getsize(self.path) == 0:
+                time.sleep(0.05)
         except Exception:
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
             self.out.close()
+
+    @staticmethod
+    def _when(stamp):
+        try:
+            head, _, frac = stamp.partition(".")
+            return time.mktime(time.strptime(head, "%Y/%m/%d %H:%M:%S")) + float("0." + (frac or "0"))
+        except ValueError:
+            return None
 
     def summary(self):
         if self.proc is None or not self.path or not os.path.exists(self.path):
@@ -205,27 +230,35 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 10:
+                if len(parts) < 11:
                     continue
                 rows.append(parts)
         os.unlink(self.path)
         if not rows:
             return None
         if self.bus_id:
-            mine = [r for r in rows if r[1].lower().endswith(self.bus_id.lower()[-12:])]
+            mine = [r for r in rows if r[2].lower().endswith(self.bus_id.lower()[-12:])]
             rows = mine or rows
-        ids = sorted(set(r[0] for r in rows))
+        ids = sorted(set(r[1] for r in rows))
         if len(ids) > 1:
-            rows = [r for r in rows if r[0] == ids[0]]
+            rows = [r for r in rows if r[1] == ids[0]]
+        window = rows
+        if self.t0 is not None and self.t1 is not None:
+            def inside(r):
+                t = self._when(r[0])
+                return t is not None and self.t0 - 0.025 <= t <= self.t1 + 0.025
+            window = [r for r in rows if inside(r)] or rows
         try:
-            sm = [float(r[2]) for r in rows]
-            smax = max(float(r[3]) for r in rows)
+            sm = [float(r[3]) for r in window]
+            smax = max(float(r[4]) for r in window)
+            power = [float(r[5]) for r in window]
         except ValueError:
             return None
-        loaded = [x for x in sm if x > 0.5 * smax] or sm
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for r in rows for k in range(4) if r[6 + k].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({names[k] for r in window for k in range(4) if r[7 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons, "samples": len(window),
+                "samples_in_timed_region": len(window) if window is not rows else 0,
+                "power_w_max": max(power), "period_ms": 50}
 
 
 def measured_peaks():
@@ -237,19 +270,53 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
-def profile_traffic(workload):
-    """dram bytes per main-kernel launch recorded from an ncu capture, if one is committed."""
+def profile_traffic(workload, kernel):
+    """dram bytes per launch of `kernel` on `workload` from a committed ncu capture, if one matches
+    the current kernel revision (profiles/traffic.json)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        v = d.get(workload)
-        if v and v.get("kernel_rev") == KERNEL_REV:
+        v = d.get(workload, {}).get(kernel)
+        if v and v.get("kernel_rev") == KERNEL_REV.get(kernel):
             return v.get("dram_bytes_per_launch")
     return None
 
 
-KERNEL_REV = "main-v1"
+def stage_table(pb, r, peak_tf, peak_hbm):
+    """Per-stage timing with each kernel's algorithmic work: tensor stages count 2·(the inner
+    dimensions of their own products) flops per visible (query, key) pair; HBM stages count the
+    bytes they must read and write."""
+    w = pb.w
+    pairs = w.N1 * sum(visible_pairs(L1, L2, w) for L1, L2 in seq_lengths(pb))
+    e = 2
+    rows_pad = w.B * w.N1 * ((pb.S1 + 127) // 128 * 128)
+    dq_acc = 0 if r["separate"] else 4 * r["dq_elems"]
+    pre_bytes = e * 2 * pb.dout.numel() + 4 * w.N1 * pb.T1 + 2 * 4 * rows_pad + dq_acc
+
+    def hbm(kernel, ms, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+        return {"kernel": kernel, "bound": "hbm", "ms": ms, "bytes": nbytes, "GB/s": gbs, "frac_of_hbm": gbs / peak_hbm}
+
+    def tensor(kernel, ms, per_pair):
+        f = per_pair * pairs
+        tf = f / (ms * 1e-3) / 1e12 if ms > 0 else 0.0
+        return {"kernel": kernel, "bound": "tensor", "ms": ms, "flops": f, "flops_per_pair": per_pair,
+                "TFLOP/s": tf, "frac_of_peak": tf / peak_tf}
+
+    out = {"preprocess": hbm("preprocess_kernel", r["ms_pre"], pre_bytes)}
+    if r["separate"]:
+        out["dkdv"] = tensor("fabwd_kv_kernel" if w.D <= 128 else "fabwd_main_kernel", r["ms_main"],
+                             2 * (2 * w.D + 2 * w.Dv))
+        out["dq"] = tensor("fabwd_dq_kernel", r["ms_conv"], 2 * (2 * w.D + w.Dv))
+    else:
+        out["main"] = tensor("fabwd_main_kernel", r["ms_main"], 2 * (3 * w.D + 2 * w.Dv))
+        out["convert"] = hbm("convert_kernel", r["ms_conv"], (4 + e) * r["dq_elems"])
+    return out
+
+
+# revision of each kernel's code that profiles/traffic.json must match
+KERNEL_REV = {"fabwd_kv_kernel": "kv-v1", "fabwd_dq_kernel": "dq-v1", "fabwd_main_kernel": "main-v4"}
 
 
 def max_over_ranks(values, world, device="cpu"):
@@ -299,6 +366,7 @@ def gpu_arm(args, rank, world, local_rank):
                         softmax_scale=w.softmax_scale, mask_mode=w.mask_mode, win_left=w.win_left,
                         win_right=w.win_right, layout=w.layout, dq_mode=args.dq_mode, **extra)
     nbytes = fabwd.fabwd_workspace_size(p)
+    resolved = fabwd.fabwd_resolve_dq_mode(p)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     st = torch.cuda.current_stream(dev)
     sp = st.cuda_stream
@@ -336,16 +404,18 @@ def gpu_arm(args, rank, world, local_rank):
     except Exception:
         bus = None
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
-    barrier()
-    t_wall0 = time.perf_counter()
-    with ClockSampler() as clk:
+    with ClockSampler(bus) as clk:
+        torch.cuda.synchronize(dev)
+        barrier()
+        t_wall0 = time.perf_counter()
+        clk.mark_start()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             step(evs[i])
         torch.cuda.synchronize(dev)
-    barrier()
-    t_wall = time.perf_counter() - t_wall0
+        clk.mark_end()
+        barrier()
+        t_wall = time.perf_counter() - t_wall0
     pre = [e[0].elapsed_time(e[1]) for e in evs]
     main = [e[1].elapsed_time(e[2]) for e in evs]
     conv = [e[2].elapsed_time(e[3]) for e in evs]
@@ -362,7 +432,7 @@ def gpu_arm(args, rank, world, local_rank):
         hq, hk, hv, hdo, hy, hl = (t.cpu().pin_memory() for t in (q, k, v, dout, attn_out, lse))
         ho = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
         h2d, d2h = io_bytes(pb)
-        e2e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(3, args.steps // 2))]
+        e2e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(min(50, max(3, args.steps // 2)))]
         for i in range(len(e2e_evs) + 2):
             flush.fill_(i & 0xFF)
             ev = e2e_evs[i - 2] if i >= 2 else None
@@ -383,7 +453,8 @@ def gpu_arm(args, rank, world, local_rank):
     ms_step, ms_main, ms_pre, ms_conv, e2e_ms, t_wall = max_over_ranks(
         [ms_step, ms_main, statistics.mean(pre), statistics.mean(conv), e2e["ms"] if e2e else 0.0, t_wall], world, dev)
     return dict(pb=pb, w=w, ms_step=ms_step, ms_main=ms_main, ms_pre=ms_pre, ms_conv=ms_conv, e2e=e2e, e2e_ms=e2e_ms,
-                t_wall=t_wall, clocks=clk.summary(), dq_elems=dq.numel(), nbytes=nbytes)
+                t_wall=t_wall, clocks=clk.summary(), dq_elems=dq.numel(), nbytes=nbytes,
+                separate=resolved == fabwd.FABWD_DQ_SEPARATE)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -532,30 +603,22 @@ def main():
     conv, alg = flop_counts(pb)
     peak_tf, peak_hbm, peak_kind = measured_peaks()
     value = job_tflops(conv, world, r["ms_step"])
-    achieved = alg / (r["ms_main"] * 1e-3) / 1e12
-    # HBM-bound helper kernels: algorithmic bytes per launch
-    e = 2
-    pre_bytes = e * 2 * pb.dout.numel() + 4 * w.N1 * pb.T1 + 2 * 4 * w.B * w.N1 * ((pb.S1 + 127) // 128 * 128) \
-        + 4 * r["dq_elems"]
-    conv_bytes = 4 * r["dq_elems"] + e * r["dq_elems"]
+    stages = stage_table(pb, r, peak_tf, peak_hbm)
+    dom = max((st for st in stages.values() if st["bound"] == "tensor"), key=lambda st: st["ms"])
     out = {
         "metric": "attention-backward TFLOP/s (bf16) at 1 GB300 and % of dense tensor peak",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(pb, l2="flushed: 256 MB buffer written between timed steps (untimed)"),
+        "dq_mode": "separate" if r["separate"] else "atomic",
         "pct_of_peak": 100.0 * value / world / peak_tf,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": profile_traffic(w.name),
-                     "kernel": "fabwd_main_kernel", "peak_kind": f"{peak_kind} bf16 dense (burst)",
-                     "algorithmic_flops_per_launch": alg, "ms_per_launch": r["ms_main"]},
-        "kernels": {
-            "preprocess": {"ms": r["ms_pre"], "GB/s": pre_bytes / (r["ms_pre"] * 1e-3) / 1e9,
-                           "frac_of_hbm": pre_bytes / (r["ms_pre"] * 1e-3) / 1e9 / peak_hbm},
-            "main": {"ms": r["ms_main"], "TFLOP/s": achieved},
-            "convert": {"ms": r["ms_conv"], "GB/s": conv_bytes / (r["ms_conv"] * 1e-3) / 1e9,
-                        "frac_of_hbm": conv_bytes / (r["ms_conv"] * 1e-3) / 1e9 / peak_hbm},
-        },
+        "roofline": {"bound": "tensor", "achieved": dom["TFLOP/s"], "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": dom["TFLOP/s"] / peak_tf, "traffic": profile_traffic(w.name, dom["kernel"]),
+                     "kernel": dom["kernel"], "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                     "algorithmic_flops_per_launch": dom["flops"], "ms_per_launch": dom["ms"],
+                     "flops_per_pair": dom["flops_per_pair"]},
+        "kernels": stages,
         "flops_convention": conv, "flops_algorithmic": alg,
         "gpu_launches": 3 * args.steps,
         "clocks": r["clocks"],

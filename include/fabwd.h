@@ -171,6 +171,11 @@ int fabwd_debug_inject_timeout(int on);
 fabwd_status fabwd_workspace_layout(const fabwd_params* p, size_t* off_sfmg, size_t* off_lse2,
                                     size_t* off_dq_accum, int64_t* row_stride);
 
+/* Host only.  Stores in *mode the dQ mode that fabwd_run uses for these parameters: the
+ * requested one, or the library's choice (FABWD_DQ_ATOMIC or FABWD_DQ_SEPARATE) for
+ * FABWD_DQ_AUTO.  Errors as fabwd_workspace_size. */
+fabwd_status fabwd_resolve_dq_mode(const fabwd_params* p, int32_t* mode);
+
 /* Allocation-free form of fabwd_preprocess + fabwd_run (the pages have no counterpart; it is a
  * convenience of this library).  For callers that cannot call cudaMalloc when they run the
  * backward: code under a host framework that owns all device memory through its own pool (a

@@ -86,6 +86,15 @@ def test_workspace_size_formula(lib):
     assert ws_size(base_params(dq_mode=F.FABWD_DQ_AUTO)) == (F.FABWD_OK, 256 + 2 * r256(rows))
 
 
+def test_resolve_dq_mode(lib):
+    for asked, got in ((F.FABWD_DQ_ATOMIC, F.FABWD_DQ_ATOMIC), (F.FABWD_DQ_SEPARATE, F.FABWD_DQ_SEPARATE),
+                       (F.FABWD_DQ_AUTO, F.FABWD_DQ_SEPARATE)):
+        assert F.fabwd_resolve_dq_mode(base_params(dq_mode=asked)) == got
+        assert F.fabwd_resolve_dq_mode(base_params(dq_mode=asked, D=192)) == got
+    with pytest.raises(F.FabwdError):
+        F.fabwd_resolve_dq_mode(base_params(dq_mode=3))
+
+
 @pytest.mark.parametrize("change,code", [
     (dict(dtype=2), F.FABWD_ERR_INVALID),
     (dict(layout=3), F.FABWD_ERR_INVALID),
