@@ -14,8 +14,10 @@
 // query row, so the per-row lse and sfmg are per-thread scalars.
 //
 // Warp roles (320 threads): warps 0-7 compute (warp w reads TMEM lanes 32·(w%4)..+31; warps 0-3
-// take key columns [0, BN/2), warps 4-7 [BN/2, BN)), warp 8 issues TMA loads (Q, dO once; K, V
-// through a 2-stage ring), warp 9 allocates TMEM and issues the MMAs.
+// take key columns [0, BN/2), warps 4-7 [BN/2, BN)), warp 8 issues TMA loads (Q, dO once; K
+// through a 3-stage ring released after dQ, V through a 2-stage ring released after dP), warp 9
+// allocates TMEM and issues the MMAs in the order S(t+1), dP(t+1), dQ(t): dP of the next key
+// block goes ahead of the current dQ product, so its dS can start as soon as P is ready.
 // TMEM columns: dQ [0, D), S buffer 0 [D, D+BN), S buffer 1 [D+BN, D+2BN), dP [D+2BN, D+3BN).
 // Every mbarrier wait is bounded as in the kv-stationary kernel.
 #pragma once
@@ -31,20 +33,21 @@ template <int D, int DV>
 struct DqCfg {
   static constexpr int BM = 128;                 // query rows per CTA (TMEM lanes)
   static constexpr int BN = D > 128 ? 64 : 128;  // keys per step
-  static constexpr int NS = 2;                   // K/V ring stages
+  static constexpr int NK = 3, NV = 2;           // K ring and V ring stages
   static constexpr int NC = BN / 2;              // key columns per compute thread
   static constexpr uint32_t kQ = D * BM * 2, kdO = DV * BM * 2, kK = D * BN * 2, kV = DV * BN * 2;
-  static constexpr uint32_t oQ = 0, odO = oQ + kQ, oK = odO + kdO, oV = oK + NS * kK;
-  static constexpr uint32_t oBar = oV + NS * kV;
-  static constexpr uint32_t oMisc = oBar + 32 * 8;
+  static constexpr uint32_t oQ = 0, odO = oQ + kQ, oK = odO + kdO, oV = oK + NK * kK;
+  static constexpr uint32_t oBar = oV + NV * kV;
+  static constexpr uint32_t oMisc = oBar + 20 * 8;
   static constexpr uint32_t bytes = oMisc + 64;
   static constexpr uint32_t cDQ = 0, cS0 = D, cP = D + 2 * BN;  // S buffer b at cS0 + b·BN
   static_assert(cP + BN <= 512, "TMEM budget");
   static_assert(bytes <= 232448, "shared memory budget");
 };
 
-constexpr int kDqQdoFull = 0, kDqKvFull = 1 /*+2*/, kDqKvEmpty = 3 /*+2*/, kDqSFull = 5 /*+2*/, kDqDpFull = 7,
-              kDqDsFull = 8, kDqAccDone = 9, kDqNever = 10, kDqDrain = 11, kDqNumBars = 12;
+constexpr int kDqQdoFull = 0, kDqKFull = 1 /*+3*/, kDqKEmpty = 4 /*+3*/, kDqVFull = 7 /*+2*/, kDqVEmpty = 9 /*+2*/,
+              kDqSFull = 11 /*+2*/, kDqDpFull = 13, kDqDsFull = 14, kDqAccDone = 15, kDqNever = 16, kDqDrain = 17,
+              kDqNumBars = 18;
 
 template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
@@ -52,7 +55,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const MainArgs a) {
   using C = DqCfg<D, DV>;
-  constexpr int BM = C::BM, BN = C::BN, NS = C::NS, NC = C::NC;
+  constexpr int BM = C::BM, BN = C::BN, NK = C::NK, NV = C::NV, NC = C::NC;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -124,18 +127,21 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tma_load_4d(smem + C::odO + c * BM * 128, &tm_do, &bars[kDqQdoFull], c * 64, bnsd ? q_row : n1,
                     bnsd ? n1 : q_row, bcoord);
       for (int t = 0; t < T; ++t) {
-        const int st = t % NS;
-        if (t >= NS && !wait_bar(&bars[kDqKvEmpty + st], ((t / NS) - 1) & 1, abort_flag, a)) break;
-        uint64_t* full = &bars[kDqKvFull + st];
-        mbar_arrive_expect_tx(full, (D + DV) * BN * 2);
+        const int sk = t % NK, sv = t % NV;
         const int row = kv_rowbase + (kb_begin + t) * BN;
+        if (t >= NK && !wait_bar(&bars[kDqKEmpty + sk], ((t / NK) - 1) & 1, abort_flag, a)) break;
+        uint64_t* kfull = &bars[kDqKFull + sk];
+        mbar_arrive_expect_tx(kfull, D * BN * 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(smem + C::oK + st * C::kK + c * BN * 128, &tm_k, full, c * 64, bnsd ? row : n2, bnsd ? n2 : row,
+          tma_load_4d(smem + C::oK + sk * C::kK + c * BN * 128, &tm_k, kfull, c * 64, bnsd ? row : n2, bnsd ? n2 : row,
                       bcoord);
+        if (t >= NV && !wait_bar(&bars[kDqVEmpty + sv], ((t / NV) - 1) & 1, abort_flag, a)) break;
+        uint64_t* vfull = &bars[kDqVFull + sv];
+        mbar_arrive_expect_tx(vfull, DV * BN * 2);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(smem + C::oV + st * C::kV + c * BN * 128, &tm_v, full, c * 64, bnsd ? row : n2,
+          tma_load_4d(smem + C::oV + sv * C::kV + c * BN * 128, &tm_v, vfull, c * 64, bnsd ? row : n2,
                       bnsd ? n2 : row, bcoord);
       }
     }
@@ -147,9 +153,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       constexpr uint32_t ID_DQ = idesc_f16(BM, D, kBF16, false, true);
       const uint32_t aQ = smem_u32(smem + C::oQ), adO = smem_u32(smem + C::odO);
       auto issue_s = [&](int t) -> bool {
-        const int st = t % NS;
-        const uint32_t aK = smem_u32(smem + C::oK + st * C::kK);
-        if (!wait_bar(&bars[kDqKvFull + st], (t / NS) & 1, abort_flag, a)) return false;
+        const int sk = t % NK;
+        const uint32_t aK = smem_u32(smem + C::oK + sk * C::kK);
+        if (!wait_bar(&bars[kDqKFull + sk], (t / NK) & 1, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -158,29 +164,34 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         mma_commit(&bars[kDqSFull + (t & 1)]);
         return true;
       };
-      auto issue_dp = [&](int t) {
-        const uint32_t aV = smem_u32(smem + C::oV + (t % NS) * C::kV);
+      auto issue_dp = [&](int t) -> bool {
+        const int sv = t % NV;
+        const uint32_t aV = smem_u32(smem + C::oV + sv * C::kV);
+        if (!wait_bar(&bars[kDqVFull + sv], (t / NV) & 1, abort_flag, a)) return false;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
           mma_ss(tmem + C::cP, sdesc_sw128(adO + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(aV + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
         mma_commit(&bars[kDqDpFull]);
+        mma_commit(&bars[kDqVEmpty + sv]);
+        return true;
       };
-      bool ok = wait_bar(&bars[kDqQdoFull], 0, abort_flag, a) && issue_s(0);
-      if (ok) issue_dp(0);
+      bool ok = wait_bar(&bars[kDqQdoFull], 0, abort_flag, a) && issue_s(0) && issue_dp(0);
       for (int t = 0; ok && t < T; ++t) {
         // S of the next key block into the other buffer (its dS was consumed by the previous dQ product)
         if (t + 1 < T && !(ok = issue_s(t + 1))) break;
         if (!(ok = wait_bar(&bars[kDqDsFull], t & 1, abort_flag, a))) break;
         tc_fence_after();
-        const uint32_t aK = smem_u32(smem + C::oK + (t % NS) * C::kK);
+        // every compute warp has read dP(t): the next dP may go ahead of this step's dQ product
+        if (t + 1 < T && !(ok = issue_dp(t + 1))) break;
+        const uint32_t aK = smem_u32(smem + C::oK + (t % NK) * C::kK);
         const uint32_t sb = tmem + C::cS0 + (t & 1) * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)  // dS of warpgroup kk/(NC/16) sits in its own S columns
           mma_ts(tmem + C::cDQ, sb + (kk / (NC / 16)) * NC + (kk % (NC / 16)) * 8,
                  sdesc_sw128(aK + kk * 2048, BN * 128, 1024), ID_DQ, (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[kDqKvEmpty + (t % NS)]);
-        if (t + 1 < T) issue_dp(t + 1);  // dP was read before the dS arrival awaited above
+        mma_commit(&bars[kDqKEmpty + (t % NK)]);
       }
       if (ok) {
         mma_commit(&bars[kDqAccDone]);
