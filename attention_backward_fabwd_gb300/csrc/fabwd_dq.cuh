@@ -16,8 +16,14 @@
 // Warp roles (320 threads): warps 0-7 compute (warp w reads TMEM lanes 32·(w%4)..+31; warps 0-3
 // take key columns [0, BN/2), warps 4-7 [BN/2, BN)), warp 8 issues TMA loads (Q, dO once; K
 // through a 3-stage ring released after dQ, V through a 2-stage ring released after dP), warp 9
-// allocates TMEM and issues the MMAs in the order S(t+1), dP(t+1), dQ(t): dP of the next key
-// block goes ahead of the current dQ product, so its dS can start as soon as P is ready.
+// allocates TMEM and issues the MMAs.  One thread issues every tcgen05.mma, and an MMA of these
+// shapes occupies it about as long as the tensor pipe takes to run it, so each barrier wait
+// between MMA groups idles the pipe.  The MMA thread therefore issues
+//     [dS(t) written] dP(t+1), dQ(t), [K(t+2) landed] S(t+2)
+// (S is double-buffered, so S(t+2) reuses the buffer whose dS dQ(t) has just read), and the
+// compute warps, not the MMA thread, wait for V(t+1) before they signal dS(t): that wait falls
+// while the warps wait for dP anyway.  K(t+2) stays with the MMA thread: its stage is freed by
+// dQ(t-1), too late for the compute warps to vouch for it by dS(t).
 // TMEM columns: dQ [0, D), S buffer 0 [D, D+BN), S buffer 1 [D+BN, D+2BN), dP [D+2BN, D+3BN).
 // Every mbarrier wait is bounded as in the kv-stationary kernel.
 #pragma once
@@ -152,39 +158,38 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       constexpr uint32_t ID_S = idesc_f16(BM, BN, kBF16, false, false);
       constexpr uint32_t ID_DQ = idesc_f16(BM, D, kBF16, false, true);
       const uint32_t aQ = smem_u32(smem + C::oQ), adO = smem_u32(smem + C::odO);
-      auto issue_s = [&](int t) -> bool {
-        const int sk = t % NK;
-        const uint32_t aK = smem_u32(smem + C::oK + sk * C::kK);
-        if (!wait_bar(&bars[kDqKFull + sk], (t / NK) & 1, abort_flag, a)) return false;
-        tc_fence_after();
+      auto issue_s = [&](int t) {  // K(t) landed (see above)
+        const uint32_t aK = smem_u32(smem + C::oK + (t % NK) * C::kK);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + C::cS0 + (t & 1) * BN, sdesc_sw128(aQ + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(aK + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
         mma_commit(&bars[kDqSFull + (t & 1)]);
-        return true;
       };
-      auto issue_dp = [&](int t) -> bool {
+      auto issue_dp = [&](int t) {  // V(t) landed (see above)
         const int sv = t % NV;
         const uint32_t aV = smem_u32(smem + C::oV + sv * C::kV);
-        if (!wait_bar(&bars[kDqVFull + sv], (t / NV) & 1, abort_flag, a)) return false;
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
           mma_ss(tmem + C::cP, sdesc_sw128(adO + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(aV + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
         mma_commit(&bars[kDqDpFull]);
         mma_commit(&bars[kDqVEmpty + sv]);
-        return true;
       };
-      bool ok = wait_bar(&bars[kDqQdoFull], 0, abort_flag, a) && issue_s(0) && issue_dp(0);
+      bool ok = wait_bar(&bars[kDqQdoFull], 0, abort_flag, a) && wait_bar(&bars[kDqKFull], 0, abort_flag, a) &&
+                wait_bar(&bars[kDqVFull], 0, abort_flag, a) && (T < 2 || wait_bar(&bars[kDqKFull + 1], 0, abort_flag, a));
+      // from here on V(t+1) is vouched for by the compute warps' dS(t) arrival
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+        if (T > 1) issue_s(1);
+      }
       for (int t = 0; ok && t < T; ++t) {
-        // S of the next key block into the other buffer (its dS was consumed by the previous dQ product)
-        if (t + 1 < T && !(ok = issue_s(t + 1))) break;
+        // dS(t) written, dP(t) read by every compute warp, V(t+1) landed
         if (!(ok = wait_bar(&bars[kDqDsFull], t & 1, abort_flag, a))) break;
         tc_fence_after();
-        // every compute warp has read dP(t): the next dP may go ahead of this step's dQ product
-        if (t + 1 < T && !(ok = issue_dp(t + 1))) break;
+        if (t + 1 < T) issue_dp(t + 1);
         const uint32_t aK = smem_u32(smem + C::oK + (t % NK) * C::kK);
         const uint32_t sb = tmem + C::cS0 + (t & 1) * BN;
 #pragma unroll
@@ -192,6 +197,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_ts(tmem + C::cDQ, sb + (kk / (NC / 16)) * NC + (kk % (NC / 16)) * 8,
                  sdesc_sw128(aK + kk * 2048, BN * 128, 1024), ID_DQ, (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kDqKEmpty + (t % NK)]);
+        if (t + 2 < T) {  // into the S buffer whose dS the dQ product above has read
+          if (!(ok = wait_bar(&bars[kDqKFull + (t + 2) % NK], ((t + 2) / NK) & 1, abort_flag, a))) break;
+          tc_fence_after();
+          issue_s(t + 2);
+        }
       }
       if (ok) {
         mma_commit(&bars[kDqAccDone]);
@@ -237,6 +247,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int c = 0; c < NC; ++c)
           if (jc + c < j_vis_lo || jc + c > j_vis_hi) p[c] = 0u;
       }
+      // the MMA thread issues dP(t+1) right after the dS(t) handoff below: its V stage must have landed
+      if (t + 1 < T && !(ok = wait_bar_warp(&bars[kDqVFull + (t + 1) % NV], ((t + 1) / NV) & 1, abort_flag, a))) break;
       if (!(ok = wait_bar_warp(&bars[kDqDpFull], t & 1, abort_flag, a))) break;
       tc_fence_after();
 #pragma unroll
