@@ -13,7 +13,14 @@
 // the dPᵀ columns frees the Sᵀ columns as soon as dV has read Pᵀ, so the MMA warp issues
 //     Sᵀ(t), dPᵀ(t), dV(t), Sᵀ(t+1), dK(t), dPᵀ(t+1), dV(t+1), ...
 // and the elementwise work of each step overlaps the previous step's dK and the next step's Sᵀ.
-// Warp 8 streams Q, dO, lse and sfmg through a 2-stage TMA ring (K and V are loaded once).
+// Warp 8 streams Q with lse·log2e through a 3-stage TMA ring and dO with sfmg through a 2-stage
+// ring (K and V are loaded once); a Q stage is released by a commit after dK, a dO stage by a commit
+// after dV together with an arrival of every compute warp once it has read the stage's sfmg.
+// One thread issues every tcgen05.mma, and an MMA of this shape occupies it about as long as the
+// tensor pipe takes to run it, so each barrier wait between MMA groups idles the pipe.  The MMA
+// thread therefore waits only for the compute warps' P and dS handoffs; the compute warps wait
+// for the TMA stages the MMA thread reads next (Q(t+1) before they hand over P(t), dO(t+1) before
+// dS(t)), which falls where they would otherwise idle.
 // TMEM columns: dK [0, D), dV [D, D+Dv), Sᵀ/Pᵀ [D+Dv, +128), dPᵀ/dSᵀ [D+Dv+128, +128).
 // Bounded waits, abort flag, drain and TMEM release as in the fused kernel.
 #pragma once
@@ -27,13 +34,13 @@ namespace fabwd {
 
 template <int D, int DV>
 struct KvCfg {
-  static constexpr int BR = 128, BC = kBlockKV, NS = 2;
+  static constexpr int BR = 128, BC = kBlockKV, NQ = 3, NO = 2;  // Q ring and dO ring stages
   static constexpr uint32_t kK = D * BC * 2, kV = DV * BC * 2, kQ = D * BR * 2, kdO = DV * BR * 2;
-  static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + NS * kQ;
-  static constexpr uint32_t oL = odO + NS * kdO;     // [NS][BR] fp32 lse·log2(e)
-  static constexpr uint32_t oF = oL + NS * BR * 4;   // [NS][BR] fp32 sfmg
-  static constexpr uint32_t oBar = oF + NS * BR * 4;
-  static constexpr uint32_t oMisc = oBar + 32 * 8;
+  static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + NQ * kQ;
+  static constexpr uint32_t oL = odO + NO * kdO;     // [NQ][BR] fp32 lse·log2(e)
+  static constexpr uint32_t oF = oL + NQ * BR * 4;   // [NO][BR] fp32 sfmg
+  static constexpr uint32_t oBar = oF + NO * BR * 4;
+  static constexpr uint32_t oMisc = oBar + 20 * 8;
   static constexpr uint32_t bytes = oMisc + 64;
   static constexpr uint32_t cDK = 0, cDV = D, cS = D + DV, cP = cS + BR;
   static_assert(D % 64 == 0 && DV % 64 == 0 && D <= 128 && DV <= D, "head dims");
@@ -41,8 +48,9 @@ struct KvCfg {
   static_assert(bytes <= 232448, "shared memory budget");
 };
 
-constexpr int kKvKvFull = 0, kKvQFull = 1 /*+2*/, kKvQEmpty = 3 /*+2*/, kKvSFull = 5, kKvDpFull = 6, kKvPFull = 7,
-              kKvDsFull = 8, kKvAccDone = 9, kKvNever = 10, kKvDrain = 11, kKvNumBars = 12;
+constexpr int kKvKvFull = 0, kKvQFull = 1 /*+3*/, kKvQEmpty = 4 /*+3*/, kKvOFull = 7 /*+2*/, kKvOEmpty = 9 /*+2*/,
+              kKvSFull = 11, kKvDpFull = 12, kKvPFull = 13, kKvDsFull = 14, kKvAccDone = 15, kKvNever = 16,
+              kKvDrain = 17, kKvNumBars = 18;
 
 template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
@@ -50,7 +58,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const MainArgs a) {
   using C = KvCfg<D, DV>;
-  constexpr int BR = C::BR, BC = C::BC, NS = C::NS;
+  constexpr int BR = C::BR, BC = C::BC, NQ = C::NQ, NO = C::NO;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -78,7 +86,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::oMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oMisc + 16);
   if (tid == 0) {
-    for (int i = 0; i < kKvNumBars; ++i) mbar_init(&bars[i], (i == kKvPFull || i == kKvDsFull) ? 8 : 1);
+    for (int i = 0; i < kKvNumBars; ++i) {
+      // P/dS handoffs: one arrival per compute warp; a dO stage: the dV commit + 8 compute warps
+      const bool oe = i >= kKvOEmpty && i < kKvOEmpty + NO;
+      mbar_init(&bars[i], (i == kKvPFull || i == kKvDsFull) ? 8 : (oe ? 9 : 1));
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -119,24 +131,27 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tma_load_4d(smem + C::oV + c * BC * 128, &tm_v, &bars[kKvKvFull], c * 64, bnsd ? kv_row0 : n2,
                     bnsd ? n2 : kv_row0, bcoord);
       for (int t = 0; t < T; ++t) {
-        const int st = t % NS;
+        const int sq_ = t % NQ, so = t % NO;
         const int h = t / nqb, qb = qb_begin + t % nqb;
         const int n1 = n2 * a.G + h, i0 = qb * BR;
-        if (t >= NS && !wait_bar(&bars[kKvQEmpty + st], ((t / NS) - 1) & 1, abort_flag, a)) break;
-        uint64_t* full = &bars[kKvQFull + st];
-        mbar_arrive_expect_tx(full, (D + DV) * BR * 2 + 2 * BR * 4);
         const int row = q_rowbase + i0;
+        const long long rbase = ((long long)b * a.N1 + n1) * a.S1p + i0;
+        if (t >= NQ && !wait_bar(&bars[kKvQEmpty + sq_], ((t / NQ) - 1) & 1, abort_flag, a)) break;
+        uint64_t* qfull = &bars[kKvQFull + sq_];
+        mbar_arrive_expect_tx(qfull, D * BR * 2 + BR * 4);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(smem + C::oQ + st * C::kQ + c * BR * 128, &tm_q, full, c * 64, bnsd ? row : n1,
+          tma_load_4d(smem + C::oQ + sq_ * C::kQ + c * BR * 128, &tm_q, qfull, c * 64, bnsd ? row : n1,
                       bnsd ? n1 : row, bcoord);
+        bulk_load(smem + C::oL + sq_ * BR * 4, a.lse2 + rbase, BR * 4, qfull);
+        if (t >= NO && !wait_bar(&bars[kKvOEmpty + so], ((t / NO) - 1) & 1, abort_flag, a)) break;
+        uint64_t* ofull = &bars[kKvOFull + so];
+        mbar_arrive_expect_tx(ofull, DV * BR * 2 + BR * 4);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(smem + C::odO + st * C::kdO + c * BR * 128, &tm_do, full, c * 64, bnsd ? row : n1,
+          tma_load_4d(smem + C::odO + so * C::kdO + c * BR * 128, &tm_do, ofull, c * 64, bnsd ? row : n1,
                       bnsd ? n1 : row, bcoord);
-        const long long rbase = ((long long)b * a.N1 + n1) * a.S1p + i0;
-        bulk_load(smem + C::oL + st * BR * 4, a.lse2 + rbase, BR * 4, full);
-        bulk_load(smem + C::oF + st * BR * 4, a.sfmg + rbase, BR * 4, full);
+        bulk_load(smem + C::oF + so * BR * 4, a.sfmg + rbase, BR * 4, ofull);
       }
     }
     __syncwarp();
@@ -150,46 +165,48 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       // A operand columns of k-step kk (16 queries): warpgroup kk/4 holds queries 64·(kk/4)..,
       // its 16-bit pairs at +0..31 of its own 64 columns
       auto a_col = [](int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; };
-      auto issue_s = [&](int t) -> bool {
-        const int st = t % NS;
-        const uint32_t aQ = smem_u32(smem + C::oQ + st * C::kQ);
-        if (!wait_bar(&bars[kKvQFull + st], (t / NS) & 1, abort_flag, a)) return false;
-        tc_fence_after();
+      auto issue_s = [&](int t) {  // Q(t) landed: vouched for by the compute warps' P(t-1) handoff
+        const uint32_t aQ = smem_u32(smem + C::oQ + (t % NQ) * C::kQ);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + C::cS, sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(aQ + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
         mma_commit(&bars[kKvSFull]);
-        return true;
       };
-      auto issue_dp = [&](int t) {
-        const uint32_t adO = smem_u32(smem + C::odO + (t % NS) * C::kdO);
+      auto issue_dp = [&](int t) {  // dO(t) landed: vouched for by the compute warps' dS(t-1) handoff
+        const uint32_t adO = smem_u32(smem + C::odO + (t % NO) * C::kdO);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
           mma_ss(tmem + C::cP, sdesc_sw128(aV + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(adO + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
         mma_commit(&bars[kKvDpFull]);
       };
-      bool ok = wait_bar(&bars[kKvKvFull], 0, abort_flag, a) && issue_s(0);
-      if (ok) issue_dp(0);
+      bool ok = wait_bar(&bars[kKvKvFull], 0, abort_flag, a) && wait_bar(&bars[kKvQFull], 0, abort_flag, a) &&
+                wait_bar(&bars[kKvOFull], 0, abort_flag, a);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
       for (int t = 0; ok && t < T; ++t) {
-        const int st = t % NS;
-        const uint32_t aQ = smem_u32(smem + C::oQ + st * C::kQ), adO = smem_u32(smem + C::odO + st * C::kdO);
+        const int sq_ = t % NQ, so = t % NO;
+        const uint32_t aQ = smem_u32(smem + C::oQ + sq_ * C::kQ), adO = smem_u32(smem + C::odO + so * C::kdO);
         if (!(ok = wait_bar(&bars[kKvPFull], t & 1, abort_flag, a))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BR / 16; ++kk)
           mma_ts(tmem + C::cDV, tmem + C::cS + a_col(kk), sdesc_sw128(adO + kk * 2048, BR * 128, 1024), ID_DV,
                  (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kKvOEmpty + so]);  // dO(t) read; the compute warps add their sfmg arrivals
         // Sᵀ of the next step may overwrite the Pᵀ columns once dV (issued above) has read them
-        if (t + 1 < T && !(ok = issue_s(t + 1))) break;
+        if (t + 1 < T) issue_s(t + 1);
         if (!(ok = wait_bar(&bars[kKvDsFull], t & 1, abort_flag, a))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BR / 16; ++kk)
           mma_ts(tmem + C::cDK, tmem + C::cP + a_col(kk), sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK,
                  (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[kKvQEmpty + st]);
+        mma_commit(&bars[kKvQEmpty + sq_]);
         if (t + 1 < T) issue_dp(t + 1);  // after dK read the dSᵀ held in the dPᵀ columns
       }
       if (ok) {
@@ -212,15 +229,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const int i_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
     const int i_vis_hi = (int)(vhi < -1 ? -1 : (vhi > (1 << 30) ? (1 << 30) : vhi));
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int st = t % NS;
+    if (T > 0) ok = wait_bar_warp(&bars[kKvQFull], 0, abort_flag, a) && wait_bar_warp(&bars[kKvOFull], 0, abort_flag, a);
+    for (int t = 0; ok && t < T; ++t) {
+      const int sq_ = t % NQ, so = t % NO;
       const int qb = qb_begin + t % nqb;
       const int i0 = qb * BR, ic0 = i0 + g * 64;
-      if (!(ok = wait_bar_warp(&bars[kKvQFull + st], (t / NS) & 1, abort_flag, a))) break;
+      // lse(t) and sfmg(t) landed: observed before the previous step's handoffs (or above)
       if (!(ok = wait_bar_warp(&bars[kKvSFull], t & 1, abort_flag, a))) break;
       tc_fence_after();
-      const float4* sL4 = reinterpret_cast<const float4*>(smem + C::oL + st * BR * 4 + g * 256);
-      const float4* sF4 = reinterpret_cast<const float4*>(smem + C::oF + st * BR * 4 + g * 256);
+      const float4* sL4 = reinterpret_cast<const float4*>(smem + C::oL + sq_ * BR * 4 + g * 256);
+      const float4* sF4 = reinterpret_cast<const float4*>(smem + C::oF + so * BR * 4 + g * 256);
       const long long dmin = (long long)j0 - (i0 + BR - 1) - off, dmax = (long long)(j1 - 1) - i0 - off;
       const bool full = dmin >= lo && dmax <= hi;
       uint32_t p0[32], p1[32];  // Sᵀ row (64 queries), then P (fp32 bits)
@@ -260,9 +278,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tmem_st32(sS, pk);  // Pᵀ over this warpgroup's own (already read) Sᵀ columns
         tmem_wait_st();
       }
+      // the MMA thread issues Sᵀ(t+1) right after this handoff: its Q stage must have landed
+      if (t + 1 < T && !(ok = wait_bar_warp(&bars[kKvQFull + (t + 1) % NQ], ((t + 1) / NQ) & 1, abort_flag, a))) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kKvPFull]);
+      // and dPᵀ(t+1) right after the dS handoff: its dO stage must have landed
+      if (t + 1 < T && !(ok = wait_bar_warp(&bars[kKvOFull + (t + 1) % NO], ((t + 1) / NO) & 1, abort_flag, a))) break;
       if (!(ok = wait_bar_warp(&bars[kKvDpFull], t & 1, abort_flag, a))) break;
       tc_fence_after();
       {
@@ -291,7 +313,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kKvDsFull]);
+      if (lane == 0) {
+        mbar_arrive(&bars[kKvDsFull]);
+        mbar_arrive(&bars[kKvOEmpty + so]);  // this warp's sfmg reads of stage so are done
+      }
     }
     // ---- epilogue: dK = scale · acc, dV = acc; zeros when no query sees this block
     if (ok && T > 0) ok = wait_bar_warp(&bars[kKvAccDone], 0, abort_flag, a);
