@@ -17,7 +17,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <bool FP16, int DV>
+template <bool FP16, int DV, bool SMALL>
 __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     unsigned st = 0;
@@ -33,62 +33,89 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
     *a.status = st;
   }
 
+  // Grid-stride over rows (b, i, n1) in the layout's row order over the padded length S1p; each
+  // lane group of LPR lanes takes UN rows per iteration, whose dout, attn_out and lse loads are
+  // all issued before the arithmetic.  SMALL: every row index fits 32 bits, so the per-row
+  // index split uses 32-bit division.
   constexpr int LPR = DV / 8;    // lanes per row: one 16-byte chunk (8 elements) each
   constexpr int RPW = 32 / LPR;  // rows per warp step
+  constexpr int UN = 2;          // row groups per iteration
   const long long nrows = (long long)a.B * a.N1 * a.S1p;
   const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, part = lane % LPR;
-  for (long long base = gwarp * RPW; base < nrows; base += nwarp * RPW) {
-    const long long w = base + sub;
-    const bool active = w < nrows;
-    int b = 0, n1 = 0;
-    long long i = 0;
-    if (active) {
-      if (a.layout == kBNSD) {
-        i = w % a.S1p;
-        n1 = (int)((w / a.S1p) % a.N1);
-        b = (int)(w / ((long long)a.S1p * a.N1));
-      } else {
-        n1 = (int)(w % a.N1);
-        i = (w / a.N1) % a.S1p;
-        b = (int)(w / ((long long)a.N1 * a.S1p));
+  const bool bnsd = a.layout == kBNSD, tnd = a.layout == kTND;
+  for (long long base = gwarp * RPW * UN; base < nrows; base += nwarp * RPW * UN) {
+    uint4 x[UN], y[UN];
+    float l[UN];
+    bool act[UN], val[UN];
+    long long o[UN];
+#pragma unroll
+    for (int u = 0; u < UN; ++u) {
+      const long long w = base + u * RPW + sub;
+      act[u] = w < nrows;
+      int b = 0, n1 = 0;
+      long long i = 0;
+      if (act[u]) {
+        if (SMALL) {
+          const uint32_t w32 = (uint32_t)w, S1p = (uint32_t)a.S1p, N1 = (uint32_t)a.N1;
+          if (bnsd) {
+            const uint32_t hq = w32 / S1p;
+            i = w32 - hq * S1p;
+            b = (int)(hq / N1);
+            n1 = (int)(hq - (uint32_t)b * N1);
+          } else {
+            const uint32_t tq = w32 / N1;
+            n1 = (int)(w32 - tq * N1);
+            b = (int)(tq / S1p);
+            i = tq - (uint32_t)b * S1p;
+          }
+        } else if (bnsd) {
+          i = w % a.S1p;
+          n1 = (int)((w / a.S1p) % a.N1);
+          b = (int)(w / ((long long)a.S1p * a.N1));
+        } else {
+          n1 = (int)(w % a.N1);
+          i = (w / a.N1) % a.S1p;
+          b = (int)(w / ((long long)a.N1 * a.S1p));
+        }
+      }
+      long long q0 = 0, L1 = a.S1;
+      if (act[u] && tnd) {
+        q0 = a.cu_q[b];
+        L1 = (long long)a.cu_q[b + 1] - q0;
+        if (q0 < 0 || q0 > a.T1) L1 = 0;                 // bad cu_seqlens: touch nothing
+        L1 = L1 < 0 ? 0 : (L1 > a.S1 ? a.S1 : L1);
+        if (q0 + L1 > a.T1) L1 = a.T1 - q0 < 0 ? 0 : a.T1 - q0;
+      }
+      val[u] = act[u] && i < L1;
+      o[u] = ((long long)b * a.N1 + n1) * a.S1p + i;
+      x[u] = y[u] = make_uint4(0u, 0u, 0u, 0u);
+      l[u] = 0.f;
+      if (val[u]) {
+        const long long r = row_index(a.layout, b, q0 + i, n1, a.N1, a.S1);
+        x[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * DV + part * 8);
+        y[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.attn_out) + r * DV + part * 8);
+        if (part == 0) l[u] = a.lse[tnd ? (long long)n1 * a.T1 + q0 + i : ((long long)b * a.N1 + n1) * a.S1 + i];
       }
     }
-    long long q0 = 0, L1 = a.S1;
-    if (active && a.layout == kTND) {
-      q0 = a.cu_q[b];
-      L1 = (long long)a.cu_q[b + 1] - q0;
-      if (q0 < 0 || q0 > a.T1) L1 = 0;                 // bad cu_seqlens: touch nothing
-      L1 = L1 < 0 ? 0 : (L1 > a.S1 ? a.S1 : L1);
-      if (q0 + L1 > a.T1) L1 = a.T1 - q0 < 0 ? 0 : a.T1 - q0;
-    }
-    const bool valid = active && i < L1;
-    float acc = 0.f;
-    if (valid) {
-      const long long r = row_index(a.layout, b, q0 + i, n1, a.N1, a.S1);
-      const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * DV + part * 8);
-      const uint4 y = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.attn_out) + r * DV + part * 8);
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int u = 0; u < UN; ++u) {
+      const uint32_t xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w}, ys[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+      float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 xf = unpack2<FP16>(xs[e]), yf = unpack2<FP16>(ys[e]);
         acc = fmaf(xf.x, yf.x, acc);
         acc = fmaf(xf.y, yf.y, acc);
       }
-    }
 #pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (active && part == 0) {
-      const long long o = ((long long)b * a.N1 + n1) * a.S1p + i;
-      float l2 = INFINITY;
-      if (valid) {
-        const long long li = a.layout == kTND ? (long long)n1 * a.T1 + q0 + i : ((long long)b * a.N1 + n1) * a.S1 + i;
-        l2 = a.lse[li] * kLog2e;
+      for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (act[u] && part == 0) {
+        a.lse2[o[u]] = val[u] ? l[u] * kLog2e : INFINITY;
+        a.sfmg[o[u]] = val[u] ? acc : 0.f;
       }
-      a.lse2[o] = l2;
-      a.sfmg[o] = valid ? acc : 0.f;
     }
   }
 
@@ -142,12 +169,13 @@ cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st) {
   const long long rows = (long long)a.B * a.N1 * a.S1p;
   const long long work = rows * (a.Dv / 8) > a.dq_acc_elems / 4 ? rows * (a.Dv / 8) : a.dq_acc_elems / 4;
   const int grid = grid_for(work, 256);
+  const bool small = rows < (1ll << 31);
   if (a.Dv == 128) {
-    if (fp16) preprocess_kernel<true, 128><<<grid, 256, 0, st>>>(a);
-    else preprocess_kernel<false, 128><<<grid, 256, 0, st>>>(a);
+    if (fp16) small ? preprocess_kernel<true, 128, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<true, 128, false><<<grid, 256, 0, st>>>(a);
+    else small ? preprocess_kernel<false, 128, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<false, 128, false><<<grid, 256, 0, st>>>(a);
   } else if (a.Dv == 64) {
-    if (fp16) preprocess_kernel<true, 64><<<grid, 256, 0, st>>>(a);
-    else preprocess_kernel<false, 64><<<grid, 256, 0, st>>>(a);
+    if (fp16) small ? preprocess_kernel<true, 64, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<true, 64, false><<<grid, 256, 0, st>>>(a);
+    else small ? preprocess_kernel<false, 64, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<false, 64, false><<<grid, 256, 0, st>>>(a);
   } else {
     return cudaErrorInvalidValue;
   }
