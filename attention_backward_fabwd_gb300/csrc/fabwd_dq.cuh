@@ -55,21 +55,20 @@ constexpr int kDqQdoFull = 0, kDqKFull = 1 /*+3*/, kDqKEmpty = 4 /*+3*/, kDqVFul
               kDqSFull = 11 /*+2*/, kDqDpFull = 13, kDqDsFull = 14, kDqAccDone = 15, kDqNever = 16, kDqDrain = 17,
               kDqNumBars = 18;
 
+// One CTA of the dQ kernel: query block (latest first) bx / N1 of q-head bx % N1, batch by.
 template <int D, int DV, bool FP16>
-__global__ void __launch_bounds__(kMainThreads, 1)
-    fabwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const MainArgs a) {
+__device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                         const CUtensorMap& tm_do, const MainArgs& a, int bx, int by) {
   using C = DqCfg<D, DV>;
   constexpr int BM = C::BM, BN = C::BN, NK = C::NK, NV = C::NV, NC = C::NC;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y;
+  const int b = by;
   SeqRange sq;
   if (!seq_range(a, b, sq)) return;  // bad cu_seqlens: the preprocess kernel reports it
   const int nqb_all = (a.S1 + BM - 1) / BM;
-  const int qb = nqb_all - 1 - (int)(blockIdx.x / a.N1), n1 = blockIdx.x % a.N1;  // latest query blocks first
+  const int qb = nqb_all - 1 - bx / a.N1, n1 = bx % a.N1;  // latest query blocks first
   const int i0 = qb * BM;
   if (i0 >= sq.L1) return;
   if ((smem_u32(smem) & 1023u) != 0) {
@@ -309,6 +308,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+template <int D, int DV, bool FP16>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    fabwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const MainArgs a) {
+  dq_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
 }
 
 template <int D, int DV, bool FP16>

@@ -86,6 +86,10 @@ cudaError_t launch_dq_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, 
 cudaError_t launch_kv_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
 cudaError_t launch_kv_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
 cudaError_t launch_dq_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
+// Both separate-mode kernels in one launch (dK/dV CTAs, then dQ CTAs); D <= 128, maps with
+// 128-row boxes on both sides.  Returns cudaErrorInvalidValue for other head dims.
+cudaError_t launch_bwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
+cudaError_t launch_bwd_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
 bool main_supported(int D, int Dv);
 
 }  // namespace fabwd

@@ -52,17 +52,16 @@ constexpr int kKvKvFull = 0, kKvQFull = 1 /*+3*/, kKvQEmpty = 4 /*+3*/, kKvOFull
               kKvSFull = 11, kKvDpFull = 12, kKvPFull = 13, kKvDsFull = 14, kKvAccDone = 15, kKvNever = 16,
               kKvDrain = 17, kKvNumBars = 18;
 
+// One CTA of the dK/dV kernel: key block bx / N2 of kv-head bx % N2, batch (or sequence) by.
 template <int D, int DV, bool FP16>
-__global__ void __launch_bounds__(kMainThreads, 1)
-    fabwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const MainArgs a) {
+__device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                         const CUtensorMap& tm_do, const MainArgs& a, int bx, int by) {
   using C = KvCfg<D, DV>;
   constexpr int BR = C::BR, BC = C::BC, NQ = C::NQ, NO = C::NO;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int jb = blockIdx.x / a.N2, n2 = blockIdx.x % a.N2, b = blockIdx.y;
+  const int jb = bx / a.N2, n2 = bx % a.N2, b = by;
   SeqRange sq;
   if (!seq_range(a, b, sq)) return;  // bad cu_seqlens: the preprocess kernel reports it
   const int j0 = jb * BC;
@@ -375,6 +374,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+template <int D, int DV, bool FP16>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    fabwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const MainArgs a) {
+  kv_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
 }
 
 template <int D, int DV, bool FP16>

@@ -1,0 +1,44 @@
+// One launch for the whole separate-mode backward (D <= 128): the CTAs of the dK/dV kernel
+// (heaviest key blocks first) followed by those of the dQ kernel (heaviest query blocks first).
+// Both CTA kinds take one SM each (shared memory and all 512 TMEM columns), read only the
+// inputs and the preprocess rows, and write disjoint outputs, so they need no ordering between
+// them; putting them in one grid lets the dQ CTAs fill the SMs that the short dK/dV CTAs leave
+// while the long ones (the first key blocks under a causal mask) are still running, instead of
+// the dK/dV grid's tail leaving SMs idle before a second launch.
+#pragma once
+
+#include "fabwd_dq.cuh"
+#include "fabwd_kv.cuh"
+
+namespace fabwd {
+
+template <int D, int DV, bool FP16>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    fabwd_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const MainArgs a, int kv_ctas) {
+  if ((int)blockIdx.x < kv_ctas)
+    kv_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
+  else
+    dq_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x - kv_ctas, blockIdx.y);
+}
+
+template <int D, int DV, bool FP16>
+cudaError_t launch_bwd_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
+  static_assert(DqCfg<D, DV>::BN == KvCfg<D, DV>::BC, "one tensor map box for both CTA kinds");
+  constexpr uint32_t bytes = KvCfg<D, DV>::bytes > DqCfg<D, DV>::bytes ? KvCfg<D, DV>::bytes : DqCfg<D, DV>::bytes;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fabwd_bwd_kernel<D, DV, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)bytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int kv_ctas = n_kv_blocks * a.N2;
+  const int dq_ctas = ((a.S1 + DqCfg<D, DV>::BM - 1) / DqCfg<D, DV>::BM) * a.N1;
+  dim3 grid(kv_ctas + dq_ctas, a.B);
+  fabwd_bwd_kernel<D, DV, FP16><<<grid, kMainThreads, bytes, st>>>(m.q, m.k, m.v, m.dout, a, kv_ctas);
+  return cudaGetLastError();
+}
+
+}  // namespace fabwd

@@ -305,7 +305,12 @@ def stage_table(pb, r, peak_tf, peak_hbm):
                 "TFLOP/s": tf, "frac_of_peak": tf / peak_tf}
 
     out = {"preprocess": hbm("preprocess_kernel", r["ms_pre"], pre_bytes)}
-    if r["separate"]:
+    if r.get("merged"):
+        # one grid of dK/dV CTAs (S, dP, dV, dK) and dQ CTAs (S, dP again, dQ)
+        out["backward"] = tensor("fabwd_bwd_kernel", r["ms_main"], 2 * (2 * w.D + 2 * w.Dv) + 2 * (2 * w.D + w.Dv))
+        if r.get("alone"):
+            out["backward"]["launched_alone_ms"] = r["alone"]
+    elif r["separate"]:
         out["dkdv"] = tensor("fabwd_kv_kernel" if w.D <= 128 else "fabwd_main_kernel", r["ms_main"],
                              2 * (2 * w.D + 2 * w.Dv))
         out["dq"] = tensor("fabwd_dq_kernel", r["ms_conv"], 2 * (2 * w.D + w.Dv))
@@ -372,12 +377,21 @@ def gpu_arm(args, rank, world, local_rank):
     sp = st.cuda_stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
+    # separate dQ mode with D <= 128: fabwd_run launches the dK/dV and dQ CTAs as one grid
+    merged = resolved == fabwd.FABWD_DQ_SEPARATE and w.D <= 128
+
     def step(evs=None):
         if evs:
             evs[0].record(st)
         fabwd.fabwd_preprocess(p, ws.data_ptr(), nbytes, sp)
         if evs:
             evs[1].record(st)
+        if merged:
+            fabwd.fabwd_run(p, ws.data_ptr(), nbytes, sp)
+            if evs:
+                evs[2].record(st)
+                evs[3].record(st)
+            return
         fabwd.fabwd_run_main(p, ws.data_ptr(), nbytes, sp)
         if evs:
             evs[2].record(st)
@@ -426,6 +440,22 @@ def gpu_arm(args, rank, world, local_rank):
     if s_ != fabwd.FABWD_OK:
         raise RuntimeError(f"device status {bits:#x} after the timed steps")
 
+    # breakdown only (untimed region): the dK/dV and dQ kernels launched on their own
+    alone = None
+    if merged:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(10)]
+        for e_ in ev:
+            flush.fill_(3)
+            fabwd.fabwd_preprocess(p, ws.data_ptr(), nbytes, sp)
+            e_[0].record(st)
+            fabwd.fabwd_run_main(p, ws.data_ptr(), nbytes, sp)
+            e_[1].record(st)
+            fabwd.fabwd_run_dq(p, ws.data_ptr(), nbytes, sp)
+            e_[2].record(st)
+        torch.cuda.synchronize(dev)
+        alone = {"dkdv_ms": statistics.mean(e_[0].elapsed_time(e_[1]) for e_ in ev),
+                 "dq_ms": statistics.mean(e_[1].elapsed_time(e_[2]) for e_ in ev)}
+
     # e2e: host buffers through the C ABI, copies inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -454,7 +484,7 @@ def gpu_arm(args, rank, world, local_rank):
         [ms_step, ms_main, statistics.mean(pre), statistics.mean(conv), e2e["ms"] if e2e else 0.0, t_wall], world, dev)
     return dict(pb=pb, w=w, ms_step=ms_step, ms_main=ms_main, ms_pre=ms_pre, ms_conv=ms_conv, e2e=e2e, e2e_ms=e2e_ms,
                 t_wall=t_wall, clocks=clk.summary(), dq_elems=dq.numel(), nbytes=nbytes,
-                separate=resolved == fabwd.FABWD_DQ_SEPARATE)
+                separate=resolved == fabwd.FABWD_DQ_SEPARATE, merged=merged, alone=alone)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -620,7 +650,7 @@ def main():
                      "flops_per_pair": dom["flops_per_pair"]},
         "kernels": stages,
         "flops_convention": conv, "flops_algorithmic": alg,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (2 if r["merged"] else 3) * args.steps,
         "clocks": r["clocks"],
         "wall_s_timed_region": r["t_wall"],
     }

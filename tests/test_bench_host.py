@@ -8,8 +8,9 @@ import pytest
 from attention_backward_fabwd_gb300 import inputs
 
 
-def _r(separate, ms=(0.01, 0.2, 0.1)):
-    return {"separate": separate, "ms_pre": ms[0], "ms_main": ms[1], "ms_conv": ms[2], "dq_elems": 1000}
+def _r(separate, ms=(0.01, 0.2, 0.1), merged=False):
+    return {"separate": separate, "ms_pre": ms[0], "ms_main": ms[1], "ms_conv": ms[2], "dq_elems": 1000,
+            "merged": merged}
 
 
 def test_stage_table_splits_the_five_products():
@@ -27,6 +28,10 @@ def test_stage_table_splits_the_five_products():
     assert sep["dq"]["flops_per_pair"] == 2 * (2 * w.D + w.Dv)
     assert sep["dkdv"]["flops"] + sep["dq"]["flops"] == pytest.approx(alg * (4 * w.D + 3 * w.Dv) / (3 * w.D + 2 * w.Dv))
     assert sep["dkdv"]["TFLOP/s"] == pytest.approx(sep["dkdv"]["flops"] / 0.2e-3 / 1e12)
+    # one grid for both separate-mode kernels: their products together
+    mer = bench.stage_table(pb, _r(True, merged=True), 1000.0, 5000.0)
+    assert set(mer) == {"preprocess", "backward"}
+    assert mer["backward"]["flops"] == pytest.approx(sep["dkdv"]["flops"] + sep["dq"]["flops"])
     # the separate mode has no fp32 accumulator to zero
     assert ato["preprocess"]["bytes"] - sep["preprocess"]["bytes"] == 4 * 1000
     assert ato["convert"]["bytes"] == 6 * 1000
