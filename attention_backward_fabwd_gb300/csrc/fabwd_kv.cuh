@@ -233,7 +233,10 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
       const int sq_ = t % NQ, so = t % NO;
       const int qb = qb_begin + t % nqb;
       const int i0 = qb * BR, ic0 = i0 + g * 64;
-      // lse(t) and sfmg(t) landed: observed before the previous step's handoffs (or above)
+      // lse(t) and sfmg(t) landed: observed before the previous step's handoffs (or above).  The
+      // MMA thread issues Sᵀ(t+1) right after this step's P handoff: its Q stage (loaded long
+      // ago) is confirmed here, while the warps would wait for Sᵀ(t) anyway.
+      if (t + 1 < T && !(ok = wait_bar_warp(&bars[kKvQFull + (t + 1) % NQ], ((t + 1) / NQ) & 1, abort_flag, a))) break;
       if (!(ok = wait_bar_warp(&bars[kKvSFull], t & 1, abort_flag, a))) break;
       tc_fence_after();
       const float4* sL4 = reinterpret_cast<const float4*>(smem + C::oL + sq_ * BR * 4 + g * 256);
@@ -277,8 +280,6 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
         tmem_st32(sS, pk);  // Pᵀ over this warpgroup's own (already read) Sᵀ columns
         tmem_wait_st();
       }
-      // the MMA thread issues Sᵀ(t+1) right after this handoff: its Q stage must have landed
-      if (t + 1 < T && !(ok = wait_bar_warp(&bars[kKvQFull + (t + 1) % NQ], ((t + 1) / NQ) & 1, abort_flag, a))) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kKvPFull]);
