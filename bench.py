@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-breakdown", action="store_true",
+                    help="skip the untimed pass that launches the dK/dV and dQ kernels on their own")
     return ap.parse_args()
 
 
@@ -321,7 +323,8 @@ def stage_table(pb, r, peak_tf, peak_hbm):
 
 
 # revision of each kernel's code that profiles/traffic.json must match
-KERNEL_REV = {"fabwd_kv_kernel": "kv-v1", "fabwd_dq_kernel": "dq-v1", "fabwd_main_kernel": "main-v4"}
+KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v1", "fabwd_kv_kernel": "kv-v3", "fabwd_dq_kernel": "dq-v3",
+              "fabwd_main_kernel": "main-v4"}
 
 
 def max_over_ranks(values, world, device="cpu"):
@@ -442,7 +445,7 @@ def gpu_arm(args, rank, world, local_rank):
 
     # breakdown only (untimed region): the dK/dV and dQ kernels launched on their own
     alone = None
-    if merged:
+    if merged and not args.no_breakdown:
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(10)]
         for e_ in ev:
             flush.fill_(3)
