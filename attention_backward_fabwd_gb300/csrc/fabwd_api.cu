@@ -325,17 +325,27 @@ fabwd_status fabwd_run(const fabwd_params* p, void* ws, size_t ws_bytes, void* s
   fabwd_status s = plan_and_check(p, &pl, true);
   if (s != FABWD_OK) return s;
   if ((s = check_ws(pl, ws, ws_bytes)) != FABWD_OK) return s;
-  if (pl.separate && p->D <= 128 && any_pair(p, pl)) {
-    // separate mode, D <= 128: the dK/dV and dQ kernels as one grid (same tensor maps)
+  if (pl.separate && any_pair(p, pl)) {
+    // separate mode: the dK/dV and dQ CTAs as one grid (one set of tensor maps for D <= 128,
+    // one per CTA kind above)
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int inject = g_inject_timeout;
     g_inject_timeout = 0;
-    MainMaps maps;
-    if (!make_maps(p, &maps, 128, kBlockKV)) return FABWD_ERR_CUDA;
     const MainArgs a = main_args(p, pl, static_cast<uint8_t*>(ws), inject);
     const int n_kv_blocks = (int)((p->S2 + kBlockKV - 1) / kBlockKV);
-    const cudaError_t e = p->dtype == FABWD_FP16 ? launch_bwd_fp16(a, maps, (int)p->D, (int)p->Dv, n_kv_blocks, st)
-                                                 : launch_bwd_bf16(a, maps, (int)p->D, (int)p->Dv, n_kv_blocks, st);
+    const bool fp16 = p->dtype == FABWD_FP16;
+    const int D = (int)p->D, Dv = (int)p->Dv;
+    cudaError_t e;
+    if (D <= 128) {
+      MainMaps maps;
+      if (!make_maps(p, &maps, 128, kBlockKV)) return FABWD_ERR_CUDA;
+      e = fp16 ? launch_bwd_fp16(a, maps, D, Dv, n_kv_blocks, st) : launch_bwd_bf16(a, maps, D, Dv, n_kv_blocks, st);
+    } else {
+      MainMaps mkv, mdq;
+      if (!make_maps(p, &mkv, kBlockQ, kBlockKV) || !make_maps(p, &mdq, kDqBlockQ, 64)) return FABWD_ERR_CUDA;
+      e = fp16 ? launch_bwd_wide_fp16(a, mkv, mdq, D, Dv, n_kv_blocks, st)
+               : launch_bwd_wide_bf16(a, mkv, mdq, D, Dv, n_kv_blocks, st);
+    }
     return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
   }
   s = fabwd_run_main(p, ws, ws_bytes, stream);

@@ -90,6 +90,12 @@ cudaError_t launch_dq_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, 
 // 128-row boxes on both sides.  Returns cudaErrorInvalidValue for other head dims.
 cudaError_t launch_bwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
 cudaError_t launch_bwd_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
+// The same for D > 128 (D = 192, Dv = 128): mkv are the kv-stationary kernel's maps (64-row query,
+// 128-row key boxes), mdq the dQ kernel's (128-row query, 64-row key boxes).
+cudaError_t launch_bwd_wide_bf16(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int D, int Dv,
+                                 int n_kv_blocks, cudaStream_t st);
+cudaError_t launch_bwd_wide_fp16(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int D, int Dv,
+                                 int n_kv_blocks, cudaStream_t st);
 bool main_supported(int D, int Dv);
 
 }  // namespace fabwd

@@ -135,17 +135,16 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, vo
 
 // FUSED: also compute dQᵀ and reduce it into the fp32 workspace accumulator (atomic dQ mode);
 // otherwise the kernel produces dK and dV only and a separate q-stationary kernel computes dQ.
+// One CTA of the kv-stationary kernel: key block bx / N2 of kv-head bx % N2, batch (or sequence) by.
 template <int D, int DV, bool FP16, bool FUSED>
-__global__ void __launch_bounds__(kMainThreads, 1)
-    fabwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                      const MainArgs a) {
+__device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                           const CUtensorMap& tm_do, const MainArgs& a, int bx, int by) {
   using C = MainCfg<D, DV, FUSED>;
   constexpr int BR = C::BR, BC = C::BC, NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int jb = blockIdx.x / a.N2, n2 = blockIdx.x % a.N2, b = blockIdx.y;
+  const int jb = bx / a.N2, n2 = bx % a.N2, b = by;
 
   SeqRange sq;
   if (!seq_range(a, b, sq)) return;  // bad cu_seqlens: the preprocess kernel reports it
@@ -543,6 +542,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+template <int D, int DV, bool FP16, bool FUSED>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    fabwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                      const MainArgs a) {
+  main_block<D, DV, FP16, FUSED>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
 }
 
 template <int D, int DV, bool FP16, bool FUSED>

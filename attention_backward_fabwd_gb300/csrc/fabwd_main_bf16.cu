@@ -23,4 +23,9 @@ cudaError_t launch_bwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv,
   if (D == 128 && Dv == 128) return launch_bwd_t<128, 128, false>(a, m, n_kv_blocks, st);
   return cudaErrorInvalidValue;
 }
+cudaError_t launch_bwd_wide_bf16(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int D, int Dv,
+                                  int n_kv_blocks, cudaStream_t st) {
+  if (D == 192 && Dv == 128) return launch_bwd_wide_t<192, 128, false>(a, mkv, mdq, n_kv_blocks, st);
+  return cudaErrorInvalidValue;
+}
 }  // namespace fabwd

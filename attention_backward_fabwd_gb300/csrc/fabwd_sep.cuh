@@ -1,4 +1,4 @@
-// One launch for the whole separate-mode backward (D <= 128): the CTAs of the dK/dV kernel
+// One launch for the whole separate-mode backward: the CTAs of the dK/dV kernel
 // (heaviest key blocks first) followed by those of the dQ kernel (heaviest query blocks first).
 // Both CTA kinds take one SM each (shared memory and all 512 TMEM columns), read only the
 // inputs and the preprocess rows, and write disjoint outputs, so they need no ordering between
@@ -38,6 +38,42 @@ cudaError_t launch_bwd_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, 
   const int dq_ctas = ((a.S1 + DqCfg<D, DV>::BM - 1) / DqCfg<D, DV>::BM) * a.N1;
   dim3 grid(kv_ctas + dq_ctas, a.B);
   fabwd_bwd_kernel<D, DV, FP16><<<grid, kMainThreads, bytes, st>>>(m.q, m.k, m.v, m.dout, a, kv_ctas);
+  return cudaGetLastError();
+}
+
+// D > 128: the two CTA kinds take different tensor-map boxes (the kv-stationary kernel streams
+// 64-row query tiles against 128 resident keys, the dQ kernel 64-key tiles against 128 resident
+// queries), so this grid gets both sets of maps.
+template <int D, int DV, bool FP16>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    fabwd_bwd_wide_kernel(const __grid_constant__ CUtensorMap kq, const __grid_constant__ CUtensorMap kk,
+                          const __grid_constant__ CUtensorMap kvv, const __grid_constant__ CUtensorMap kdo,
+                          const __grid_constant__ CUtensorMap qq, const __grid_constant__ CUtensorMap qk,
+                          const __grid_constant__ CUtensorMap qv, const __grid_constant__ CUtensorMap qdo,
+                          const MainArgs a, int kv_ctas) {
+  if ((int)blockIdx.x < kv_ctas)
+    main_block<D, DV, FP16, false>(kq, kk, kvv, kdo, a, blockIdx.x, blockIdx.y);
+  else
+    dq_block<D, DV, FP16>(qq, qk, qv, qdo, a, blockIdx.x - kv_ctas, blockIdx.y);
+}
+
+template <int D, int DV, bool FP16>
+cudaError_t launch_bwd_wide_t(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int n_kv_blocks,
+                              cudaStream_t st) {
+  constexpr uint32_t kb = MainCfg<D, DV, false>::bytes, qb = DqCfg<D, DV>::bytes;
+  constexpr uint32_t bytes = kb > qb ? kb : qb;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fabwd_bwd_wide_kernel<D, DV, FP16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int kv_ctas = n_kv_blocks * a.N2;
+  const int dq_ctas = ((a.S1 + DqCfg<D, DV>::BM - 1) / DqCfg<D, DV>::BM) * a.N1;
+  dim3 grid(kv_ctas + dq_ctas, a.B);
+  fabwd_bwd_wide_kernel<D, DV, FP16><<<grid, kMainThreads, bytes, st>>>(mkv.q, mkv.k, mkv.v, mkv.dout, mdq.q, mdq.k,
+                                                                        mdq.v, mdq.dout, a, kv_ctas);
   return cudaGetLastError();
 }
 

@@ -309,7 +309,8 @@ def stage_table(pb, r, peak_tf, peak_hbm):
     out = {"preprocess": hbm("preprocess_kernel", r["ms_pre"], pre_bytes)}
     if r.get("merged"):
         # one grid of dK/dV CTAs (S, dP, dV, dK) and dQ CTAs (S, dP again, dQ)
-        out["backward"] = tensor("fabwd_bwd_kernel", r["ms_main"], 2 * (2 * w.D + 2 * w.Dv) + 2 * (2 * w.D + w.Dv))
+        out["backward"] = tensor("fabwd_bwd_kernel" if w.D <= 128 else "fabwd_bwd_wide_kernel", r["ms_main"],
+                                 2 * (2 * w.D + 2 * w.Dv) + 2 * (2 * w.D + w.Dv))
         if r.get("alone"):
             out["backward"]["launched_alone_ms"] = r["alone"]
     elif r["separate"]:
@@ -380,8 +381,8 @@ def gpu_arm(args, rank, world, local_rank):
     sp = st.cuda_stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    # separate dQ mode with D <= 128: fabwd_run launches the dK/dV and dQ CTAs as one grid
-    merged = resolved == fabwd.FABWD_DQ_SEPARATE and w.D <= 128
+    # separate dQ mode: fabwd_run launches the dK/dV and dQ CTAs as one grid
+    merged = resolved == fabwd.FABWD_DQ_SEPARATE
 
     def step(evs=None):
         if evs:
