@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
         L1 = L1 < 0 ? 0 : (L1 > a.S1 ? a.S1 : L1);
         if (q0 + L1 > a.T1) L1 = a.T1 - q0 < 0 ? 0 : a.T1 - q0;
       }
+      // rows past the sequence's last 128-row block are never read by the backward kernels
+      if (tnd && i >= ((L1 + 127) / 128) * 128) act[u] = false;
       val[u] = act[u] && i < L1;
       o[u] = ((long long)b * a.N1 + n1) * a.S1p + i;
       x[u] = y[u] = make_uint4(0u, 0u, 0u, 0u);
@@ -168,8 +170,8 @@ cudaError_t launch_zero(void* p, long long bytes, cudaStream_t st) {
 cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st) {
   const long long rows = (long long)a.B * a.N1 * a.S1p;
   const long long work = rows * (a.Dv / 8) > a.dq_acc_elems / 4 ? rows * (a.Dv / 8) : a.dq_acc_elems / 4;
-  const int grid = grid_for(work, 256);
   const bool small = rows < (1ll << 31);
+  const int grid = grid_for(work, 256);
   if (a.Dv == 128) {
     if (fp16) small ? preprocess_kernel<true, 128, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<true, 128, false><<<grid, 256, 0, st>>>(a);
     else small ? preprocess_kernel<false, 128, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<false, 128, false><<<grid, 256, 0, st>>>(a);

@@ -165,9 +165,10 @@ uint64_t fabwd_set_wait_limit_ns(uint64_t ns);
 int fabwd_debug_inject_timeout(int on);
 
 /* Host only.  Byte offsets inside the workspace of the fp32 sfmg rows, the fp32 lse·log2(e)
- * rows (both [B][N1][row_stride], row_stride = S1 rounded up to 128; for TND, B counts sequences
- * and rows are sequence-local) and the fp32 dq accumulator (q's layout with D).  Lets callers
- * inspect the intermediate sfmg (the V1 output of [FAG] §5.2).  Errors as fabwd_workspace_size. */
+ * rows (both [B][N1][row_stride], row_stride = S1 rounded up to 128; for TND, B counts sequences,
+ * rows are sequence-local, and rows past a sequence's length rounded up to 128 are left unwritten)
+ * and the fp32 dq accumulator (q's layout with D).  Lets callers inspect the intermediate sfmg
+ * (the V1 output of [FAG] §5.2).  Errors as fabwd_workspace_size. */
 fabwd_status fabwd_workspace_layout(const fabwd_params* p, size_t* off_sfmg, size_t* off_lse2,
                                     size_t* off_dq_accum, int64_t* row_stride);
 

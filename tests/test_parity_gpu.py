@@ -119,6 +119,42 @@ def test_modes_agree():
         tl.assert_close(f"{name} atomic vs separate", outs["atomic"][i], inputs.to_f64(outs["separate"][i]))
 
 
+@pytest.mark.parametrize("case", ["gqa_causal_ragged", "band_bnsd_d64", "tnd_bf16_gqa_dense", "d192_dv128_gqa_fp16_band"])
+def test_one_grid_equals_separate_launches(case):
+    # fabwd_run launches the dK/dV and dQ CTAs of the separate mode as one grid; launched on
+    # their own (fabwd_run_main, then fabwd_run_dq) the same CTA code must give identical bits
+    name, w, lens = next(c for c in SMALL if c[0] == case)
+    pb = inputs.make_problem(w, *(lens or ()))
+    ref = tl.forward_inputs(pb)
+    dev = torch.device("cuda")
+    d = lambda x: x.to(dev)
+    cu_q = cu_kv = None
+    extra = {}
+    if w.layout == "TND":
+        cu_q, cu_kv = d(torch.from_numpy(pb.cu_seqlens_q)), d(torch.from_numpy(pb.cu_seqlens_kv))
+        extra = dict(max_seqlen_q=pb.S1, max_seqlen_kv=pb.S2)
+    ins = [d(t) for t in (pb.q, pb.k, pb.v, pb.dout, ref.attn_out, ref.lse)]
+    outs = []
+    for one_grid in (True, False):
+        dq, dk, dv = (torch.full_like(ins[i], 3.0) for i in (0, 1, 2))
+        p = api.make_params(*ins, dq, dk, dv, cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv, layout=w.layout,
+                            dq_mode="separate", **tl.mask_kwargs(w), **extra)
+        n = F.fabwd_workspace_size(p)
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+        st = torch.cuda.current_stream().cuda_stream
+        F.fabwd_preprocess(p, ws.data_ptr(), ws.numel(), st)
+        if one_grid:
+            F.fabwd_run(p, ws.data_ptr(), ws.numel(), st)
+        else:
+            F.fabwd_run_main(p, ws.data_ptr(), ws.numel(), st)
+            F.fabwd_run_dq(p, ws.data_ptr(), ws.numel(), st)
+        s_, bits = F.fabwd_read_device_status(ws.data_ptr(), ws.numel(), st)
+        assert s_ == F.FABWD_OK, hex(bits)
+        outs.append((dq, dk, dv))
+    for name, a, b in zip(("dq", "dk", "dv"), outs[0], outs[1]):
+        assert torch.equal(a, b), name
+
+
 # ---------------------------------------------------------------------------------------------
 # degenerate and edge cases
 # ---------------------------------------------------------------------------------------------
