@@ -98,7 +98,7 @@ def make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, *, cu_seqlens_
     return p
 
 
-def _check_tensors(q, k, v, dout, attn_out, softmax_lse, cu_q, cu_kv):
+def _check_tensors(q, k, v, dout, attn_out, stats, cu_q, cu_kv):
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("libfabwd runs on CUDA tensors only")
@@ -107,8 +107,11 @@ def _check_tensors(q, k, v, dout, attn_out, softmax_lse, cu_q, cu_kv):
             raise TypeError(f"{name} must have q's dtype {q.dtype} ([FAG] §4.6), got {t.dtype}")
         if t.device != dev:
             raise ValueError(f"{name} is on {t.device}, q on {dev}")
-    if softmax_lse.dtype != torch.float32:
-        raise TypeError("softmax_lse must be float32 ([FAG] §4.6)")
+    for name, t in stats:
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32 ([FAG] §4.6)")
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, q on {dev}")
     for name, t in (("cu_seqlens_q", cu_q), ("cu_seqlens_kv", cu_kv)):
         if t is not None and t.dtype != torch.int32:
             raise TypeError(f"{name} must be int32")
@@ -117,8 +120,8 @@ def _check_tensors(q, k, v, dout, attn_out, softmax_lse, cu_q, cu_kv):
 def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_seqlens_kv=None, seqused_q=None,
                     seqused_kv=None, sinks=None, attn_mask=None, metadata=None, softmax_scale=0.0, mask_mode=0,
                     win_left=-1, win_right=-1, max_seqlen_q=-1, max_seqlen_kv=-1, layout_q="BSND",
-                    layout_kv="BSND", layout_out="BSND", *, dq_mode="auto", check_status=False,
-                    return_workspace=False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+                    layout_kv="BSND", layout_out="BSND", *, softmax_max=None, softmax_sum=None, dq_mode="auto",
+                    check_status=False, return_workspace=False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Gradients (dq, dk, dv) of attention from the saved attn_out and softmax_lse.
 
     Arguments follow [FAG] §4.2.  Differences: seqused_q/kv, sinks and attn_mask are not
@@ -128,18 +131,37 @@ def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_
     max_seqlen_* = -1 the lengths are read from cu_seqlens on the host (a synchronisation).
     dq_mode selects how dQ is formed: 'atomic' (fp32 reduce-adds into a workspace accumulator, then
     a convert pass), 'separate' (a q-stationary pass, bitwise reproducible) or 'auto'.
+    softmax_max / softmax_sum: the forward statistics as a row maximum and a row sum of
+    exp(S − max), in place of softmax_lse (which may then be None): lse = max + ln(sum).  They
+    have softmax_lse's shape, optionally with a trailing axis that repeats each row's value (the
+    (..., 8) layout of the LaserAttentionGrad and FusedFloydAttentionGrad pages).
     check_status=True synchronises and raises if the kernels reported a device-side problem.
     """
     if seqused_q is not None or seqused_kv is not None or sinks is not None or attn_mask is not None:
         raise NotImplementedError("seqused_q/seqused_kv/sinks/attn_mask are not supported")
     if not (layout_q == layout_kv == layout_out):
         raise ValueError("layout_q, layout_kv and layout_out must be the same ([FAG] §4.6)")
-    q, k, v, dout, attn_out, softmax_lse = (t.contiguous() for t in (q, k, v, dout, attn_out, softmax_lse))
+    use_stats = softmax_max is not None or softmax_sum is not None
+    if use_stats and (softmax_max is None or softmax_sum is None):
+        raise ValueError("softmax_max and softmax_sum go together")
+    if not use_stats and softmax_lse is None:
+        raise ValueError("softmax_lse (or softmax_max with softmax_sum) is required")
+    q, k, v, dout, attn_out = (t.contiguous() for t in (q, k, v, dout, attn_out))
+    if use_stats:
+        softmax_max, softmax_sum = softmax_max.contiguous(), softmax_sum.contiguous()
+        if softmax_max.shape != softmax_sum.shape:
+            raise ValueError("softmax_max and softmax_sum must have the same shape")
+        lse_dims = 2 if layout_q == "TND" else 3
+        stat_stride = softmax_max.shape[-1] if softmax_max.dim() == lse_dims + 1 else 1
+        softmax_lse = None
+    else:
+        softmax_lse = softmax_lse.contiguous()
     if cu_seqlens_q is not None:
         cu_seqlens_q = cu_seqlens_q.contiguous()
     if cu_seqlens_kv is not None:
         cu_seqlens_kv = cu_seqlens_kv.contiguous()
-    _check_tensors(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q, cu_seqlens_kv)
+    stats = [("softmax_max", softmax_max), ("softmax_sum", softmax_sum)] if use_stats else [("softmax_lse", softmax_lse)]
+    _check_tensors(q, k, v, dout, attn_out, stats, cu_seqlens_q, cu_seqlens_kv)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     p = make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, cu_seqlens_q=cu_seqlens_q,
                     cu_seqlens_kv=cu_seqlens_kv, softmax_scale=softmax_scale, mask_mode=mask_mode,
@@ -148,7 +170,11 @@ def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_
     nbytes = F.fabwd_workspace_size(p)
     ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
     stream = torch.cuda.current_stream(q.device).cuda_stream
-    F.fabwd_preprocess(p, ws.data_ptr(), ws.numel(), stream)
+    if use_stats:
+        F.fabwd_preprocess_stats(p, softmax_max.data_ptr(), softmax_sum.data_ptr(), stat_stride, ws.data_ptr(),
+                                 ws.numel(), stream)
+    else:
+        F.fabwd_preprocess(p, ws.data_ptr(), ws.numel(), stream)
     F.fabwd_run(p, ws.data_ptr(), ws.numel(), stream)
     if check_status:
         s, bits = F.fabwd_read_device_status(ws.data_ptr(), ws.numel(), stream)

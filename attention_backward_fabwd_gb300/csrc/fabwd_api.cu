@@ -78,7 +78,8 @@ fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
 
   if (check_ptrs) {
     const bool q_nonempty = pl->rowsQ > 0, k_nonempty = pl->rowsK > 0;
-    if (q_nonempty && (!p->q || !p->dout || !p->attn_out || !p->softmax_lse || !p->dq)) return FABWD_ERR_NULLPTR;
+    // attn_out and softmax_lse are read by the preprocess only (which checks softmax_lse itself)
+    if (q_nonempty && (!p->q || !p->dout || !p->attn_out || !p->dq)) return FABWD_ERR_NULLPTR;
     if (k_nonempty && (!p->k || !p->v || !p->dk || !p->dv)) return FABWD_ERR_NULLPTR;
     if (q_nonempty && (!aligned16(p->q) || !aligned16(p->dout) || !aligned16(p->attn_out) || !aligned16(p->dq) ||
                        (reinterpret_cast<uintptr_t>(p->softmax_lse) & 3u)))
@@ -144,6 +145,11 @@ bool main_supported(int D, int Dv) {
 }
 }  // namespace fabwd
 
+namespace {
+fabwd_status preprocess_impl(const fabwd_params* p, const float* smax, const float* ssum, int64_t stat_stride,
+                             void* ws, size_t ws_bytes, void* stream);
+}  // namespace
+
 extern "C" {
 
 fabwd_status fabwd_workspace_size(const fabwd_params* p, size_t* bytes) {
@@ -178,9 +184,31 @@ fabwd_status fabwd_resolve_dq_mode(const fabwd_params* p, int32_t* mode) {
 }
 
 fabwd_status fabwd_preprocess(const fabwd_params* p, void* ws, size_t ws_bytes, void* stream) {
+  return preprocess_impl(p, nullptr, nullptr, 0, ws, ws_bytes, stream);
+}
+
+fabwd_status fabwd_preprocess_stats(const fabwd_params* p, const float* softmax_max, const float* softmax_sum,
+                                    int64_t stat_stride, void* ws, size_t ws_bytes, void* stream) {
+  if (!p) return FABWD_ERR_NULLPTR;
+  fabwd_params q = *p;
+  q.softmax_lse = softmax_max;  // the statistics replace softmax_lse: checked like it
+  const bool rows = q.S1 > 0 && q.B > 0 && q.N1 > 0 && (q.layout != FABWD_TND || q.T1 > 0);
+  if (rows && (!softmax_max || !softmax_sum)) return FABWD_ERR_NULLPTR;
+  if (stat_stride < 1 || stat_stride > 1024 ||
+      (rows && (reinterpret_cast<uintptr_t>(softmax_sum) & 3u)))
+    return FABWD_ERR_INVALID;
+  return preprocess_impl(&q, softmax_max, softmax_sum, stat_stride, ws, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+fabwd_status preprocess_impl(const fabwd_params* p, const float* smax, const float* ssum, int64_t stat_stride,
+                             void* ws, size_t ws_bytes, void* stream) {
   Plan pl;
   fabwd_status s = plan_and_check(p, &pl, true);
   if (s != FABWD_OK) return s;
+  if (pl.rowsQ > 0 && !p->softmax_lse) return FABWD_ERR_NULLPTR;
   if ((s = check_ws(pl, ws, ws_bytes)) != FABWD_OK) return s;
   uint8_t* w = static_cast<uint8_t*>(ws);
   PreArgs a;
@@ -197,6 +225,9 @@ fabwd_status fabwd_preprocess(const fabwd_params* p, void* ws, size_t ws_bytes, 
   a.dout = p->dout;
   a.attn_out = p->attn_out;
   a.lse = p->softmax_lse;
+  a.smax = smax;
+  a.ssum = ssum;
+  a.stat_stride = stat_stride;
   a.cu_q = p->cu_seqlens_q;
   a.cu_kv = p->cu_seqlens_kv;
   a.lse2 = reinterpret_cast<float*>(w + pl.off_lse2);
@@ -207,8 +238,7 @@ fabwd_status fabwd_preprocess(const fabwd_params* p, void* ws, size_t ws_bytes, 
   cudaError_t e = launch_preprocess(a, p->dtype == FABWD_FP16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
 }
-
-}  // extern "C"
+}  // namespace
 
 namespace {
 

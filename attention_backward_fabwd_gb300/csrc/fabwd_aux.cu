@@ -99,7 +99,16 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
         const long long r = row_index(a.layout, b, q0 + i, n1, a.N1, a.S1);
         x[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * DV + part * 8);
         y[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.attn_out) + r * DV + part * 8);
-        if (part == 0) l[u] = a.lse[tnd ? (long long)n1 * a.T1 + q0 + i : ((long long)b * a.N1 + n1) * a.S1 + i];
+        if (part == 0) {
+          const long long li = tnd ? (long long)n1 * a.T1 + q0 + i : ((long long)b * a.N1 + n1) * a.S1 + i;
+          if (a.smax) {
+            // (row maximum, row sum of exp(S - max)) -> lse; no visible key (sum <= 0) -> +inf
+            const float m = a.smax[li * a.stat_stride], sm = a.ssum[li * a.stat_stride];
+            l[u] = sm > 0.f ? m + logf(sm) : INFINITY;
+          } else {
+            l[u] = a.lse[li];
+          }
+        }
       }
     }
 #pragma unroll

@@ -30,6 +30,9 @@ struct PreArgs {
   const void* dout;
   const void* attn_out;
   const float* lse;
+  const float* smax;         // non-null: lse = smax + ln(ssum) per row, read at stride stat_stride
+  const float* ssum;
+  long long stat_stride;
   const int* cu_q;
   const int* cu_kv;
   float* lse2;               // [B][N1][S1p]: lse * log2(e), +inf on padding rows

@@ -103,7 +103,9 @@ typedef struct {
   const void* v;
   const void* dout;
   const void* attn_out;
-  const float* softmax_lse;      /* device, fp32, natural-log lse of the scaled scores */
+  const float* softmax_lse;      /* device, fp32, natural-log lse of the scaled scores (read by
+                                    fabwd_preprocess only; unused by fabwd_preprocess_stats and
+                                    the run entry points) */
   const int32_t* cu_seqlens_q;   /* device, B+1 entries, TND only (NULL otherwise) */
   const int32_t* cu_seqlens_kv;  /* device, B+1 entries, TND only (NULL otherwise) */
   double softmax_scale;          /* 0 -> 1/sqrt(D) ([FAG] §一 scale rule) */
@@ -171,6 +173,19 @@ int fabwd_debug_inject_timeout(int on);
  * (the V1 output of [FAG] §5.2).  Errors as fabwd_workspace_size. */
 fabwd_status fabwd_workspace_layout(const fabwd_params* p, size_t* off_sfmg, size_t* off_lse2,
                                     size_t* off_dq_accum, int64_t* row_stride);
+
+/* fabwd_preprocess for callers that saved the forward's softmax statistics as a per-row maximum
+ * and a per-row sum of exp(S - max) (the (softmaxMax, softmaxSum) pair of the pages
+ * "LaserAttentionGrad" and "aclnnFusedFloydAttentionGrad", their forward-statistics inputs)
+ * instead of softmax_lse: it uses lse = max + ln(sum) per row and is otherwise the same call.
+ * softmax_max and softmax_sum: device fp32 in softmax_lse's row layout ([B][N1][S1], or [N1][T1]
+ * for TND), each row's value stored stat_stride times in a row (1 for a plain layout; those pages'
+ * layout repeats it 8 times), 4-byte aligned; p->softmax_lse is ignored.  A row whose sum is
+ * <= 0 (it saw no key) gets lse = +inf, so its P is 0.  Errors: NULLPTR for a missing statistic
+ * when there are query rows, INVALID for stat_stride outside [1, 1024] or a misaligned pointer,
+ * otherwise as fabwd_preprocess. */
+fabwd_status fabwd_preprocess_stats(const fabwd_params* p, const float* softmax_max, const float* softmax_sum,
+                                    int64_t stat_stride, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Host only.  Stores in *mode the dQ mode that fabwd_run uses for these parameters: the
  * requested one, or the library's choice (FABWD_DQ_ATOMIC or FABWD_DQ_SEPARATE) for

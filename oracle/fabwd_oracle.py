@@ -132,6 +132,29 @@ def forward_head(q, k, v, scale: float, ok) -> Tuple[np.ndarray, np.ndarray]:
     return p @ v, lse
 
 
+def forward_stats_head(q, k, v, scale: float, ok) -> Tuple[np.ndarray, np.ndarray]:
+    """One head's forward statistics in the (softmaxMax, softmaxSum) form that the pages
+    "LaserAttentionGrad" (ascend-transformer-boost, its backward inputs) and
+    "aclnnFusedFloydAttentionGrad" (its softmaxMax/softmaxSum parameters) take in place of an
+    lse: the row maximum m_i of the visible S_ij and the row sum l_i = Σ_{visible j} exp(S_ij − m_i).
+    Rows with no visible key get m = −inf, l = 0."""
+    s = np.where(ok, _scores(q, k, scale), -np.inf)
+    m = s.max(axis=1) if s.shape[1] else np.full(s.shape[0], -np.inf)
+    has = np.isfinite(m)
+    with np.errstate(invalid="ignore"):
+        l = np.where(has, np.exp(s - np.where(has, m, 0.0)[:, None]).sum(axis=1), 0.0)
+    return m, l
+
+
+def lse_from_stats(m, l) -> np.ndarray:
+    """lse = m + ln(l) for a (maximum, sum of exp(S − maximum)) pair, so that exp(S − lse) is the
+    softmax; a row with l <= 0 saw no key and gets lse = +inf (P = 0), as forward_head gives."""
+    m = np.asarray(m, np.float64)
+    l = np.asarray(l, np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), np.inf)
+
+
 def backward_head(q, k, v, dy, y, lse, scale: float, ok):
     """[FAG §一] one head's backward from saved Y and lse: returns (dQ, dK, dV, sfmg)."""
     p = _probs(_scores(q, k, scale), lse, ok)

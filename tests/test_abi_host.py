@@ -128,9 +128,11 @@ def test_null_and_workspace_codes(lib):
     assert F.lib().fabwd_workspace_size(None, ctypes.byref(ctypes.c_size_t())) == F.FABWD_ERR_NULLPTR
     p = base_params()
     assert F.lib().fabwd_workspace_size(ctypes.byref(p), None) == F.FABWD_ERR_NULLPTR
-    for name in ("q", "k", "dout", "softmax_lse", "dq", "dv"):
+    for name in ("q", "k", "dout", "attn_out", "dq", "dv"):
         pp = base_params(**{name: None})
         assert F.call_status("fabwd_run", pp, 0x100000, 1 << 30, None) == F.FABWD_ERR_NULLPTR, name
+    # softmax_lse is read by the preprocess only
+    assert F.call_status("fabwd_preprocess", base_params(softmax_lse=None), 0x100000, 1 << 30, None) == F.FABWD_ERR_NULLPTR
     _, need = ws_size(p)
     assert F.call_status("fabwd_preprocess", p, None, need, None) == F.FABWD_ERR_WORKSPACE
     assert F.call_status("fabwd_run", p, 0x100000, need - 1, None) == F.FABWD_ERR_WORKSPACE
@@ -139,6 +141,23 @@ def test_null_and_workspace_codes(lib):
     assert F.call_status("fabwd_run", misaligned, 0x100000, need, None) == F.FABWD_ERR_INVALID
     v = ctypes.c_uint32(0)
     assert F.lib().fabwd_read_device_status(None, 256, None, ctypes.byref(v)) == F.FABWD_ERR_NULLPTR
+
+
+def test_statistics_preprocess_validation(lib):
+    # every case below is refused on the host, before anything is enqueued
+    p = base_params(softmax_lse=None)   # softmax_lse is not used by this entry point
+    _, need = ws_size(base_params())
+    st = lambda mx, sm, stride, ws=0x100000, n=need, pp=p: F.call_status("fabwd_preprocess_stats", pp, mx, sm,
+                                                                        stride, ws, n, None)
+    assert st(None, 0x20000, 1) == F.FABWD_ERR_NULLPTR
+    assert st(0x20000, None, 1) == F.FABWD_ERR_NULLPTR
+    assert st(0x20000, 0x20000, 0) == F.FABWD_ERR_INVALID
+    assert st(0x20000, 0x20000, 1025) == F.FABWD_ERR_INVALID
+    assert st(0x20000, 0x20002, 8) == F.FABWD_ERR_INVALID          # misaligned sum
+    assert st(0x20002, 0x20000, 8) == F.FABWD_ERR_INVALID          # misaligned max (checked as softmax_lse)
+    assert st(0x20000, 0x20000, 8, n=need - 1) == F.FABWD_ERR_WORKSPACE
+    assert st(0x20000, 0x20000, 8, pp=base_params(N1=3)) == F.FABWD_ERR_INVALID
+    assert F.call_status("fabwd_preprocess_stats", None, 0x20000, 0x20000, 1, 0x100000, need, None) == F.FABWD_ERR_NULLPTR
 
 
 def test_tnd_validation(lib):

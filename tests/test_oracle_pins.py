@@ -419,3 +419,37 @@ def test_planted_gqa_map_is_caught(monkeypatch):
     monkeypatch.setattr(orc, "_kv_head", lambda n1, N1, N2: n1 % N2)
     with pytest.raises(AssertionError):
         test_gqa_equals_repeated_kv()
+
+
+# ---------------------------------------------------------------------------------------------
+# (max, sum) statistics form of the forward (LaserAttentionGrad / FusedFloydAttentionGrad pages)
+# ---------------------------------------------------------------------------------------------
+
+
+def test_stats_give_the_logsumexp_of_the_visible_scores():
+    from scipy.special import logsumexp
+
+    rng = np.random.default_rng(11)
+    S1, S2, D = 9, 13, 5
+    q, k, v = rng.normal(size=(S1, D)), rng.normal(size=(S2, D)), rng.normal(size=(S2, 3))
+    ok = orc.visible(S1, S2, 2, 3, 1)
+    ok[4, :] = False                                  # a row with no visible key
+    m, l = orc.forward_stats_head(q, k, v, 0.37, ok)
+    lse = orc.lse_from_stats(m, l)
+    s = 0.37 * q @ k.T
+    for i in range(S1):
+        want = logsumexp(s[i][ok[i]]) if ok[i].any() else np.inf
+        assert lse[i] == pytest.approx(want, rel=1e-13, abs=1e-13) if np.isfinite(want) else lse[i] == np.inf
+    # and the same lse as the forward itself produces
+    _, lse_fwd = orc.forward_head(q, k, v, 0.37, ok)
+    np.testing.assert_allclose(lse, lse_fwd, rtol=1e-14)
+
+
+def test_stats_adapter_does_not_need_the_true_maximum():
+    # (c, Σ exp(S − c)) for any shift c describes the same softmax: lse must not depend on c
+    rng = np.random.default_rng(12)
+    s = rng.normal(size=(6, 10)) * 3
+    ref = orc.lse_from_stats(s.max(axis=1), np.exp(s - s.max(axis=1, keepdims=True)).sum(axis=1))
+    for c in (0.0, -5.0, 7.5):
+        np.testing.assert_allclose(orc.lse_from_stats(np.full(6, c), np.exp(s - c).sum(axis=1)), ref, rtol=1e-13)
+    assert orc.lse_from_stats(np.array([-np.inf]), np.array([0.0]))[0] == np.inf

@@ -155,6 +155,55 @@ def test_one_grid_equals_separate_launches(case):
         assert torch.equal(a, b), name
 
 
+def _oracle_stats(pb):
+    """(row maximum, row sum) of the fp64 forward per head, in softmax_lse's layout."""
+    w = pb.w
+    q, k, v = (inputs.to_f64(t) for t in (pb.q, pb.k, pb.v))
+    scale = orc.resolve_scale(w.softmax_scale, w.D)
+    G = w.N1 // w.N2
+    if w.layout == "TND":
+        m, l = np.zeros((w.N1, pb.T1)), np.zeros((w.N1, pb.T1))
+        cu_q, cu_k = pb.cu_seqlens_q, pb.cu_seqlens_kv
+        for s_ in range(w.B):
+            rq, rk = slice(int(cu_q[s_]), int(cu_q[s_ + 1])), slice(int(cu_k[s_]), int(cu_k[s_ + 1]))
+            ok = orc.visible(rq.stop - rq.start, rk.stop - rk.start, w.mask_mode, w.win_left, w.win_right)
+            for n1 in range(w.N1):
+                m[n1, rq], l[n1, rq] = orc.forward_stats_head(q[rq, n1], k[rk, n1 // G], v[rk, n1 // G], scale, ok)
+    else:
+        m, l = np.zeros((w.B, w.N1, pb.S1)), np.zeros((w.B, w.N1, pb.S1))
+        ok = orc.visible(pb.S1, pb.S2, w.mask_mode, w.win_left, w.win_right)
+        for b in range(w.B):
+            for n1 in range(w.N1):
+                m[b, n1], l[b, n1] = orc.forward_stats_head(q[b, :, n1], k[b, :, n1 // G], v[b, :, n1 // G], scale, ok)
+    return m.astype(np.float32), l.astype(np.float32)
+
+
+@pytest.mark.parametrize("stride", [1, 8])
+@pytest.mark.parametrize("case", ["gqa_causal_ragged", "tnd_fp16_window"])
+def test_max_sum_statistics_in_place_of_lse(case, stride):
+    # the forward's (row maximum, row sum) pair instead of softmax_lse, optionally with each row's
+    # value repeated `stride` times (the (..., 8) layout of the LaserAttentionGrad and
+    # FusedFloydAttentionGrad pages); rows without a visible key carry (-inf, 0)
+    name, w, lens = next(c for c in SMALL if c[0] == case)
+    pb = inputs.make_problem(w, *(lens or ()))
+    ref = tl.full_reference(pb)
+    m, l = _oracle_stats(pb)
+    if stride > 1:
+        m, l = np.repeat(m[..., None], stride, axis=-1), np.repeat(l[..., None], stride, axis=-1)
+    dev = torch.device("cuda")
+    d = lambda x: x.to(dev)
+    kw = dict(layout_q=w.layout, layout_kv=w.layout, layout_out=w.layout, check_status=True, **tl.mask_kwargs(w))
+    if w.layout == "TND":
+        kw.update(cu_seqlens_q=d(torch.from_numpy(pb.cu_seqlens_q)), cu_seqlens_kv=d(torch.from_numpy(pb.cu_seqlens_kv)),
+                  max_seqlen_q=pb.S1, max_seqlen_kv=pb.S2)
+    ins = [d(t) for t in (pb.q, pb.k, pb.v, pb.dout, ref.attn_out)]
+    dq, dk, dv = api.flash_attn_grad(*ins, None, softmax_max=d(torch.from_numpy(m)), softmax_sum=d(torch.from_numpy(l)),
+                                     **kw)
+    tl.assert_close("dq", dq.cpu(), ref.dq)
+    tl.assert_close("dk", dk.cpu(), ref.dk)
+    tl.assert_close("dv", dv.cpu(), ref.dv)
+
+
 # ---------------------------------------------------------------------------------------------
 # degenerate and edge cases
 # ---------------------------------------------------------------------------------------------
