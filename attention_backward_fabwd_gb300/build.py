@@ -13,7 +13,7 @@ OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libfabwd.so")
 
 SOURCES = ["fabwd_api.cu", "fabwd_aux.cu", "fabwd_main_bf16.cu", "fabwd_main_fp16.cu", "fabwd_static_ws.cu"]
-HEADERS = ["fabwd_ptx.cuh", "fabwd_internal.cuh", "fabwd_main.cuh", "fabwd_dq.cuh", "fabwd_kv.cuh", "fabwd_sep.cuh"]
+HEADERS = ["fabwd_ptx.cuh", "fabwd_internal.cuh", "fabwd_main.cuh", "fabwd_dq.cuh", "fabwd_kv.cuh", "fabwd_sep.cuh", "fabwd_fwd.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -265,6 +265,7 @@ MainArgs main_args(const fabwd_params* p, const Plan& pl, uint8_t* w, int inject
   a.sfmg = reinterpret_cast<const float*>(w + pl.off_sfmg);
   a.dq_acc = pl.separate ? nullptr : reinterpret_cast<float*>(w + pl.off_dqacc);
   a.dq = p->dq;
+  a.lse_out = nullptr;
   a.dk = p->dk;
   a.dv = p->dv;
   a.status = reinterpret_cast<unsigned*>(w + pl.off_status);
@@ -381,6 +382,46 @@ fabwd_status fabwd_run(const fabwd_params* p, void* ws, size_t ws_bytes, void* s
   s = fabwd_run_main(p, ws, ws_bytes, stream);
   if (s != FABWD_OK) return s;
   return fabwd_run_dq(p, ws, ws_bytes, stream);
+}
+
+fabwd_status fabwd_forward(const fabwd_params* p, void* attn_out, float* softmax_lse, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!p) return FABWD_ERR_NULLPTR;
+  fabwd_params f = *p;  // the backward-only fields are not used: fill them so the shared checks pass
+  f.attn_out = attn_out;
+  f.softmax_lse = softmax_lse;
+  f.dout = attn_out;
+  f.dq = attn_out;  // non-null stand-ins: these fields are not read here
+  f.dk = const_cast<void*>(f.k);
+  f.dv = const_cast<void*>(f.v);
+  f.dq_mode = FABWD_DQ_SEPARATE;
+  Plan pl;
+  fabwd_status s = plan_and_check(&f, &pl, true);
+  if (s != FABWD_OK) return s;
+  if (pl.rowsQ > 0 && !softmax_lse) return FABWD_ERR_NULLPTR;
+  if (!ws) return FABWD_ERR_NULLPTR;
+  if (ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255u)) return FABWD_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_zero(ws, 256, st) != cudaSuccess) return FABWD_ERR_CUDA;  // status word
+  if (pl.rowsQ == 0) return FABWD_OK;
+  if (!any_pair(&f, pl)) {  // no key at all: Y = 0, lse = +inf
+    const long long rows = pl.rowsQ * p->N1;
+    return launch_zero(attn_out, rows * p->Dv * 2, st) == cudaSuccess &&
+                   launch_fill_f32(softmax_lse, rows, INFINITY, st) == cudaSuccess
+               ? FABWD_OK
+               : FABWD_ERR_CUDA;
+  }
+  const int inject = g_inject_timeout;
+  g_inject_timeout = 0;
+  MainArgs a = main_args(&f, pl, static_cast<uint8_t*>(ws), inject);
+  a.status = static_cast<unsigned*>(ws);
+  a.dq = attn_out;
+  a.lse_out = softmax_lse;
+  MainMaps maps;
+  if (!make_maps(&f, &maps, 128, p->D > 128 ? 64 : 128)) return FABWD_ERR_CUDA;
+  const cudaError_t e = p->dtype == FABWD_FP16 ? launch_fwd_fp16(a, maps, (int)p->D, (int)p->Dv, st)
+                                               : launch_fwd_bf16(a, maps, (int)p->D, (int)p->Dv, st);
+  return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
 }
 
 fabwd_status fabwd_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32_t* device_status) {

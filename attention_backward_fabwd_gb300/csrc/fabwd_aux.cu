@@ -157,6 +157,11 @@ __global__ void __launch_bounds__(256) zero_kernel(uint4* p, long long n16) {
     p[x] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+__global__ void __launch_bounds__(256) fill_f32_kernel(float* p, long long n, float v) {
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (long long)gridDim.x * blockDim.x)
+    p[x] = v;
+}
+
 int grid_for(long long work_items, int per_block) {
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -173,6 +178,12 @@ cudaError_t launch_zero(void* p, long long bytes, cudaStream_t st) {
   if (bytes <= 0) return cudaSuccess;
   const long long n16 = bytes / 16;
   zero_kernel<<<grid_for(n16, 256), 256, 0, st>>>(static_cast<uint4*>(p), n16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_f32(float* p, long long n, float v, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  fill_f32_kernel<<<grid_for(n, 256), 256, 0, st>>>(p, n, v);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,362 @@
+// q-stationary forward kernel for sm_103a: the attn_out and softmax_lse that the backward takes.
+//
+// What it computes is the forward of the page "CANN ops-transformer FlashAttnGrad 算子详解"
+// (discosf.com/news/4863418), §一: S = scale·QKᵀ, lse_i = ln Σ_j exp(S_ij) over the visible keys,
+// P = exp(S − lse), Y = P·V; a row with no visible key gets Y = 0 and lse = +inf.  One CTA owns
+// 128 query rows of one q-head and loops over the key blocks those rows can see:
+//     S = Q·Kᵀ        tcgen05 (M = 128 queries, N = BN keys, K = D), double-buffered in TMEM
+//     P = exp2(S·scale·log2e − m) with a running row maximum m, written back over S as 16-bit pairs
+//     O_g += P_g·V_g  tcgen05 with the A operand read from TMEM
+// Warpgroup g (warps 4g..4g+3, lane = query row) takes key columns [g·BN/2, (g+1)·BN/2) of every
+// block and keeps its own online softmax (m_g, l_g) and its own accumulator O_g in TMEM; the two
+// halves are combined once at the end: m = max(m_0, m_1), O = Σ_g O_g·2^(m_g − m), l likewise.
+// The running maximum is updated lazily: O_g and l_g are rescaled only when a block's row
+// maximum exceeds the reference by more than 8 (in log2 units), so P stays below 2^8 and most
+// blocks need no pass over O_g.
+// Warp 8 issues TMA loads (Q once; K and V through 3-stage rings, a K stage released after its S
+// product, a V stage after its O product); warp 9 allocates TMEM and issues the MMAs
+//     S(0), S(1), [P(t) written] O(t), S(t+2), ...
+// The compute warps confirm V(t) before they hand over P(t); the MMA thread waits for K itself.
+// TMEM columns: S buffer 0 [0, BN), S buffer 1 [BN, 2BN), O_0 [2BN, 2BN+Dv), O_1 [2BN+Dv, 2BN+2Dv).
+// Bounded waits, abort flag, drain and TMEM release as in the backward kernels.
+#pragma once
+
+#include "fabwd_internal.cuh"
+#include "fabwd_main.cuh"
+#include "fabwd_ptx.cuh"
+#include "../../include/fabwd.h"
+
+namespace fabwd {
+
+template <int D, int DV>
+struct FwdCfg {
+  static constexpr int BM = 128;                 // query rows per CTA (TMEM lanes)
+  static constexpr int BN = D > 128 ? 64 : 128;  // keys per step
+  static constexpr int NK = 3, NV = 3;           // K ring and V ring stages
+  static constexpr int NC = BN / 2;              // key columns per compute thread
+  static constexpr uint32_t kQ = D * BM * 2, kK = D * BN * 2, kV = DV * BN * 2;
+  static constexpr uint32_t oQ = 0, oK = oQ + kQ, oV = oK + NK * kK;
+  static constexpr uint32_t oStat = oV + NV * kV;  // [2 halves][m, l][BM] fp32
+  static constexpr uint32_t oBar = oStat + 2 * 2 * BM * 4;
+  static constexpr uint32_t oMisc = oBar + 20 * 8;
+  static constexpr uint32_t bytes = oMisc + 64;
+  static constexpr uint32_t cS0 = 0, cO = 2 * BN;  // O_g at cO + g·DV
+  static_assert(cO + 2 * DV <= 512, "TMEM budget");
+  static_assert(bytes <= 232448, "shared memory budget");
+  static_assert(NC % 16 == 0 && DV % 64 == 0, "tile shapes");
+};
+
+constexpr int kFwQFull = 0, kFwKFull = 1 /*+3*/, kFwKEmpty = 4 /*+3*/, kFwVFull = 7 /*+3*/, kFwVEmpty = 10 /*+3*/,
+              kFwSFull = 13 /*+2*/, kFwPFull = 15, kFwOFull = 16, kFwNever = 17, kFwDrain = 18, kFwNumBars = 19;
+
+// One CTA of the forward: query block (latest first) bx / N1 of q-head bx % N1, batch (or sequence) by.
+template <int D, int DV, bool FP16>
+__device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                          const MainArgs& a, int bx, int by) {
+  using C = FwdCfg<D, DV>;
+  constexpr int BM = C::BM, BN = C::BN, NK = C::NK, NV = C::NV, NC = C::NC;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = by;
+  SeqRange sq;
+  if (!seq_range(a, b, sq)) {  // bad cu_seqlens: reported, nothing touched
+    if (tid == 0) atomicOr(a.status, FABWD_DEV_BAD_SEQLENS);
+    return;
+  }
+  const int nqb_all = (a.S1 + BM - 1) / BM;
+  const int qb = nqb_all - 1 - bx / a.N1, n1 = bx % a.N1;  // latest query blocks first
+  const int i0 = qb * BM;
+  if (i0 >= sq.L1) return;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) atomicOr(a.status, FABWD_DEV_INTERNAL);
+    return;
+  }
+  const int n2 = n1 / a.G;
+  const int i1 = min(i0 + BM, sq.L1);
+  const long long off = (long long)sq.L2 - sq.L1;
+  long long lo, hi;
+  mask_bounds(a, lo, hi);
+  // keys seen by at least one row of [i0, i1)
+  long long jb_ = (long long)i0 + off + lo, je_ = (long long)(i1 - 1) + off + hi;
+  if (jb_ < 0) jb_ = 0;
+  if (je_ > sq.L2 - 1) je_ = sq.L2 - 1;
+  const int kb_begin = jb_ <= je_ ? (int)(jb_ / BN) : 0;
+  const int T = jb_ <= je_ ? (int)(je_ / BN) + 1 - kb_begin : 0;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBar);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::oMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oMisc + 16);
+  if (tid == 0) {
+    for (int i = 0; i < kFwNumBars; ++i) mbar_init(&bars[i], i == kFwPFull ? 8 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  __syncwarp();
+  if (warp == 9) tmem_alloc(tm_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tm_holder;
+  if (a.inject_timeout) {
+    if (lane == 0) wait_bar(&bars[kFwNever], 0, abort_flag, a);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
+  const int q_row = (tnd ? sq.q0 : 0) + i0;
+  const int kv_rowbase = tnd ? sq.k0 : 0;
+  const int bcoord = tnd ? 0 : b;
+  constexpr bool kBF16 = !FP16;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && T > 0 && !*abort_flag) {
+      mbar_arrive_expect_tx(&bars[kFwQFull], D * BM * 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_4d(smem + C::oQ + c * BM * 128, &tm_q, &bars[kFwQFull], c * 64, bnsd ? q_row : n1,
+                    bnsd ? n1 : q_row, bcoord);
+      for (int t = 0; t < T; ++t) {
+        const int sk = t % NK, sv = t % NV;
+        const int row = kv_rowbase + (kb_begin + t) * BN;
+        if (t >= NK && !wait_bar(&bars[kFwKEmpty + sk], ((t / NK) - 1) & 1, abort_flag, a)) break;
+        mbar_arrive_expect_tx(&bars[kFwKFull + sk], D * BN * 2);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(smem + C::oK + sk * C::kK + c * BN * 128, &tm_k, &bars[kFwKFull + sk], c * 64,
+                      bnsd ? row : n2, bnsd ? n2 : row, bcoord);
+        if (t >= NV && !wait_bar(&bars[kFwVEmpty + sv], ((t / NV) - 1) & 1, abort_flag, a)) break;
+        mbar_arrive_expect_tx(&bars[kFwVFull + sv], DV * BN * 2);
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_4d(smem + C::oV + sv * C::kV + c * BN * 128, &tm_v, &bars[kFwVFull + sv], c * 64,
+                      bnsd ? row : n2, bnsd ? n2 : row, bcoord);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t ID_S = idesc_f16(BM, BN, kBF16, false, false);
+      constexpr uint32_t ID_O = idesc_f16(BM, DV, kBF16, false, true);
+      const uint32_t aQ = smem_u32(smem + C::oQ);
+      auto issue_s = [&](int t) -> bool {  // into S buffer t & 1
+        const int sk = t % NK;
+        const uint32_t aK = smem_u32(smem + C::oK + sk * C::kK);
+        if (!wait_bar(&bars[kFwKFull + sk], (t / NK) & 1, abort_flag, a)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::cS0 + (t & 1) * BN, sdesc_sw128(aQ + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(aK + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+        mma_commit(&bars[kFwSFull + (t & 1)]);
+        mma_commit(&bars[kFwKEmpty + sk]);  // K(t) is read by S(t) only
+        return true;
+      };
+      bool ok = wait_bar(&bars[kFwQFull], 0, abort_flag, a) && issue_s(0) && (T < 2 || issue_s(1));
+      for (int t = 0; ok && t < T; ++t) {
+        // P(t) written by both warpgroups; V(t) landed (confirmed by them before the handoff)
+        if (!(ok = wait_bar(&bars[kFwPFull], t & 1, abort_flag, a))) break;
+        tc_fence_after();
+        const int sv = t % NV;
+        const uint32_t aV = smem_u32(smem + C::oV + sv * C::kV);
+        const uint32_t sb = tmem + C::cS0 + (t & 1) * BN;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+#pragma unroll
+          for (int kk = 0; kk < NC / 16; ++kk)  // keys 16·kk.. of half g: P pairs at +8·kk of its columns
+            mma_ts(tmem + C::cO + g * DV, sb + g * NC + kk * 8,
+                   sdesc_sw128(aV + (g * (NC / 16) + kk) * 2048, BN * 128, 1024), ID_O, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars[kFwOFull]);
+        mma_commit(&bars[kFwVEmpty + sv]);
+        // S(t+2) may overwrite this buffer once O(t) (issued above) has read its P
+        if (t + 2 < T && !(ok = issue_s(t + 2))) break;
+      }
+      if (!ok) {
+        mma_commit(&bars[kFwDrain]);
+        mbar_wait(&bars[kFwDrain], 0, kDrainNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ compute warpgroups 0, 1
+    const int q4 = warp & 3, g = warp >> 2;
+    const int row = q4 * 32 + lane;  // TMEM lane = query row i0 + row
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t oG = tmem + lane_off + C::cO + g * DV;
+    const int ir = i0 + row;
+    // keys visible to this row: j - ir - off in [lo, hi]
+    const long long vlo = (long long)ir + off + lo, vhi = (long long)ir + off + hi;
+    const int j_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
+    const int j_vis_hi = (int)min((long long)sq.L2 - 1, vhi < -1 ? -1ll : (vhi > (1 << 30) ? (long long)(1 << 30) : vhi));
+    const bool i_valid = ir < sq.L1;
+    float m = -INFINITY, l = 0.f;  // running reference maximum (log2 units) and row sum of this half
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int j0 = (kb_begin + t) * BN;
+      const uint32_t sb = tmem + lane_off + C::cS0 + (t & 1) * BN + g * NC;
+      const long long dmin = (long long)j0 - (i0 + BM - 1) - off, dmax = (long long)(j0 + BN - 1) - i0 - off;
+      const bool full = j0 + BN <= sq.L2 && dmin >= lo && dmax <= hi;
+      if (!(ok = wait_bar_warp(&bars[kFwSFull + (t & 1)], (t >> 1) & 1, abort_flag, a))) break;
+      tc_fence_after();
+      uint32_t p[NC];
+      tmem_ld32(sb, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+      if constexpr (NC == 64) tmem_ld32(sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      tmem_wait_ld();
+      reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+      if constexpr (NC == 64) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      const int jc = j0 + g * NC;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        float x = __uint_as_float(p[c]) * a.scale_log2;
+        if (!full && (jc + c < j_vis_lo || jc + c > j_vis_hi)) x = -INFINITY;
+        p[c] = __float_as_uint(x);
+        mx = fmaxf(mx, x);
+      }
+      // New reference maximum when a row's block maximum exceeds it by more than 8.  The decision
+      // is taken per warp (the TMEM loads and stores below are warp-collective); every row of the
+      // warp then moves to its own max(m, mx).
+      if (__any_sync(0xffffffffu, mx > m + 8.f)) {
+        const float mnew = fmaxf(m, mx);
+        const float alpha = mnew == -INFINITY ? 1.f : ex2(m - mnew);  // 0 while nothing was seen
+        l *= alpha;
+        if (t > 0) {
+          // O(t-1) must be complete; O(t) waits for this step's P handoff below
+          if (!(ok = wait_bar_warp(&bars[kFwOFull], (t - 1) & 1, abort_flag, a))) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < DV; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(oG + c, r);
+            tmem_wait_ld();
+            reg_fence(r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(oG + c, r);
+          }
+          tmem_wait_st();
+        }
+        m = mnew;
+      }
+      const float mref = m == -INFINITY ? 0.f : m;  // every x is -inf then: P = 0
+      uint32_t pk[NC / 2];
+#pragma unroll
+      for (int c = 0; c < NC; c += 2) {
+        const float e0 = ex2(__uint_as_float(p[c]) - mref), e1 = ex2(__uint_as_float(p[c + 1]) - mref);
+        l += e0 + e1;
+        pk[c >> 1] = pack2<FP16>(e0, e1);
+      }
+      if constexpr (NC == 64) {
+        tmem_st32(sb, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      } else {
+        tmem_st16(sb, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      }
+      tmem_wait_st();
+      // the MMA thread issues O(t) right after this handoff: its V stage must have landed
+      if (!(ok = wait_bar_warp(&bars[kFwVFull + t % NV], (t / NV) & 1, abort_flag, a))) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kFwPFull]);
+    }
+    // ---- epilogue: combine the halves, Y = O / l in the io dtype, lse = ln-sum-exp (+inf: no key)
+    if (ok && T > 0) ok = wait_bar_warp(&bars[kFwOFull], (T - 1) & 1, abort_flag, a);
+    float* st_m = reinterpret_cast<float*>(smem + C::oStat);
+    float* st_l = st_m + 2 * BM;
+    st_m[g * BM + row] = m;
+    st_l[g * BM + row] = l;
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight compute warps
+    if (ok) {
+      tc_fence_after();
+      const float mo = st_m[(1 - g) * BM + row], lo_ = st_l[(1 - g) * BM + row];
+      const float m0 = g == 0 ? m : mo, m1 = g == 0 ? mo : m, l0 = g == 0 ? l : lo_, l1 = g == 0 ? lo_ : l;
+      const float M = fmaxf(m0, m1);
+      const float c0 = m0 == -INFINITY ? 0.f : ex2(m0 - M), c1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+      const float L = l0 * c0 + l1 * c1;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const long long qrow = row_index(a.layout, b, (long long)(tnd ? sq.q0 : 0) + (i_valid ? ir : 0), n1, a.N1, a.S1);
+      uint16_t* y = static_cast<uint16_t*>(a.dq) + qrow * DV;
+#pragma unroll 1
+      for (int c = 0; c < DV / 64; ++c) {
+        const int col = g * (DV / 2) + c * 32;
+        uint32_t r0[32], r1[32];
+        if (T > 0) {
+          tmem_ld32(tmem + lane_off + C::cO + col, r0);
+          tmem_ld32(tmem + lane_off + C::cO + DV + col, r1);
+          tmem_wait_ld();
+          reg_fence(r0);
+          reg_fence(r1);
+        }
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>((__uint_as_float(r0[e]) * c0 + __uint_as_float(r1[e]) * c1) * inv,
+                                          (__uint_as_float(r0[e + 1]) * c0 + __uint_as_float(r1[e + 1]) * c1) * inv)
+                            : 0u;
+        if (i_valid) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            *reinterpret_cast<uint4*>(y + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+        }
+      }
+      if (g == 0 && i_valid) {
+        const long long li = tnd ? (long long)n1 * a.T1 + sq.q0 + ir : ((long long)b * a.N1 + n1) * a.S1 + ir;
+        a.lse_out[li] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kGraceNs) {
+    }
+  }
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int DV, bool FP16>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    fabwd_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const MainArgs a) {
+  fwd_block<D, DV, FP16>(tm_q, tm_k, tm_v, a, blockIdx.x, blockIdx.y);
+}
+
+template <int D, int DV, bool FP16>
+cudaError_t launch_fwd_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) {
+  using C = FwdCfg<D, DV>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fabwd_fwd_kernel<D, DV, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::bytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B);
+  fabwd_fwd_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, a);
+  return cudaGetLastError();
+}
+
+template <bool FP16>
+cudaError_t launch_fwd_dispatch(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st) {
+  if (D == 64 && Dv == 64) return launch_fwd_t<64, 64, FP16>(a, m, st);
+  if (D == 128 && Dv == 128) return launch_fwd_t<128, 128, FP16>(a, m, st);
+  if (D == 192 && Dv == 128) return launch_fwd_t<192, 128, FP16>(a, m, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fabwd

@@ -61,7 +61,8 @@ struct MainArgs {
   const float* lse2;
   const float* sfmg;
   float* dq_acc;              // fp32 accumulator (atomic dQ mode), else null
-  void* dq;                   // io-dtype dq (written by the q-stationary dQ kernel)
+  void* dq;                   // io-dtype dq (written by the q-stationary dQ kernel); attn_out for the forward
+  float* lse_out;             // forward only: softmax_lse output
   void* dk;
   void* dv;
   unsigned* status;
@@ -77,6 +78,8 @@ cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st);
 cudaError_t launch_convert(const ConvArgs& a, bool fp16, cudaStream_t st);
 // Zero `bytes` (a multiple of 16) at a 16-byte-aligned device address.
 cudaError_t launch_zero(void* p, long long bytes, cudaStream_t st);
+// Set n fp32 values to v.
+cudaError_t launch_fill_f32(float* p, long long n, float v, cudaStream_t st);
 // Return cudaErrorInvalidValue when no kernel is built for (D, Dv).  fused: the kv-stationary
 // kernel also reduces dQ into the fp32 accumulator; otherwise it writes dK, dV only.
 cudaError_t launch_main_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, bool fused,
@@ -99,6 +102,10 @@ cudaError_t launch_bwd_wide_bf16(const MainArgs& a, const MainMaps& mkv, const M
                                  int n_kv_blocks, cudaStream_t st);
 cudaError_t launch_bwd_wide_fp16(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int D, int Dv,
                                  int n_kv_blocks, cudaStream_t st);
+// Forward kernel (attn_out and softmax_lse); a.dq is attn_out, a.lse_out the lse rows, a.status the
+// status word.  Maps: q with 128-row boxes, k and v with 128-row (D <= 128) or 64-row boxes.
+cudaError_t launch_fwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
+cudaError_t launch_fwd_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
 bool main_supported(int D, int Dv);
 
 }  // namespace fabwd

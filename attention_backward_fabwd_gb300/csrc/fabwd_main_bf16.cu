@@ -2,6 +2,7 @@
 #include "fabwd_dq.cuh"
 #include "fabwd_kv.cuh"
 #include "fabwd_sep.cuh"
+#include "fabwd_fwd.cuh"
 #include "fabwd_main.cuh"
 
 namespace fabwd {
@@ -27,5 +28,8 @@ cudaError_t launch_bwd_wide_bf16(const MainArgs& a, const MainMaps& mkv, const M
                                   int n_kv_blocks, cudaStream_t st) {
   if (D == 192 && Dv == 128) return launch_bwd_wide_t<192, 128, false>(a, mkv, mdq, n_kv_blocks, st);
   return cudaErrorInvalidValue;
+}
+cudaError_t launch_fwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st) {
+  return launch_fwd_dispatch<false>(a, m, D, Dv, st);
 }
 }  // namespace fabwd

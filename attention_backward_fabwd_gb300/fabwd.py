@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
                                              ctypes.POINTER(ctypes.c_int64)]
         L.fabwd_resolve_dq_mode.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
         L.fabwd_preprocess.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
+        L.fabwd_forward.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_preprocess_stats.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, sz,
                                              ctypes.c_void_p]
         L.fabwd_run.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
@@ -80,7 +81,7 @@ def lib() -> ctypes.CDLL:
         L.fabwd_status_string.restype = ctypes.c_char_p
         for f in ("fabwd_workspace_size", "fabwd_workspace_layout", "fabwd_preprocess", "fabwd_run",
                   "fabwd_run_main", "fabwd_run_dq", "fabwd_read_device_status", "fabwd_run_static_workspace",
-                  "fabwd_resolve_dq_mode", "fabwd_preprocess_stats"):
+                  "fabwd_resolve_dq_mode", "fabwd_preprocess_stats", "fabwd_forward"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -126,6 +127,13 @@ def fabwd_preprocess(p: fabwd_params, workspace: int, workspace_bytes: int, stre
     s = lib().fabwd_preprocess(ctypes.byref(p), workspace, workspace_bytes, stream)
     if s != FABWD_OK:
         raise FabwdError(s, "fabwd_preprocess")
+
+
+def fabwd_forward(p: fabwd_params, attn_out: int, softmax_lse: int, workspace: int, workspace_bytes: int,
+                  stream: int) -> None:
+    s = lib().fabwd_forward(ctypes.byref(p), attn_out, softmax_lse, workspace, workspace_bytes, stream)
+    if s != FABWD_OK:
+        raise FabwdError(s, "fabwd_forward")
 
 
 def fabwd_preprocess_stats(p: fabwd_params, softmax_max: int, softmax_sum: int, stat_stride: int, workspace: int,

@@ -174,6 +174,19 @@ int fabwd_debug_inject_timeout(int on);
 fabwd_status fabwd_workspace_layout(const fabwd_params* p, size_t* off_sfmg, size_t* off_lse2,
                                     size_t* off_dq_accum, int64_t* row_stride);
 
+/* Forward of [FAG] §一 on the GPU: attn_out Y = P·V and softmax_lse, the two inputs the backward
+ * takes from a forward call, with P = exp(S − lse), S = scale·Q·Kᵀ and lse_i = ln Σ_j exp(S_ij)
+ * over the keys visible to row i (same masks, GQA map, layouts and scale rule as the backward).
+ * p: shapes, q, k, v, cu_seqlens, softmax_scale, mask_mode, win_left, win_right as for the
+ * backward; its dout, attn_out, softmax_lse, dq, dk, dv and dq_mode fields are ignored.
+ * attn_out: device, io dtype, q's layout with Dv (16-byte aligned); softmax_lse: device fp32,
+ * [B][N1][S1] (BSND/BNSD) or [N1][T1] (TND).  Rows with no visible key get Y = 0, lse = +inf.
+ * workspace: caller-owned, >= 256 bytes, 256-byte aligned; only its status word is used
+ * (fabwd_read_device_status reads it after the call).  Enqueued on `stream`, no allocation, no
+ * synchronisation.  Errors as fabwd_run. */
+fabwd_status fabwd_forward(const fabwd_params* p, void* attn_out, float* softmax_lse, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
 /* fabwd_preprocess for callers that saved the forward's softmax statistics as a per-row maximum
  * and a per-row sum of exp(S - max) (the (softmaxMax, softmaxSum) pair of the pages
  * "LaserAttentionGrad" and "aclnnFusedFloydAttentionGrad", their forward-statistics inputs)

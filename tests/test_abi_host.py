@@ -160,6 +160,21 @@ def test_statistics_preprocess_validation(lib):
     assert F.call_status("fabwd_preprocess_stats", None, 0x20000, 0x20000, 1, 0x100000, need, None) == F.FABWD_ERR_NULLPTR
 
 
+def test_forward_validation(lib):
+    # refused on the host before anything is enqueued
+    p = base_params(dout=None, attn_out=None, softmax_lse=None, dq=None, dk=None, dv=None)
+    fw = lambda y, lse, ws, n, pp=p: F.call_status("fabwd_forward", pp, y, lse, ws, n, None)
+    assert fw(None, 0x30000, 0x100000, 256) == F.FABWD_ERR_NULLPTR
+    assert fw(0x30000, None, 0x100000, 256) == F.FABWD_ERR_NULLPTR
+    assert fw(0x30000, 0x30000, None, 256) == F.FABWD_ERR_NULLPTR
+    assert fw(0x30000, 0x30000, 0x100000, 255) == F.FABWD_ERR_WORKSPACE
+    assert fw(0x30000, 0x30000, 0x100010, 256) == F.FABWD_ERR_WORKSPACE
+    assert fw(0x30008, 0x30000, 0x100000, 256) == F.FABWD_ERR_INVALID       # attn_out not 16-byte aligned
+    assert fw(0x30000, 0x30000, 0x100000, 256, pp=base_params(N1=3)) == F.FABWD_ERR_INVALID
+    assert fw(0x30000, 0x30000, 0x100000, 256, pp=base_params(D=96, Dv=96)) == F.FABWD_ERR_UNSUPPORTED
+    assert F.call_status("fabwd_forward", None, 0x30000, 0x30000, 0x100000, 256, None) == F.FABWD_ERR_NULLPTR
+
+
 def test_tnd_validation(lib):
     p = base_params(layout=F.FABWD_TND, cu_seqlens_q=0x20000, cu_seqlens_kv=0x20000, B=3, T1=700, T2=650,
                     S1=300, S2=300)
