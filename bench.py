@@ -52,6 +52,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-forward", action="store_true", help="skip the untimed pass that times fabwd_forward")
     ap.add_argument("--no-breakdown", action="store_true",
                     help="skip the untimed pass that launches the dK/dV and dQ kernels on their own")
     return ap.parse_args()
@@ -87,9 +88,12 @@ def visible_pairs(L1, L2, w):
     return int(np.maximum(jhi - jlo, 0).sum())
 
 
-def flop_counts(pb):
+def flop_counts(pb, per_pair=None):
+    """(convention flops, algorithmic flops) of the step: per_pair flops per (query, key) pair,
+    2·(3D + 2Dv) for the backward by default; S1·S2 pairs per head (halved when causal) or the
+    visible pairs."""
     w = pb.w
-    per_pair = 2 * (3 * w.D + 2 * w.Dv)
+    per_pair = 2 * (3 * w.D + 2 * w.Dv) if per_pair is None else per_pair
     conv = alg = 0
     for L1, L2 in seq_lengths(pb):
         f = per_pair * L1 * L2
@@ -444,6 +448,24 @@ def gpu_arm(args, rank, world, local_rank):
     if s_ != fabwd.FABWD_OK:
         raise RuntimeError(f"device status {bits:#x} after the timed steps")
 
+    # the library's forward on the same inputs (untimed region, reported beside the step)
+    fwd = None
+    if not args.no_forward:
+        y_f, lse_f = torch.empty_like(attn_out), torch.empty_like(lse)
+        ws_f = torch.empty(256, dtype=torch.uint8, device=dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(10)]
+        for i in range(13):
+            flush.fill_(5)
+            if i >= 3:
+                ev[i - 3][0].record(st)
+            fabwd.fabwd_forward(p, y_f.data_ptr(), lse_f.data_ptr(), ws_f.data_ptr(), 256, sp)
+            if i >= 3:
+                ev[i - 3][1].record(st)
+        s_, bits = fabwd.fabwd_read_device_status(ws_f.data_ptr(), 256, sp)
+        if s_ != fabwd.FABWD_OK:
+            raise RuntimeError(f"device status {bits:#x} after the forward")
+        fwd = {"ms": statistics.mean(e_[0].elapsed_time(e_[1]) for e_ in ev)}
+
     # breakdown only (untimed region): the dK/dV and dQ kernels launched on their own
     alone = None
     if merged and not args.no_breakdown:
@@ -517,7 +539,7 @@ def gpu_arm(args, rank, world, local_rank):
         [ms_step, ms_main, statistics.mean(pre), statistics.mean(conv), e2e["ms"] if e2e else 0.0, t_wall], world, dev)
     return dict(pb=pb, w=w, ms_step=ms_step, ms_main=ms_main, ms_pre=ms_pre, ms_conv=ms_conv, e2e=e2e, e2e_ms=e2e_ms,
                 t_wall=t_wall, clocks=clk.summary(), dq_elems=dq.numel(), nbytes=nbytes,
-                separate=resolved == fabwd.FABWD_DQ_SEPARATE, merged=merged, alone=alone)
+                separate=resolved == fabwd.FABWD_DQ_SEPARATE, merged=merged, alone=alone, fwd=fwd)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -687,6 +709,14 @@ def main():
         "clocks": r["clocks"],
         "wall_s_timed_region": r["t_wall"],
     }
+    if r.get("fwd"):
+        ff = flop_counts(pb, per_pair=2 * (w.D + w.Dv))
+        out["forward"] = {"kernel": "fabwd_fwd_kernel", "ms": r["fwd"]["ms"],
+                          "TFLOP/s": ff[0] / (r["fwd"]["ms"] * 1e-3) / 1e12,
+                          "algorithmic_TFLOP/s": ff[1] / (r["fwd"]["ms"] * 1e-3) / 1e12,
+                          "frac_of_peak_algorithmic": ff[1] / (r["fwd"]["ms"] * 1e-3) / 1e12 / peak_tf,
+                          "flops_convention": ff[0], "flops_per_pair": 2 * (w.D + w.Dv),
+                          "note": "untimed side pass (10 launches, L2 flushed), not part of the step"}
     if r["e2e"]:
         out["e2e"] = {"value": job_tflops(conv, world, r["e2e_ms"]), "unit": "TFLOP/s",
                       "h2d_bytes_per_step": r["e2e"]["h2d_bytes_per_step"],
