@@ -183,3 +183,39 @@ def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_
     if return_workspace:
         return dq, dk, dv, (p, ws)
     return dq, dk, dv
+
+
+def flash_attn_forward(q, k, v, cu_seqlens_q=None, cu_seqlens_kv=None, softmax_scale=0.0, mask_mode=0,
+                       win_left=-1, win_right=-1, max_seqlen_q=-1, max_seqlen_kv=-1, layout="BSND",
+                       check_status=False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(attn_out, softmax_lse) of the attention whose gradients flash_attn_grad computes, on the GPU.
+
+    The forward of [FAG] §一 with the same masks, GQA map, layouts and scale rule as the backward:
+    attn_out has q's layout with Dv, softmax_lse is fp32 [B][N1][S1] (BSND/BNSD) or [N1][T1] (TND),
+    natural-log; a row with no visible key gets attn_out = 0 and softmax_lse = +inf.  The pair is
+    what flash_attn_grad takes as attn_out and softmax_lse.
+    """
+    q, k, v = (t.contiguous() for t in (q, k, v))
+    if cu_seqlens_q is not None:
+        cu_seqlens_q = cu_seqlens_q.contiguous()
+    if cu_seqlens_kv is not None:
+        cu_seqlens_kv = cu_seqlens_kv.contiguous()
+    _check_tensors(q, k, v, q, q, [], cu_seqlens_q, cu_seqlens_kv)
+    out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    # make_params reads the shapes from q, k, v; dout/attn_out/lse/dq/dk/dv are unused by the forward.
+    p = make_params(q, k, v, None, out, None, None, None, None, cu_seqlens_q=cu_seqlens_q,
+                    cu_seqlens_kv=cu_seqlens_kv, softmax_scale=softmax_scale, mask_mode=mask_mode,
+                    win_left=win_left, win_right=win_right, max_seqlen_q=max_seqlen_q,
+                    max_seqlen_kv=max_seqlen_kv, layout=layout)
+    if layout == "TND":
+        lse = torch.empty((p.N1, p.T1), dtype=torch.float32, device=q.device)
+    else:
+        lse = torch.empty((p.B, p.N1, p.S1), dtype=torch.float32, device=q.device)
+    ws = torch.empty(256, dtype=torch.uint8, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    F.fabwd_forward(p, out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+    if check_status:
+        s, bits = F.fabwd_read_device_status(ws.data_ptr(), ws.numel(), stream)
+        if s != F.FABWD_OK:
+            raise F.FabwdError(s, f"device status 0x{bits:x}")
+    return out, lse

@@ -16,7 +16,7 @@
  *   1. fabwd_workspace_size(&p, &bytes)     host only, no CUDA call
  *   2. caller allocates `bytes` of device memory (the workspace) and the outputs dq, dk, dv
  *   3. fabwd_preprocess(&p, ws, bytes, stream)   sfmg + padded lse + dq accumulator zeroing
- *   4. fabwd_run(&p, ws, bytes, stream)          main backward kernel + dq convert kernel
+ *   4. fabwd_run(&p, ws, bytes, stream)          the backward kernel(s): dq, dk, dv
  * Steps 3 and 4 must see the same params and workspace and run on the same stream, in order.
  *
  * Ownership: the caller owns every buffer.  The library allocates nothing, never synchronises
@@ -132,11 +132,13 @@ fabwd_status fabwd_workspace_size(const fabwd_params* p, size_t* bytes);
 fabwd_status fabwd_preprocess(const fabwd_params* p, void* workspace, size_t workspace_bytes,
                               void* stream);
 
-/* Enqueue on `stream` the kv-stationary backward kernel (dK, dV written to dk/dv; in atomic
- * mode also the dQ partial sums added into the workspace accumulator) and the dQ stage (atomic
- * mode: the convert kernel, dq = cast(scale · accumulator); separate mode: the q-stationary dQ
- * kernel).  Must follow fabwd_preprocess with the same p and workspace on the same stream.  Errors: as fabwd_preprocess.  A TIMEOUT or bad-seqlens condition found on the
- * device shows up in fabwd_read_device_status, not here. */
+/* Enqueue on `stream` the backward proper.  Separate dq mode (the default): ONE grid holding
+ * both the kv-stationary CTAs (dK, dV written to dk/dv) and the q-stationary CTAs (dQ written to
+ * dq), no atomics, bitwise reproducible.  Atomic dq mode: the kv-stationary kernel (dK, dV, and
+ * the dQ partial sums reduce-added into the workspace accumulator) then the convert kernel,
+ * dq = cast(scale · accumulator).  Must follow fabwd_preprocess (or fabwd_preprocess_stats) with
+ * the same p and workspace on the same stream.  Errors: as fabwd_preprocess.  A TIMEOUT or
+ * bad-seqlens condition found on the device shows up in fabwd_read_device_status, not here. */
 fabwd_status fabwd_run(const fabwd_params* p, void* workspace, size_t workspace_bytes,
                        void* stream);
 
@@ -144,7 +146,8 @@ fabwd_status fabwd_run(const fabwd_params* p, void* workspace, size_t workspace_
  * fabwd_run_main enqueues the kv-stationary kernel (dk, dv; atomic mode: dQ partials into the
  * workspace accumulator); fabwd_run_dq enqueues the dQ stage (atomic mode: the convert kernel;
  * separate mode: the q-stationary dQ kernel, which needs only the preprocess outputs and may run
- * before, after or beside fabwd_run_main).  fabwd_run == fabwd_run_main then fabwd_run_dq.
+ * before, after or beside fabwd_run_main).  The results equal fabwd_run's bit for bit; in
+ * separate mode fabwd_run launches the two as one grid instead.
  * Errors: as fabwd_run. */
 fabwd_status fabwd_run_main(const fabwd_params* p, void* workspace, size_t workspace_bytes, void* stream);
 fabwd_status fabwd_run_dq(const fabwd_params* p, void* workspace, size_t workspace_bytes, void* stream);

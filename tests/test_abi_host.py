@@ -233,6 +233,8 @@ def test_api_rejects_unsupported_inputs():
         api.flash_attn_grad(t, t, t, t, t, torch.zeros(1, 1, 4), layout_kv="TND")
     with pytest.raises(ValueError):   # CPU tensors: the library runs on CUDA only, no fallback
         api.flash_attn_grad(t, t, t, t, t, torch.zeros(1, 1, 4))
+    with pytest.raises(ValueError):   # the forward too
+        api.flash_attn_forward(t, t, t)
 
 
 def test_lib_missing_fails_loudly(monkeypatch, tmp_path):

@@ -97,3 +97,20 @@ def test_forward_without_keys():
     pb = inputs.make_problem(w)
     y, lse = gpu_forward(pb)
     assert (y.float() == 0).all() and torch.isinf(lse).all() and (lse > 0).all()
+
+
+@pytest.mark.parametrize("case", ["gqa_causal_ragged", "tnd_fp16_window"])
+def test_api_forward_equals_c_forward(case):
+    # api.flash_attn_forward is argument marshalling over fabwd_forward: bit-identical results
+    name, w, lens = next(c for c in SMALL if c[0] == case)
+    pb = inputs.make_problem(w, *(lens or ()))
+    y0, lse0 = gpu_forward(pb)
+    dev = torch.device("cuda")
+    d = lambda x: x.to(dev)
+    kw = dict(layout=w.layout, check_status=True, **tl.mask_kwargs(w))
+    if w.layout == "TND":
+        kw.update(cu_seqlens_q=d(torch.from_numpy(pb.cu_seqlens_q)), cu_seqlens_kv=d(torch.from_numpy(pb.cu_seqlens_kv)),
+                  max_seqlen_q=pb.S1, max_seqlen_kv=pb.S2)
+    y, lse = api.flash_attn_forward(d(pb.q), d(pb.k), d(pb.v), **kw)
+    assert torch.equal(y.cpu(), y0)
+    assert torch.equal(lse.cpu(), lse0)
