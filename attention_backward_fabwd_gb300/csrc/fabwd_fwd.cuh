@@ -20,6 +20,7 @@
 // TMEM columns: S buffer 0 [0, BN), S buffer 1 [BN, 2BN), O_0 [2BN, 2BN+Dv), O_1 [2BN+Dv, 2BN+2Dv).
 // Bounded waits, abort flag, drain and TMEM release as in the backward kernels.
 #pragma once
+#include <type_traits>
 
 #include "fabwd_internal.cuh"
 #include "fabwd_main.cuh"
@@ -214,18 +215,71 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
       reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[0]));
       if constexpr (NC == 64) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[32]));
       const int jc = j0 + g * NC;
-      float mx = -INFINITY;
+      // The scores stay as loaded (natural units, unscaled).  P = 2^(s·scale_log2 − ref) is one
+      // packed fp32x2 FMA per key pair and two ex2; the row sum runs on packed adds over two
+      // accumulator pairs.  P goes out in the io dtype, two keys per 32-bit column, over this
+      // half's S columns in 16-column pieces as they are ready.
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+      uint32_t pk[NC / 2];
+      float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      auto exp_pair = [&](int c, float2 nref2) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(p[c]), __uint_as_float(p[c + 1])), sc2, nref2);
+        const float e0 = ex2(x.x), e1 = ex2(x.y);
+        ls2[(c >> 1) & 1] = __fadd2_rn(ls2[(c >> 1) & 1], make_float2(e0, e1));
+        pk[c >> 1] = pack2<FP16>(e0, e1);
+        if ((c & 31) == 30) tmem_st16(sb + (c >> 5) * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[(c >> 5) * 16]));
+      };
+      auto exps = [&](float mref) {
+        ls2[0] = ls2[1] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        float x = __uint_as_float(p[c]) * a.scale_log2;
-        if (!full && (jc + c < j_vis_lo || jc + c > j_vis_hi)) x = -INFINITY;
-        p[c] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
+        for (int c = 0; c < NC; c += 2) exp_pair(c, make_float2(-mref, -mref));
+      };
+      // One pass: hide the keys a row does not see (skipped on tiles every row sees whole,
+      // `full`, the same for the whole CTA), reduce the row (three-input max over 4 chains; min
+      // when the scale is negative, so that the scaled maximum is scale times it) and, after the
+      // first tile, form P against the reference maximum of the earlier tiles in the same loop
+      // (OPT), so the exponentials need not wait for this tile's maximum.
+      const bool neg = a.scale_log2 < 0.f;
+      const float hide = neg ? INFINITY : -INFINITY;  // scaled, it is -inf either way
+      float red[4] = {hide, hide, hide, hide};
+      const float mref_prev = m == -INFINITY ? 0.f : m;
+      auto pass = [&](auto full_c, auto opt_c, auto neg_c) {
+        constexpr bool kFull = decltype(full_c)::value, kOpt = decltype(opt_c)::value;
+        constexpr bool kNeg = decltype(neg_c)::value;
+#pragma unroll
+        for (int c = 0; c < NC; c += 2) {
+          if constexpr (!kFull) {
+            if (jc + c < j_vis_lo || jc + c > j_vis_hi) p[c] = __float_as_uint(hide);
+            if (jc + c + 1 < j_vis_lo || jc + c + 1 > j_vis_hi) p[c + 1] = __float_as_uint(hide);
+          }
+          const float r0 = __uint_as_float(p[c]), r1 = __uint_as_float(p[c + 1]);
+          if constexpr (kNeg) {
+            red[(c >> 1) & 3] = fmin3(red[(c >> 1) & 3], r0, r1);
+          } else {
+            red[(c >> 1) & 3] = fmax3(red[(c >> 1) & 3], r0, r1);
+          }
+          if constexpr (kOpt) exp_pair(c, make_float2(-mref_prev, -mref_prev));
+        }
+      };
+      using kT = std::true_type;
+      using kF = std::false_type;
+      const bool opt = t > 0;  // at t = 0 no row has a reference yet
+      auto pass_sign = [&](auto full_c, auto opt_c) {
+        if (neg) pass(full_c, opt_c, kT{}); else pass(full_c, opt_c, kF{});
+      };
+      if (full) {
+        if (opt) pass_sign(kT{}, kT{}); else pass_sign(kT{}, kF{});
+      } else {
+        if (opt) pass_sign(kF{}, kT{}); else pass_sign(kF{}, kF{});
       }
-      // New reference maximum when a row's block maximum exceeds it by more than 8.  The decision
-      // is taken per warp (the TMEM loads and stores below are warp-collective); every row of the
-      // warp then moves to its own max(m, mx).
-      if (__any_sync(0xffffffffu, mx > m + 8.f)) {
+      const float mx = (neg ? fmin3(red[0], red[1], fminf(red[2], red[3]))
+                            : fmax3(red[0], red[1], fmaxf(red[2], red[3]))) * a.scale_log2;
+      // New reference maximum when a row's block maximum exceeds it by more than 8 (P <= 2^8 in
+      // the io dtype otherwise).  The decision is taken per warp (the TMEM loads and stores below
+      // are warp-collective); every row of the warp then moves to its own max(m, mx), and P is
+      // formed again from the kept scores.
+      const bool grow = __any_sync(0xffffffffu, mx > m + 8.f);
+      if (grow) {
         const float mnew = fmaxf(m, mx);
         const float alpha = mnew == -INFINITY ? 1.f : ex2(m - mnew);  // 0 while nothing was seen
         l *= alpha;
@@ -243,23 +297,14 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
             tmem_st32(oG + c, r);
           }
-          tmem_wait_st();
         }
         m = mnew;
       }
-      const float mref = m == -INFINITY ? 0.f : m;  // every x is -inf then: P = 0
-      uint32_t pk[NC / 2];
-#pragma unroll
-      for (int c = 0; c < NC; c += 2) {
-        const float e0 = ex2(__uint_as_float(p[c]) - mref), e1 = ex2(__uint_as_float(p[c + 1]) - mref);
-        l += e0 + e1;
-        pk[c >> 1] = pack2<FP16>(e0, e1);
+      if (grow || !opt) {
+        tmem_wait_st();  // the first P stores of this tile land before these overwrite them
+        exps(m == -INFINITY ? 0.f : m);  // every x is -inf when m is: P = 0
       }
-      if constexpr (NC == 64) {
-        tmem_st32(sb, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      } else {
-        tmem_st16(sb, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-      }
+      l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
       tmem_wait_st();
       // the MMA thread issues O(t) right after this handoff: its V stage must have landed
       if (!(ok = wait_bar_warp(&bars[kFwVFull + t % NV], (t / NV) & 1, abort_flag, a))) break;

@@ -238,6 +238,20 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// min(a, b, c) in one instruction (three-input min.f32, sm_100 and later).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float y;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
 template <bool FP16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (FP16) {

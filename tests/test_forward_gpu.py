@@ -5,6 +5,8 @@ attn_out within the output tolerance of the backward's outputs (relative L2 <= 1
 <= 2e-2 · max|ref|); lse within 1e-4 + 1e-5·|lse| wherever it is finite, +inf exactly where the
 row sees no key.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -114,3 +116,36 @@ def test_api_forward_equals_c_forward(case):
     y, lse = api.flash_attn_forward(d(pb.q), d(pb.k), d(pb.v), **kw)
     assert torch.equal(y.cpu(), y0)
     assert torch.equal(lse.cpu(), lse0)
+
+
+@pytest.mark.parametrize("case", ["dense_s1_lt_s2", "causal_b2_s384", "fp16_dense_d64", "band_wide"])
+def test_forward_growing_maximum(case):
+    # Keys scaled up along the sequence (x1 at the first key to x6 at the last), so a row's
+    # maximum score keeps rising from key block to key block by more than 8 in log2 units: the
+    # running reference moves after the first tile, O and the row sum are rescaled and P is formed
+    # again from the kept scores.
+    name, w, lens = next(c for c in SMALL if c[0] == case)
+    pb = inputs.make_problem(w, *(lens or ()))
+    k = pb.k.double()
+    seq_axis = 2 if w.layout == "BNSD" else 1
+    ramp = 1.0 + 5.0 * torch.arange(k.shape[seq_axis], dtype=torch.float64) / max(k.shape[seq_axis] - 1, 1)
+    shape = [1] * k.dim()
+    shape[seq_axis] = -1
+    pb.k = (k * ramp.view(shape)).to(pb.k.dtype).contiguous()
+    y_ref, lse_ref = orc.forward(*(inputs.to_f64(t) for t in (pb.q, pb.k, pb.v)), **tl.oracle_kwargs(pb))
+    y, lse = gpu_forward(pb)
+    tl.assert_close("attn_out", y, y_ref)
+    check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("case", ["causal_b2_s384", "band_bnsd_d64", "tnd_fp16_window", "d192_dv128_causal"])
+def test_forward_negative_scale(case):
+    # a negative softmax_scale: the row maximum of scale·S is scale times the row minimum of S,
+    # hidden keys included in neither
+    name, w, lens = next(c for c in SMALL if c[0] == case)
+    w = inputs.sized(w, softmax_scale=-0.7 / math.sqrt(w.D))
+    pb = inputs.make_problem(w, *(lens or ()))
+    y_ref, lse_ref = orc.forward(*(inputs.to_f64(t) for t in (pb.q, pb.k, pb.v)), **tl.oracle_kwargs(pb))
+    y, lse = gpu_forward(pb)
+    tl.assert_close("attn_out", y, y_ref)
+    check_lse(lse, lse_ref)
