@@ -220,6 +220,8 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
     const float* sfmg_row = a.sfmg + ((long long)b * a.N1 + n1) * a.S1p;
     const float lse2 = lse2_row[ir];  // +inf beyond the sequence: P = 0 there
     const float sf = sfmg_row[ir];
+    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nl2 = make_float2(-lse2, -lse2);
+    const float2 nsf2 = make_float2(-sf, -sf);
     // keys visible to this row: j - ir - off in [lo, hi]
     const long long vlo = (long long)ir + off + lo, vhi = (long long)ir + off + hi;
     const int j_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
@@ -238,8 +240,13 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
       tmem_wait_ld();
       reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[0]));
       if constexpr (NC == 64) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      // P = 2^(s·scale_log2 − lse2): one packed fp32x2 FMA per key pair (lse2 is this row's)
 #pragma unroll
-      for (int c = 0; c < NC; ++c) p[c] = __float_as_uint(ex2(fmaf(__uint_as_float(p[c]), a.scale_log2, -lse2)));
+      for (int c = 0; c < NC; c += 2) {
+        const float2 y = __ffma2_rn(make_float2(__uint_as_float(p[c]), __uint_as_float(p[c + 1])), sc2, nl2);
+        p[c] = __float_as_uint(ex2(y.x));
+        p[c + 1] = __float_as_uint(ex2(y.y));
+      }
       if (!full) {
         const int jc = j0 + g * NC;
 #pragma unroll
@@ -258,9 +265,11 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
         reg_fence(r);
         uint32_t ds[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          ds[c >> 1] = pack2<FP16>(__uint_as_float(p[hh * 32 + c]) * (__uint_as_float(r[c]) - sf),
-                                   __uint_as_float(p[hh * 32 + c + 1]) * (__uint_as_float(r[c + 1]) - sf));
+        for (int c = 0; c < 32; c += 2) {  // dS = P ⊙ (dP − sfmg), packed
+          const float2 d = __fmul2_rn(make_float2(__uint_as_float(p[hh * 32 + c]), __uint_as_float(p[hh * 32 + c + 1])),
+                                      __fadd2_rn(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), nsf2));
+          ds[c >> 1] = pack2<FP16>(d.x, d.y);
+        }
         tmem_st16(sb + hh * 16, ds);  // dS over this warpgroup's own (already read) S columns
       }
       tmem_wait_st();

@@ -249,14 +249,25 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
       tmem_wait_ld();
       reg_fence(p0);
       reg_fence(p1);
+      // P = 2^(s·scale_log2 − lse2) as 2^−(lse2 − s·scale_log2): one packed fp32x2 FMA per
+      // query pair against the lse vector as stored; the sign goes with the exponential's operand.
+      // RN is sign-symmetric, so the value is the one the unpacked form gives, bit for bit.
+      const float2 nsc2 = make_float2(-a.scale_log2, -a.scale_log2);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 l0 = sL4[c4], l1 = sL4[c4 + 8];
         const float la[4] = {l0.x, l0.y, l0.z, l0.w}, lb[4] = {l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          p0[4 * c4 + e] = __float_as_uint(ex2(fmaf(__uint_as_float(p0[4 * c4 + e]), a.scale_log2, -la[e])));
-          p1[4 * c4 + e] = __float_as_uint(ex2(fmaf(__uint_as_float(p1[4 * c4 + e]), a.scale_log2, -lb[e])));
+        for (int e = 0; e < 4; e += 2) {
+          const int c = 4 * c4 + e;
+          const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(p0[c]), __uint_as_float(p0[c + 1])), nsc2,
+                                       make_float2(la[e], la[e + 1]));
+          const float2 y1 = __ffma2_rn(make_float2(__uint_as_float(p1[c]), __uint_as_float(p1[c + 1])), nsc2,
+                                       make_float2(lb[e], lb[e + 1]));
+          p0[c] = __float_as_uint(ex2(-y0.x));
+          p0[c + 1] = __float_as_uint(ex2(-y0.y));
+          p1[c] = __float_as_uint(ex2(-y1.x));
+          p1[c + 1] = __float_as_uint(ex2(-y1.y));
         }
       }
       if (!full) {
@@ -294,6 +305,10 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
         tmem_wait_ld();
         reg_fence(r0);
         reg_fence(r1);
+        // −dS = P ⊙ (sfmg − dP), packed: (sfmg − dP) as one fp32x2 FMA with −1 (exactly the
+        // negated difference), then a packed multiply.  dK accumulates −dS·Q and its epilogue
+        // scales by −scale.
+        const float2 m1 = make_float2(-1.f, -1.f);
         uint32_t dk[32];
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
@@ -302,13 +317,17 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const int c = 4 * c4 + e;
-            dk[c >> 1] = pack2<FP16>(__uint_as_float(p0[c]) * (__uint_as_float(r0[c]) - fa[e]),
-                                     __uint_as_float(p0[c + 1]) * (__uint_as_float(r0[c + 1]) - fa[e + 1]));
-            dk[16 + (c >> 1)] = pack2<FP16>(__uint_as_float(p1[c]) * (__uint_as_float(r1[c]) - fb[e]),
-                                            __uint_as_float(p1[c + 1]) * (__uint_as_float(r1[c + 1]) - fb[e + 1]));
+            const float2 n0 = __fmul2_rn(make_float2(__uint_as_float(p0[c]), __uint_as_float(p0[c + 1])),
+                                         __ffma2_rn(make_float2(__uint_as_float(r0[c]), __uint_as_float(r0[c + 1])), m1,
+                                                    make_float2(fa[e], fa[e + 1])));
+            const float2 n1 = __fmul2_rn(make_float2(__uint_as_float(p1[c]), __uint_as_float(p1[c + 1])),
+                                         __ffma2_rn(make_float2(__uint_as_float(r1[c]), __uint_as_float(r1[c + 1])), m1,
+                                                    make_float2(fb[e], fb[e + 1])));
+            dk[c >> 1] = pack2<FP16>(n0.x, n0.y);
+            dk[16 + (c >> 1)] = pack2<FP16>(n1.x, n1.y);
           }
         }
-        tmem_st32(sP, dk);  // dSᵀ over this warpgroup's own (already read) dPᵀ columns
+        tmem_st32(sP, dk);  // −dSᵀ over this warpgroup's own (already read) dPᵀ columns
         tmem_wait_st();
       }
       tc_fence_before();
@@ -335,7 +354,7 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
         uint32_t o[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
-          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * a.scale, __uint_as_float(r[e + 1]) * a.scale) : 0u;
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * -a.scale, __uint_as_float(r[e + 1]) * -a.scale) : 0u;
         if (j_valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
