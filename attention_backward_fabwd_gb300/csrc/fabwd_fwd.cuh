@@ -12,7 +12,10 @@
 // halves are combined once at the end: m = max(m_0, m_1), O = Σ_g O_g·2^(m_g − m), l likewise.
 // The running maximum is updated lazily: O_g and l_g are rescaled only when a block's row
 // maximum exceeds the reference by more than 8 (in log2 units), so P stays below 2^8 and most
-// blocks need no pass over O_g.
+// blocks need no pass over O_g.  After the first block, P is formed against the current
+// reference in the same pass that finds the block's row maximum (packed fp32x2 FMA and adds),
+// and formed again only when the reference moves.  The MMA warp shares its scheduler with two
+// compute warps, so fewer compute instructions leave it more issue slots.
 // Warp 8 issues TMA loads (Q once; K and V through 3-stage rings, a K stage released after its S
 // product, a V stage after its O product); warp 9 allocates TMEM and issues the MMAs
 //     S(0), S(1), [P(t) written] O(t), S(t+2), ...

@@ -7,8 +7,11 @@
 //     Sᵀ  = K·Qᵀ     tcgen05 M = 128 keys, N = 128 queries (a full-rate shape), TMEM slot S
 //     dPᵀ = V·dOᵀ    same shape, TMEM slot dP
 //     Pᵀ  = exp2(Sᵀ·scale·log2e − lse·log2e) -> 16-bit pairs over the warpgroup's own Sᵀ columns
-//     dSᵀ = Pᵀ ⊙ (dPᵀ − sfmg)               -> 16-bit pairs over its own dPᵀ columns
-//     dV += Pᵀ·dO, dK += dSᵀ·Q               tcgen05 with the A operand read from TMEM
+//     −dSᵀ = Pᵀ ⊙ (sfmg − dPᵀ)              -> 16-bit pairs over its own dPᵀ columns
+//     dV += Pᵀ·dO, dK −= (−dSᵀ)·Q            tcgen05 with the A operand read from TMEM; the
+//                                           epilogue writes −scale times the accumulator
+// The elementwise steps use packed fp32x2 FMA and multiply; the signs are chosen so that no
+// per-element negation of the lse and sfmg vectors is needed.
 // Warpgroup g (warps 4g..4g+3) handles query columns [64g, 64g+64) of every step.  Keeping dSᵀ in
 // the dPᵀ columns frees the Sᵀ columns as soon as dV has read Pᵀ, so the MMA warp issues
 //     Sᵀ(t), dPᵀ(t), dV(t), Sᵀ(t+1), dK(t), dPᵀ(t+1), dV(t+1), ...

@@ -1,6 +1,6 @@
-// Allocation-free variant of the backward path: the same preprocess, main and convert kernels as
-// fabwd_preprocess + fabwd_run, with their scratch (workspace) in a fixed-size array that this
-// library owns in device memory instead of a caller-provided buffer.
+// Allocation-free variant of the backward path: the same kernels as fabwd_preprocess +
+// fabwd_run, with their scratch (workspace) in a fixed-size array that this library owns in
+// device memory instead of a caller-provided buffer.
 //
 // Why it exists: some callers cannot call cudaMalloc at the point where they run the backward.
 // Examples are code running under a host framework that owns every byte of device memory
