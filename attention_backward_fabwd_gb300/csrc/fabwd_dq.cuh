@@ -156,22 +156,23 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
     if (lane == 0 && T > 0) {
       constexpr uint32_t ID_S = idesc_f16(BM, BN, kBF16, false, false);
       constexpr uint32_t ID_DQ = idesc_f16(BM, D, kBF16, false, true);
-      const uint32_t aQ = smem_u32(smem + C::oQ), adO = smem_u32(smem + C::odO);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::oQ), 16, 1024);
+      const uint64_t ddO0 = sdesc_sw128(smem_u32(smem + C::odO), 16, 1024);
       auto issue_s = [&](int t) {  // K(t) landed (see above)
-        const uint32_t aK = smem_u32(smem + C::oK + (t % NK) * C::kK);
+        const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::oK + (t % NK) * C::kK), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::cS0 + (t & 1) * BN, sdesc_sw128(aQ + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(aK + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+          mma_ss(tmem + C::cS0 + (t & 1) * BN, sdesc_at(dQ0, (kk >> 2) * BM * 128 + (kk & 3) * 32),
+                 sdesc_at(dK0, (kk >> 2) * BN * 128 + (kk & 3) * 32), ID_S, kk > 0);
         mma_commit(&bars[kDqSFull + (t & 1)]);
       };
       auto issue_dp = [&](int t) {  // V(t) landed (see above)
         const int sv = t % NV;
-        const uint32_t aV = smem_u32(smem + C::oV + sv * C::kV);
+        const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::oV + sv * C::kV), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
-          mma_ss(tmem + C::cP, sdesc_sw128(adO + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(aV + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+          mma_ss(tmem + C::cP, sdesc_at(ddO0, (kk >> 2) * BM * 128 + (kk & 3) * 32),
+                 sdesc_at(dV0, (kk >> 2) * BN * 128 + (kk & 3) * 32), ID_S, kk > 0);
         mma_commit(&bars[kDqDpFull]);
         mma_commit(&bars[kDqVEmpty + sv]);
       };
@@ -189,12 +190,12 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
         if (!(ok = wait_bar(&bars[kDqDsFull], t & 1, abort_flag, a))) break;
         tc_fence_after();
         if (t + 1 < T) issue_dp(t + 1);
-        const uint32_t aK = smem_u32(smem + C::oK + (t % NK) * C::kK);
+        const uint64_t dKt = sdesc_sw128(smem_u32(smem + C::oK + (t % NK) * C::kK), BN * 128, 1024);
         const uint32_t sb = tmem + C::cS0 + (t & 1) * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)  // dS of warpgroup kk/(NC/16) sits in its own S columns
           mma_ts(tmem + C::cDQ, sb + (kk / (NC / 16)) * NC + (kk % (NC / 16)) * 8,
-                 sdesc_sw128(aK + kk * 2048, BN * 128, 1024), ID_DQ, (t > 0 || kk > 0) ? 1u : 0u);
+                 sdesc_at(dKt, kk * 2048), ID_DQ, (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kDqKEmpty + (t % NK)]);
         if (t + 2 < T) {  // into the S buffer whose dS the dQ product above has read
           if (!(ok = wait_bar(&bars[kDqKFull + (t + 2) % NK], ((t + 2) / NK) & 1, abort_flag, a))) break;

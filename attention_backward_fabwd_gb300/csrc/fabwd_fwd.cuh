@@ -150,16 +150,16 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
     if (lane == 0 && T > 0) {
       constexpr uint32_t ID_S = idesc_f16(BM, BN, kBF16, false, false);
       constexpr uint32_t ID_O = idesc_f16(BM, DV, kBF16, false, true);
-      const uint32_t aQ = smem_u32(smem + C::oQ);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::oQ), 16, 1024);
       auto issue_s = [&](int t) -> bool {  // into S buffer t & 1
         const int sk = t % NK;
-        const uint32_t aK = smem_u32(smem + C::oK + sk * C::kK);
+        const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::oK + sk * C::kK), 16, 1024);
         if (!wait_bar(&bars[kFwKFull + sk], (t / NK) & 1, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::cS0 + (t & 1) * BN, sdesc_sw128(aQ + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(aK + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+          mma_ss(tmem + C::cS0 + (t & 1) * BN, sdesc_at(dQ0, (kk >> 2) * BM * 128 + (kk & 3) * 32),
+                 sdesc_at(dK0, (kk >> 2) * BN * 128 + (kk & 3) * 32), ID_S, kk > 0);
         mma_commit(&bars[kFwSFull + (t & 1)]);
         mma_commit(&bars[kFwKEmpty + sk]);  // K(t) is read by S(t) only
         return true;
@@ -170,14 +170,14 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
         if (!(ok = wait_bar(&bars[kFwPFull], t & 1, abort_flag, a))) break;
         tc_fence_after();
         const int sv = t % NV;
-        const uint32_t aV = smem_u32(smem + C::oV + sv * C::kV);
+        const uint64_t dVt = sdesc_sw128(smem_u32(smem + C::oV + sv * C::kV), BN * 128, 1024);
         const uint32_t sb = tmem + C::cS0 + (t & 1) * BN;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
 #pragma unroll
           for (int kk = 0; kk < NC / 16; ++kk)  // keys 16·kk.. of half g: P pairs at +8·kk of its columns
             mma_ts(tmem + C::cO + g * DV, sb + g * NC + kk * 8,
-                   sdesc_sw128(aV + (g * (NC / 16) + kk) * 2048, BN * 128, 1024), ID_O, (t > 0 || kk > 0) ? 1u : 0u);
+                   sdesc_at(dVt, (g * (NC / 16) + kk) * 2048), ID_O, (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars[kFwOFull]);
         mma_commit(&bars[kFwVEmpty + sv]);

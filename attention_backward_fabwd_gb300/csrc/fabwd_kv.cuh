@@ -163,24 +163,25 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
       constexpr uint32_t ID_S = idesc_f16(BC, BR, kBF16, false, false);
       constexpr uint32_t ID_DV = idesc_f16(BC, DV, kBF16, false, true);
       constexpr uint32_t ID_DK = idesc_f16(BC, D, kBF16, false, true);
-      const uint32_t aK = smem_u32(smem + C::oK), aV = smem_u32(smem + C::oV);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::oK), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::oV), 16, 1024);
       // A operand columns of k-step kk (16 queries): warpgroup kk/4 holds queries 64·(kk/4)..,
       // its 16-bit pairs at +0..31 of its own 64 columns
       auto a_col = [](int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; };
       auto issue_s = [&](int t) {  // Q(t) landed: vouched for by the compute warps' P(t-1) handoff
-        const uint32_t aQ = smem_u32(smem + C::oQ + (t % NQ) * C::kQ);
+        const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::oQ + (t % NQ) * C::kQ), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::cS, sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(aQ + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+          mma_ss(tmem + C::cS, sdesc_at(dK0, (kk >> 2) * BC * 128 + (kk & 3) * 32),
+                 sdesc_at(dQ0, (kk >> 2) * BR * 128 + (kk & 3) * 32), ID_S, kk > 0);
         mma_commit(&bars[kKvSFull]);
       };
       auto issue_dp = [&](int t) {  // dO(t) landed: vouched for by the compute warps' dS(t-1) handoff
-        const uint32_t adO = smem_u32(smem + C::odO + (t % NO) * C::kdO);
+        const uint64_t ddO0 = sdesc_sw128(smem_u32(smem + C::odO + (t % NO) * C::kdO), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
-          mma_ss(tmem + C::cP, sdesc_sw128(aV + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(adO + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
+          mma_ss(tmem + C::cP, sdesc_at(dV0, (kk >> 2) * BC * 128 + (kk & 3) * 32),
+                 sdesc_at(ddO0, (kk >> 2) * BR * 128 + (kk & 3) * 32), ID_S, kk > 0);
         mma_commit(&bars[kKvDpFull]);
       };
       bool ok = wait_bar(&bars[kKvKvFull], 0, abort_flag, a) && wait_bar(&bars[kKvQFull], 0, abort_flag, a) &&
@@ -192,12 +193,13 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
       }
       for (int t = 0; ok && t < T; ++t) {
         const int sq_ = t % NQ, so = t % NO;
-        const uint32_t aQ = smem_u32(smem + C::oQ + sq_ * C::kQ), adO = smem_u32(smem + C::odO + so * C::kdO);
+        const uint64_t dQt = sdesc_sw128(smem_u32(smem + C::oQ + sq_ * C::kQ), BR * 128, 1024);
+        const uint64_t ddOt = sdesc_sw128(smem_u32(smem + C::odO + so * C::kdO), BR * 128, 1024);
         if (!(ok = wait_bar(&bars[kKvPFull], t & 1, abort_flag, a))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BR / 16; ++kk)
-          mma_ts(tmem + C::cDV, tmem + C::cS + a_col(kk), sdesc_sw128(adO + kk * 2048, BR * 128, 1024), ID_DV,
+          mma_ts(tmem + C::cDV, tmem + C::cS + a_col(kk), sdesc_at(ddOt, kk * 2048), ID_DV,
                  (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kKvOEmpty + so]);  // dO(t) read; the compute warps add their sfmg arrivals
         // Sᵀ of the next step may overwrite the Pᵀ columns once dV (issued above) has read them
@@ -206,7 +208,7 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BR / 16; ++kk)
-          mma_ts(tmem + C::cDK, tmem + C::cP + a_col(kk), sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK,
+          mma_ts(tmem + C::cDK, tmem + C::cP + a_col(kk), sdesc_at(dQt, kk * 2048), ID_DK,
                  (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kKvQEmpty + sq_]);
         if (t + 1 < T) issue_dp(t + 1);  // after dK read the dSᵀ held in the dPᵀ columns

@@ -220,6 +220,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Descriptor of the tile `off` bytes (a multiple of 16) past the one `base` describes.  The
+// start-address field holds address >> 4 in bits 0-13; shared-memory addresses stay below
+// 2^18, so adding off >> 4 never carries out of it and the result equals sdesc_sw128 of the
+// moved address with the same strides.  Lets the MMA thread build each operand's descriptor
+// once and step through the k-slices with one add.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t base, uint32_t off) { return base + (off >> 4); }
+
 // Instruction descriptor for tcgen05.mma kind::f16 with fp32 accumulation.
 // bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (0 = f16, 1 = bf16);
 // bit 15 A major, bit 16 B major (0 = K-major, 1 = MN-major); 17-22 N >> 3; 24-28 M >> 4.

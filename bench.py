@@ -328,7 +328,7 @@ def stage_table(pb, r, peak_tf, peak_hbm):
 
 
 # revision of each kernel's code that profiles/traffic.json must match
-KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v2", "fabwd_kv_kernel": "kv-v4", "fabwd_dq_kernel": "dq-v4",
+KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v3", "fabwd_kv_kernel": "kv-v5", "fabwd_dq_kernel": "dq-v5",
               "fabwd_main_kernel": "main-v4"}
 
 
