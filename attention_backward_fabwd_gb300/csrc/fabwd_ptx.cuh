@@ -210,7 +210,7 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 //   MN-major operand: 128-B rows hold 64 consecutive M/N elements of one K index; 8 K rows form
 //                     an atom; LBO = byte stride between 64-element M/N blocks, SBO = byte
 //                     stride between 8-row K groups.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+__host__ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
   d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
@@ -225,7 +225,7 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 // 2^18, so adding off >> 4 never carries out of it and the result equals sdesc_sw128 of the
 // moved address with the same strides.  Lets the MMA thread build each operand's descriptor
 // once and step through the k-slices with one add.
-__device__ __forceinline__ uint64_t sdesc_at(uint64_t base, uint32_t off) { return base + (off >> 4); }
+__host__ __device__ __forceinline__ uint64_t sdesc_at(uint64_t base, uint32_t off) { return base + (off >> 4); }
 
 // Instruction descriptor for tcgen05.mma kind::f16 with fp32 accumulation.
 // bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (0 = f16, 1 = bf16);
