@@ -61,6 +61,13 @@ fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
     if (p->B * p->S1 >= (1ll << 31) || p->B * p->S2 >= (1ll << 31)) return FABWD_ERR_INVALID;
   }
   if (!main_supported((int)p->D, (int)p->Dv)) return FABWD_ERR_UNSUPPORTED;
+  // The workspace holds B·N1·roundup(S1, 128) fp32 rows twice.  With TND, B, N1 and the
+  // max_seqlen_q bound S1 are limited only one by one, so the product could wrap size_t;
+  // refuse more than 2^40 rows (4 TiB each) before any size is computed.
+  {
+    const long long s1p = (p->S1 + kRowPad - 1) / kRowPad * kRowPad;
+    if (s1p > 0 && (p->B * p->N1 > (1ll << 40) / s1p)) return FABWD_ERR_INVALID;
+  }
 
   pl->rowsQ = tnd ? p->T1 : p->B * p->S1;
   pl->rowsK = tnd ? p->T2 : p->B * p->S2;

@@ -186,6 +186,17 @@ def test_tnd_validation(lib):
         F.FABWD_ERR_INVALID
 
 
+def test_workspace_size_cannot_wrap(lib):
+    # TND bounds B, N1 and max_seqlen_q one by one; their product sizes the workspace rows and
+    # would wrap 64 bits at the extremes: refused on the host instead of a short workspace
+    tnd = dict(layout=F.FABWD_TND, cu_seqlens_q=0x20000, cu_seqlens_kv=0x20000, T1=1 << 20, T2=1 << 20)
+    assert ws_size(base_params(B=65535, N1=65535, N2=65535, S1=(1 << 30) - 1, S2=4096, **tnd))[0] == \
+        F.FABWD_ERR_INVALID
+    # a large but representable plan still sizes: 2^40 rows exactly
+    s, nbytes = ws_size(base_params(B=1 << 12, N1=1 << 8, N2=1 << 8, S1=1 << 20, S2=4096, **tnd))
+    assert s == F.FABWD_OK and nbytes >= 2 * 4 * (1 << 40)
+
+
 def test_empty_sizes_are_valid(lib):
     assert ws_size(base_params(S1=0))[0] == F.FABWD_OK
     assert ws_size(base_params(S2=0))[0] == F.FABWD_OK
