@@ -68,6 +68,9 @@ fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
     const long long s1p = (p->S1 + kRowPad - 1) / kRowPad * kRowPad;
     if (s1p > 0 && (p->B * p->N1 > (1ll << 40) / s1p)) return FABWD_ERR_INVALID;
   }
+  // Each batch is one grid row of 128-row query blocks over N1 heads plus 128-row key blocks
+  // over N2 heads; that count must fit a launch's x dimension (and the int the launches use).
+  if ((p->S1 + 127) / 128 * p->N1 + (p->S2 + 127) / 128 * p->N2 > 0x7fffffffll) return FABWD_ERR_UNSUPPORTED;
 
   pl->rowsQ = tnd ? p->T1 : p->B * p->S1;
   pl->rowsK = tnd ? p->T2 : p->B * p->S2;

@@ -123,7 +123,8 @@ typedef struct {
  * word, the fp32 sfmg and log2-scaled lse rows padded per (sequence, q-head) to a multiple of
  * 128, and, in FABWD_DQ_ATOMIC mode only, the fp32 dq accumulator (q's shape with D).  Errors:
  * NULLPTR (p or bytes NULL), INVALID (also when B·N1·roundup(S1, 128) exceeds 2^40 rows, so
- * that no size computation can wrap), UNSUPPORTED. */
+ * that no size computation can wrap), UNSUPPORTED (also when ceil(S1/128)·N1 + ceil(S2/128)·N2,
+ * the CTAs of one batch's grid row, exceeds 2^31 − 1). */
 fabwd_status fabwd_workspace_size(const fabwd_params* p, size_t* bytes);
 
 /* Enqueue on `stream` (a cudaStream_t; NULL = the legacy default stream) the preprocess kernel

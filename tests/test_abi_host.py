@@ -197,6 +197,14 @@ def test_workspace_size_cannot_wrap(lib):
     assert s == F.FABWD_OK and nbytes >= 2 * 4 * (1 << 40)
 
 
+def test_grid_size_limit(lib):
+    # 2^27 queries over 4096 heads: 2^32 query-block CTAs in one grid row, more than a launch's x
+    # dimension holds (the workspace, 2^39 rows, would still be sizable)
+    p = base_params(B=1, N1=4096, N2=4096, S1=1 << 27, S2=128)
+    assert ws_size(p)[0] == F.FABWD_ERR_UNSUPPORTED
+    assert ws_size(base_params(B=1, N1=4096, N2=4096, S1=1 << 20, S2=128))[0] == F.FABWD_OK
+
+
 def test_empty_sizes_are_valid(lib):
     assert ws_size(base_params(S1=0))[0] == F.FABWD_OK
     assert ws_size(base_params(S2=0))[0] == F.FABWD_OK
