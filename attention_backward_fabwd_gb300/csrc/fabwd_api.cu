@@ -473,6 +473,14 @@ const char* fabwd_status_string(fabwd_status s) {
   return "unknown status";
 }
 
-int fabwd_version(void) { return 100; }
+int fabwd_version(void) { return 101; }
+
+fabwd_status fabwd_kernel_binary_version(int32_t* version) {
+  if (!version) return FABWD_ERR_NULLPTR;
+  int v = 0;
+  if (kernel_binary_version(&v) != cudaSuccess) return FABWD_ERR_CUDA;
+  *version = v;
+  return FABWD_OK;
+}
 
 }  // extern "C"

@@ -174,6 +174,13 @@ int grid_for(long long work_items, int per_block) {
 
 }  // namespace
 
+cudaError_t kernel_binary_version(int* version) {
+  cudaFuncAttributes at;
+  const cudaError_t e = cudaFuncGetAttributes(&at, zero_kernel);
+  if (e == cudaSuccess) *version = at.binaryVersion;
+  return e;
+}
+
 cudaError_t launch_zero(void* p, long long bytes, cudaStream_t st) {
   if (bytes <= 0) return cudaSuccess;
   const long long n16 = bytes / 16;

@@ -387,13 +387,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 template <int D, int DV, bool FP16>
 cudaError_t launch_fwd_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) {
   using C = FwdCfg<D, DV>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fabwd_fwd_kernel<D, DV, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::bytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (cudaError_t e = ensure_smem_limit<fabwd_fwd_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
   dim3 grid(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B);
   fabwd_fwd_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, a);
   return cudaGetLastError();

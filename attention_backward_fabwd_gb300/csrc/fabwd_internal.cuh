@@ -1,11 +1,29 @@
 // Internal kernel arguments and launchers shared by the libfabwd translation units.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fabwd {
+
+// Raises the dynamic shared-memory limit of `Kernel` to `bytes` on the current device.  The
+// attribute belongs to a (function, device) pair, so it is set once per device: devices 0-63
+// are remembered in a bit mask, others get it before every launch.  Host threads may race here;
+// both then set the same value, which is harmless.
+template <auto Kernel>
+cudaError_t ensure_smem_limit(int bytes) {
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 constexpr int kBlockKV = 128;  // kv rows per CTA of the main kernel (M of the kv-side MMAs)
 constexpr int kBlockQ = 64;    // q rows per main-loop step (N of S^T / dP^T / dQ^T)
@@ -107,5 +125,7 @@ cudaError_t launch_bwd_wide_fp16(const MainArgs& a, const MainMaps& mkv, const M
 cudaError_t launch_fwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
 cudaError_t launch_fwd_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
 bool main_supported(int D, int Dv);
+// binaryVersion (major * 10 + minor) of the library's kernels as loaded on the current device.
+cudaError_t kernel_binary_version(int* version);
 
 }  // namespace fabwd

@@ -412,13 +412,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 template <int D, int DV, bool FP16>
 cudaError_t launch_kv_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
   using C = KvCfg<D, DV>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fabwd_kv_kernel<D, DV, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::bytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (cudaError_t e = ensure_smem_limit<fabwd_kv_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
   dim3 grid(n_kv_blocks * a.N2, a.B);
   fabwd_kv_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
   return cudaGetLastError();

@@ -555,13 +555,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 template <int D, int DV, bool FP16, bool FUSED>
 cudaError_t launch_main_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
   using C = MainCfg<D, DV, FUSED>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fabwd_main_kernel<D, DV, FP16, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::bytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (cudaError_t e = ensure_smem_limit<fabwd_main_kernel<D, DV, FP16, FUSED>>((int)C::bytes); e != cudaSuccess) return e;
   // blockIdx.x = kv-block * N2 + kv-head: the heaviest kv-blocks (earliest keys under a causal
   // mask) of every head launch first.
   dim3 grid(n_kv_blocks * a.N2, a.B);

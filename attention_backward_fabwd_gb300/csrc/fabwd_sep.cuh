@@ -27,13 +27,7 @@ template <int D, int DV, bool FP16>
 cudaError_t launch_bwd_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
   static_assert(DqCfg<D, DV>::BN == KvCfg<D, DV>::BC, "one tensor map box for both CTA kinds");
   constexpr uint32_t bytes = KvCfg<D, DV>::bytes > DqCfg<D, DV>::bytes ? KvCfg<D, DV>::bytes : DqCfg<D, DV>::bytes;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fabwd_bwd_kernel<D, DV, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)bytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (cudaError_t e = ensure_smem_limit<fabwd_bwd_kernel<D, DV, FP16>>((int)bytes); e != cudaSuccess) return e;
   const int kv_ctas = n_kv_blocks * a.N2;
   const int dq_ctas = ((a.S1 + DqCfg<D, DV>::BM - 1) / DqCfg<D, DV>::BM) * a.N1;
   dim3 grid(kv_ctas + dq_ctas, a.B);
@@ -62,13 +56,7 @@ cudaError_t launch_bwd_wide_t(const MainArgs& a, const MainMaps& mkv, const Main
                               cudaStream_t st) {
   constexpr uint32_t kb = MainCfg<D, DV, false>::bytes, qb = DqCfg<D, DV>::bytes;
   constexpr uint32_t bytes = kb > qb ? kb : qb;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fabwd_bwd_wide_kernel<D, DV, FP16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (cudaError_t e = ensure_smem_limit<fabwd_bwd_wide_kernel<D, DV, FP16>>((int)bytes); e != cudaSuccess) return e;
   const int kv_ctas = n_kv_blocks * a.N2;
   const int dq_ctas = ((a.S1 + DqCfg<D, DV>::BM - 1) / DqCfg<D, DV>::BM) * a.N1;
   dim3 grid(kv_ctas + dq_ctas, a.B);

@@ -16,7 +16,7 @@
 
 namespace {
 
-constexpr size_t kStaticWorkspaceBytes = 64ull << 20;  // 64 MiB per GPU that loads the library
+constexpr size_t kStaticWorkspaceBytes = FABWD_STATIC_WORKSPACE_BYTES;  // per GPU that loads the library
 
 // The scratch itself.  Host code must not pass this name to a kernel: on the host it is only a
 // stand-in symbol, so its device address is looked up with cudaGetSymbolAddress below.
@@ -54,3 +54,13 @@ extern "C" fabwd_status fabwd_run_static_workspace(const fabwd_params* p, void* 
   return fabwd_run(p, ws, kStaticWorkspaceBytes, stream);
 }
 
+
+extern "C" size_t fabwd_static_workspace_capacity(void) { return kStaticWorkspaceBytes; }
+
+extern "C" fabwd_status fabwd_static_workspace_status(void* stream, uint32_t* device_status) {
+  if (!device_status) return FABWD_ERR_NULLPTR;
+  void* ws = nullptr;
+  fabwd_status s = static_workspace_address(&ws);
+  if (s != FABWD_OK) return s;
+  return fabwd_read_device_status(ws, kStaticWorkspaceBytes, stream, device_status);
+}

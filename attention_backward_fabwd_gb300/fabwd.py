@@ -73,15 +73,20 @@ def lib() -> ctypes.CDLL:
         L.fabwd_run_main.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run_dq.argtypes = [P, ctypes.c_void_p, sz, ctypes.c_void_p]
         L.fabwd_run_static_workspace.argtypes = [P, ctypes.c_void_p]
+        L.fabwd_static_workspace_capacity.argtypes = []
+        L.fabwd_static_workspace_capacity.restype = ctypes.c_size_t
+        L.fabwd_static_workspace_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
         L.fabwd_read_device_status.argtypes = [ctypes.c_void_p, sz, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
         L.fabwd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.fabwd_set_wait_limit_ns.restype = ctypes.c_uint64
         L.fabwd_debug_inject_timeout.argtypes = [ctypes.c_int]
+        L.fabwd_kernel_binary_version.argtypes = [ctypes.POINTER(ctypes.c_int32)]
         L.fabwd_status_string.argtypes = [ctypes.c_int]
         L.fabwd_status_string.restype = ctypes.c_char_p
         for f in ("fabwd_workspace_size", "fabwd_workspace_layout", "fabwd_preprocess", "fabwd_run",
                   "fabwd_run_main", "fabwd_run_dq", "fabwd_read_device_status", "fabwd_run_static_workspace",
-                  "fabwd_resolve_dq_mode", "fabwd_preprocess_stats", "fabwd_forward"):
+                  "fabwd_resolve_dq_mode", "fabwd_preprocess_stats", "fabwd_forward",
+                  "fabwd_static_workspace_status", "fabwd_kernel_binary_version"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -91,7 +96,7 @@ def declared_functions() -> list:
     """Names of the functions include/fabwd.h declares."""
     with open(HEADER) as f:
         text = f.read()
-    return sorted(set(re.findall(r"^\s*(?:fabwd_status|const char\*|uint64_t|int)\s+(fabwd_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:fabwd_status|const char\*|uint64_t|size_t|int)\s+(fabwd_\w+)\s*\(", text, re.M)))
 
 
 def status_string(status: int) -> str:
@@ -169,6 +174,18 @@ def fabwd_run_static_workspace(p: fabwd_params, stream: int) -> None:
         raise FabwdError(s, "fabwd_run_static_workspace")
 
 
+def fabwd_static_workspace_capacity() -> int:
+    return lib().fabwd_static_workspace_capacity()
+
+
+def fabwd_static_workspace_status(stream: int):
+    """Returns (status code, device status bits) of the last fabwd_run_static_workspace call on the
+    current device; synchronises the stream."""
+    v = ctypes.c_uint32(0)
+    s = lib().fabwd_static_workspace_status(stream, ctypes.byref(v))
+    return s, v.value
+
+
 def fabwd_read_device_status(workspace: int, workspace_bytes: int, stream: int):
     """Returns (status code, device status bits); synchronises the stream."""
     v = ctypes.c_uint32(0)
@@ -182,6 +199,14 @@ def fabwd_set_wait_limit_ns(ns: int) -> int:
 
 def fabwd_debug_inject_timeout(on: bool) -> int:
     return lib().fabwd_debug_inject_timeout(1 if on else 0)
+
+
+def fabwd_kernel_binary_version() -> int:
+    v = ctypes.c_int32(0)
+    s = lib().fabwd_kernel_binary_version(ctypes.byref(v))
+    if s != FABWD_OK:
+        raise FabwdError(s, "fabwd_kernel_binary_version")
+    return v.value
 
 
 def fabwd_version() -> int:

@@ -2,20 +2,28 @@
 """Benchmark: attention-backward TFLOP/s (bf16) on one GB300 and % of dense tensor peak.
 
 One step = one pass of the whole backward path over one batch of synthetic input:
-fabwd_preprocess (sfmg, lse rows, dq accumulator zeroing) -> fabwd_run_main (the dK/dV kernel,
-or the fused kernel in the atomic dQ mode) -> fabwd_run_dq (the dQ kernel, or the convert pass),
-all libfabwd kernels on one stream, with CUDA events between the stages.
+fabwd_preprocess (sfmg, lse rows, dq accumulator zeroing) then fabwd_run (in the default
+separate dQ mode one grid of dK/dV and dQ CTAs; in the atomic dQ mode the fused kv-stationary
+kernel and the convert pass), all libfabwd kernels on one stream, with CUDA events between the
+stages.
 
 `value` follows the measurement convention: per head 2·S1·S2·(3D + 2Dv), halved under a causal
-mask, over the whole step.  `roofline` is the stage kernel with the longest time, credited with
-its own algorithmic flops: 2·(inner dimensions of the products it forms) per visible (query, key)
-pair — (3D + 2Dv) for the fused kernel, (2D + 2Dv) for the dK/dV kernel, (2D + Dv) for the dQ
-kernel (which forms S and dP again).
+mask, over the whole step.  `roofline` is the tensor kernel with the longest time, credited with
+the method's algorithmic work only: 2·(3D + 2Dv) flops per visible (query, key) pair, the five
+products of the backward once each.  The separate dQ mode forms S and dP a second time in its
+dQ CTAs; that executed work, 2·(4D + 3Dv) per pair, is reported beside it as `executed_frac`
+and never counted in `frac`.
+
+The headline workload (--workload, default the causal GQA S=4096 one) carries every extra: the
+e2e pass through pinned host buffers, the forward side pass, the per-kind breakdown and the CPU
+baseline.  The `workloads` object times the step of every workload of the measurement with the
+same --steps/--warmup, L2 flushed between steps.
 
 Inputs: q, k, v, dout are the seeded draws of attention_backward_fabwd_gb300.inputs; attn_out
 and softmax_lse come from a plain torch fp32 forward on the GPU (input synthesis, untimed).
 The L2 cache (129 MB) is flushed between timed steps by writing a 256 MB buffer (untimed).
-SM clocks and throttle reasons are sampled by nvidia-smi every 50 ms inside the timed region.
+SM clocks, power and clock-event reasons are read in-process through NVML's read-only queries
+every 2 ms inside the timed region (nvidia-smi at 50 ms when NVML cannot be loaded).
 
 `--impl reference` times the fp64 CPU oracle instead (host cores, bounded sample per step).
 Multi-GPU (torchrun): each rank runs an independent replica (no collective on the data path);
@@ -55,6 +63,8 @@ def parse_args():
     ap.add_argument("--no-forward", action="store_true", help="skip the untimed pass that times fabwd_forward")
     ap.add_argument("--no-breakdown", action="store_true",
                     help="skip the untimed pass that launches the dK/dV and dQ kernels on their own")
+    ap.add_argument("--workloads", default="all",
+                    help="comma-separated workloads whose step is timed beside the headline one, 'all' or 'none'")
     return ap.parse_args()
 
 
@@ -267,6 +277,108 @@ class ClockSampler:
                 "power_w_max": max(power), "period_ms": 50}
 
 
+class NvmlClocks:
+    """SM clock, power and clock-event reasons of one GPU, read in-process through NVML's
+    read-only queries every `period_s` by a background thread (no setting is changed).
+    summary() keeps the samples taken inside the window marked by mark_start()/mark_end().
+    available is False when libnvidia-ml cannot be loaded or the GPU is not found."""
+
+    # nvmlClocksEventReasons bits (NVML API constants)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id=None, period_s=0.002):
+        import ctypes
+        import threading
+
+        self.period_s = period_s
+        self.samples = []
+        self.t0 = self.t1 = None
+        self.available = False
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            ok = False
+            if pci_bus_id:
+                ok = self.nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h)) == 0
+            if not ok:
+                n = ctypes.c_uint(0)
+                if self.nv.nvmlDeviceGetCount_v2(ctypes.byref(n)) != 0 or n.value != 1:
+                    return
+                ok = self.nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h)) == 0
+            if not ok:
+                return
+            self._reasons = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint(0)
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM = 1
+            self.sm_max = mx.value
+            self.available = self._read() is not None
+        except (OSError, AttributeError):
+            self.available = False
+
+    def _read(self):
+        import ctypes
+
+        clk, mw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) != 0:
+            return None
+        self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw))
+        self._reasons(self.h, ctypes.byref(rs))
+        return time.time(), clk.value, mw.value / 1000.0, rs.value
+
+    def _loop(self):
+        while not self._stop.is_set():
+            r = self._read()
+            if r is not None:
+                self.samples.append(r)
+            time.sleep(self.period_s)
+
+    def __enter__(self):
+        import threading
+
+        if self.available:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def summary(self):
+        if not self.available or not self.samples:
+            return None
+        win = [r for r in self.samples if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        rows = win or self.samples
+        reasons = sorted({name for r in rows for bit, name in self.REASONS.items() if r[3] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": self.sm_max, "reasons": reasons,
+                "samples": len(rows), "samples_in_timed_region": len(win),
+                "power_w_max": max(r[2] for r in rows), "period_ms": 1e3 * self.period_s, "source": "nvml"}
+
+
+def pci_bus_id_string(dev):
+    """The GPU's PCI address in NVML's form (domain:bus:device.0), or None."""
+    import torch
+
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        return f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -290,9 +402,12 @@ def profile_traffic(workload, kernel):
 
 
 def stage_table(pb, r, peak_tf, peak_hbm):
-    """Per-stage timing with each kernel's algorithmic work: tensor stages count 2·(the inner
-    dimensions of their own products) flops per visible (query, key) pair; HBM stages count the
-    bytes they must read and write."""
+    """Per-stage timing with each kernel's algorithmic work.  Tensor stages are credited with the
+    method's products they form, 2·(inner dimension) flops per visible (query, key) pair each:
+    the one-grid separate-mode kernel and the fused atomic-mode kernel with all five,
+    2·(3D + 2Dv); the dK/dV kernel alone with S, dP, dV, dK, 2·(2D + 2Dv); the dQ kernel alone
+    with dQ, 2·D (its S and dP are recomputed).  `executed_*` counts every product a kernel
+    forms, recomputed ones included.  HBM stages count the bytes they must read and write."""
     w = pb.w
     pairs = w.N1 * sum(visible_pairs(L1, L2, w) for L1, L2 in seq_lengths(pb))
     e = 2
@@ -304,25 +419,29 @@ def stage_table(pb, r, peak_tf, peak_hbm):
         gbs = nbytes / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
         return {"kernel": kernel, "bound": "hbm", "ms": ms, "bytes": nbytes, "GB/s": gbs, "frac_of_hbm": gbs / peak_hbm}
 
-    def tensor(kernel, ms, per_pair):
-        f = per_pair * pairs
+    def tensor(kernel, ms, method_per_pair, executed_per_pair):
+        f, fx = method_per_pair * pairs, executed_per_pair * pairs
         tf = f / (ms * 1e-3) / 1e12 if ms > 0 else 0.0
-        return {"kernel": kernel, "bound": "tensor", "ms": ms, "flops": f, "flops_per_pair": per_pair,
-                "TFLOP/s": tf, "frac_of_peak": tf / peak_tf}
+        tfx = fx / (ms * 1e-3) / 1e12 if ms > 0 else 0.0
+        return {"kernel": kernel, "bound": "tensor", "ms": ms, "flops": f, "flops_per_pair": method_per_pair,
+                "TFLOP/s": tf, "frac_of_peak": tf / peak_tf, "executed_flops": fx,
+                "executed_flops_per_pair": executed_per_pair, "executed_TFLOP/s": tfx,
+                "executed_frac_of_peak": tfx / peak_tf}
 
+    full = 2 * (3 * w.D + 2 * w.Dv)
+    kv_part, dq_exec = 2 * (2 * w.D + 2 * w.Dv), 2 * (2 * w.D + w.Dv)
     out = {"preprocess": hbm("preprocess_kernel", r["ms_pre"], pre_bytes)}
     if r.get("merged"):
         # one grid of dK/dV CTAs (S, dP, dV, dK) and dQ CTAs (S, dP again, dQ)
-        out["backward"] = tensor("fabwd_bwd_kernel" if w.D <= 128 else "fabwd_bwd_wide_kernel", r["ms_main"],
-                                 2 * (2 * w.D + 2 * w.Dv) + 2 * (2 * w.D + w.Dv))
+        out["backward"] = tensor("fabwd_bwd_kernel" if w.D <= 128 else "fabwd_bwd_wide_kernel", r["ms_main"], full,
+                                 kv_part + dq_exec)
         if r.get("alone"):
             out["backward"]["launched_alone_ms"] = r["alone"]
     elif r["separate"]:
-        out["dkdv"] = tensor("fabwd_kv_kernel" if w.D <= 128 else "fabwd_main_kernel", r["ms_main"],
-                             2 * (2 * w.D + 2 * w.Dv))
-        out["dq"] = tensor("fabwd_dq_kernel", r["ms_conv"], 2 * (2 * w.D + w.Dv))
+        out["dkdv"] = tensor("fabwd_kv_kernel" if w.D <= 128 else "fabwd_main_kernel", r["ms_main"], kv_part, kv_part)
+        out["dq"] = tensor("fabwd_dq_kernel", r["ms_conv"], 2 * w.D, dq_exec)
     else:
-        out["main"] = tensor("fabwd_main_kernel", r["ms_main"], 2 * (3 * w.D + 2 * w.Dv))
+        out["main"] = tensor("fabwd_main_kernel", r["ms_main"], full, full)
         out["convert"] = hbm("convert_kernel", r["ms_conv"], (4 + e) * r["dq_elems"])
     return out
 
@@ -356,15 +475,11 @@ def replica_workload(w, rank):
     return inputs.sized(w, seed=w.seed + 7919 * rank)
 
 
-def gpu_arm(args, rank, world, local_rank):
+def prepare(w, dev, dq_mode):
+    """Device inputs, outputs, params and workspace of one workload (untimed)."""
     import torch
-    from attention_backward_fabwd_gb300 import api, build, fabwd, inputs
+    from attention_backward_fabwd_gb300 import api, fabwd, inputs
 
-    build.build()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    w = inputs.WORKLOADS[args.workload]
-    w = replica_workload(w, rank)
     pb = inputs.make_problem(w)
     attn_out, lse = synth_forward(pb, dev)
     q, k, v, dout = (t.to(dev) for t in (pb.q, pb.k, pb.v, pb.dout))
@@ -375,78 +490,106 @@ def gpu_arm(args, rank, world, local_rank):
         cu_kv = torch.from_numpy(pb.cu_seqlens_kv).to(dev)
         extra = dict(max_seqlen_q=pb.S1, max_seqlen_kv=pb.S2)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    p = api.make_params(q, k, v, dout, attn_out, lse, dq, dk, dv, cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv,
-                        softmax_scale=w.softmax_scale, mask_mode=w.mask_mode, win_left=w.win_left,
-                        win_right=w.win_right, layout=w.layout, dq_mode=args.dq_mode, **extra)
+    mk = dict(cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv, softmax_scale=w.softmax_scale, mask_mode=w.mask_mode,
+              win_left=w.win_left, win_right=w.win_right, layout=w.layout, dq_mode=dq_mode, **extra)
+    p = api.make_params(q, k, v, dout, attn_out, lse, dq, dk, dv, **mk)
     nbytes = fabwd.fabwd_workspace_size(p)
     resolved = fabwd.fabwd_resolve_dq_mode(p)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    # separate dQ mode: fabwd_run launches the dK/dV and dQ CTAs as one grid
+    return dict(pb=pb, w=w, ins=[q, k, v, dout, attn_out, lse], outs=[dq, dk, dv], p=p, mk=mk, ws=ws, nbytes=nbytes,
+                separate=resolved == fabwd.FABWD_DQ_SEPARATE, merged=resolved == fabwd.FABWD_DQ_SEPARATE,
+                cu_q=cu_q, cu_kv=cu_kv)
+
+
+def run_step(c, st, evs=None):
+    """One step on stream st: preprocess, then the backward; events between the stages."""
+    from attention_backward_fabwd_gb300 import fabwd
+
+    p, ws, nbytes, sp = c["p"], c["ws"], c["nbytes"], st.cuda_stream
+    if evs:
+        evs[0].record(st)
+    fabwd.fabwd_preprocess(p, ws.data_ptr(), nbytes, sp)
+    if evs:
+        evs[1].record(st)
+    if c["merged"]:
+        fabwd.fabwd_run(p, ws.data_ptr(), nbytes, sp)
+        if evs:
+            evs[2].record(st)
+            evs[3].record(st)
+        return
+    fabwd.fabwd_run_main(p, ws.data_ptr(), nbytes, sp)
+    if evs:
+        evs[2].record(st)
+    fabwd.fabwd_run_dq(p, ws.data_ptr(), nbytes, sp)
+    if evs:
+        evs[3].record(st)
+
+
+def check_status(c, st, when):
+    from attention_backward_fabwd_gb300 import fabwd
+
+    s_, bits = fabwd.fabwd_read_device_status(c["ws"].data_ptr(), c["nbytes"], st.cuda_stream)
+    if s_ != fabwd.FABWD_OK:
+        raise RuntimeError(f"device status {bits:#x} {when}")
+
+
+def time_steps(c, dev, st, steps, warmup, flush, barrier=lambda: None, clk=None):
+    """W untimed warm-up steps, then `steps` timed ones, each after an untimed L2 flush; returns
+    per-stage mean ms (preprocess, main, dQ stage, step) and the wall time of the timed loop."""
+    import torch
+
+    for _ in range(max(warmup, 0)):
+        flush.fill_(1)
+        run_step(c, st)
+    check_status(c, st, "after warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall0 = time.perf_counter()
+    if clk is not None:
+        clk.mark_start()
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        run_step(c, st, evs[i])
+    torch.cuda.synchronize(dev)
+    if clk is not None:
+        clk.mark_end()
+    barrier()
+    t_wall = time.perf_counter() - t_wall0
+    check_status(c, st, "after the timed steps")
+    mean = lambda i, j: statistics.mean(e[i].elapsed_time(e[j]) for e in evs)
+    return dict(ms_pre=mean(0, 1), ms_main=mean(1, 2), ms_conv=mean(2, 3), ms_step=mean(0, 3), t_wall=t_wall)
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    from attention_backward_fabwd_gb300 import api, build, fabwd, inputs
+
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = replica_workload(inputs.WORKLOADS[args.workload], rank)
+    c = prepare(w, dev, args.dq_mode)
+    pb = c["pb"]
+    q, k, v, dout, attn_out, lse = c["ins"]
+    dq, dk, dv = c["outs"]
+    p, ws, nbytes, merged = c["p"], c["ws"], c["nbytes"], c["merged"]
+    cu_q, cu_kv = c["cu_q"], c["cu_kv"]
     st = torch.cuda.current_stream(dev)
     sp = st.cuda_stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    # separate dQ mode: fabwd_run launches the dK/dV and dQ CTAs as one grid
-    merged = resolved == fabwd.FABWD_DQ_SEPARATE
-
-    def step(evs=None):
-        if evs:
-            evs[0].record(st)
-        fabwd.fabwd_preprocess(p, ws.data_ptr(), nbytes, sp)
-        if evs:
-            evs[1].record(st)
-        if merged:
-            fabwd.fabwd_run(p, ws.data_ptr(), nbytes, sp)
-            if evs:
-                evs[2].record(st)
-                evs[3].record(st)
-            return
-        fabwd.fabwd_run_main(p, ws.data_ptr(), nbytes, sp)
-        if evs:
-            evs[2].record(st)
-        fabwd.fabwd_run_dq(p, ws.data_ptr(), nbytes, sp)
-        if evs:
-            evs[3].record(st)
-
-    for _ in range(max(args.warmup, 0)):
-        flush.fill_(1)
-        step()
-    s_, bits = fabwd.fabwd_read_device_status(ws.data_ptr(), nbytes, sp)
-    if s_ != fabwd.FABWD_OK:
-        raise RuntimeError(f"device status {bits:#x} after warm-up")
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    bus = None
-    try:
-        bus = torch.cuda.get_device_properties(dev).pci_bus_id
-        bus = f"{bus:02x}" if isinstance(bus, int) else str(bus)
-    except Exception:
-        bus = None
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    with ClockSampler(bus) as clk:
-        torch.cuda.synchronize(dev)
-        barrier()
-        t_wall0 = time.perf_counter()
-        clk.mark_start()
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)
-            step(evs[i])
-        torch.cuda.synchronize(dev)
-        clk.mark_end()
-        barrier()
-        t_wall = time.perf_counter() - t_wall0
-    pre = [e[0].elapsed_time(e[1]) for e in evs]
-    main = [e[1].elapsed_time(e[2]) for e in evs]
-    conv = [e[2].elapsed_time(e[3]) for e in evs]
-    tot = [e[0].elapsed_time(e[3]) for e in evs]
-    ms_step = statistics.mean(tot)
-    ms_main = statistics.mean(main)
-    s_, bits = fabwd.fabwd_read_device_status(ws.data_ptr(), nbytes, sp)
-    if s_ != fabwd.FABWD_OK:
-        raise RuntimeError(f"device status {bits:#x} after the timed steps")
+    bus = pci_bus_id_string(dev)
+    nv = NvmlClocks(bus)
+    with (nv if nv.available else ClockSampler(bus)) as clk:
+        t = time_steps(c, dev, st, args.steps, args.warmup, flush, barrier, clk)
+    clocks = clk.summary()
 
     # the library's forward on the same inputs (untimed region, reported beside the step)
     fwd = None
@@ -495,9 +638,7 @@ def gpu_arm(args, rank, world, local_rank):
             d_in = [q, k, v, dout, attn_out, lse] if sl == 0 else [torch.empty_like(t) for t in (q, k, v, dout, attn_out, lse)]
             d_out = [dq, dk, dv] if sl == 0 else [torch.empty_like(t) for t in (dq, dk, dv)]
             h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in d_out]
-            ps = api.make_params(*d_in, *d_out, cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv, softmax_scale=w.softmax_scale,
-                                 mask_mode=w.mask_mode, win_left=w.win_left, win_right=w.win_right, layout=w.layout,
-                                 dq_mode=args.dq_mode, **extra)
+            ps = api.make_params(*d_in, *d_out, **c["mk"])
             wss = ws if sl == 0 else torch.empty(nbytes, dtype=torch.uint8, device=dev)
             slots.append((d_in, d_out, h_out, ps, wss))
         s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -535,11 +676,33 @@ def gpu_arm(args, rank, world, local_rank):
         e2e = {"ms": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "pipelining": "two device buffer sets; H2D of step i+1 and D2H of step i-1 overlap step i"}
 
-    ms_step, ms_main, ms_pre, ms_conv, e2e_ms, t_wall = max_over_ranks(
-        [ms_step, ms_main, statistics.mean(pre), statistics.mean(conv), e2e["ms"] if e2e else 0.0, t_wall], world, dev)
-    return dict(pb=pb, w=w, ms_step=ms_step, ms_main=ms_main, ms_pre=ms_pre, ms_conv=ms_conv, e2e=e2e, e2e_ms=e2e_ms,
-                t_wall=t_wall, clocks=clk.summary(), dq_elems=dq.numel(), nbytes=nbytes,
-                separate=resolved == fabwd.FABWD_DQ_SEPARATE, merged=merged, alone=alone, fwd=fwd)
+    # every workload of the measurement: its step with the same steps/warm-up (the headline one
+    # reuses the numbers above)
+    others = {}
+    names = list(inputs.WORKLOADS) if args.workloads == "all" else \
+        ([] if args.workloads == "none" else [x for x in args.workloads.split(",") if x])
+    for name in names:
+        if name == args.workload:
+            continue
+        wo = replica_workload(inputs.WORKLOADS[name], rank)
+        co = prepare(wo, dev, args.dq_mode)
+        to = time_steps(co, dev, st, args.steps, args.warmup, flush, barrier)
+        others[name] = dict(co=co, t=to)
+        for key in ("ins", "outs", "ws"):
+            co.pop(key)
+        torch.cuda.empty_cache()
+
+    keys = ("ms_step", "ms_main", "ms_pre", "ms_conv")
+    vals = [t[k_] for k_ in keys] + [e2e["ms"] if e2e else 0.0, t["t_wall"]]
+    for name in others:
+        vals += [others[name]["t"][k_] for k_ in keys]
+    vals = max_over_ranks(vals, world, dev)
+    t = dict(zip(keys, vals[:4]))
+    e2e_ms, t_wall = vals[4], vals[5]
+    for i, name in enumerate(others):
+        others[name]["t"] = dict(zip(keys, vals[6 + 4 * i:10 + 4 * i]))
+    return dict(pb=pb, w=w, **t, e2e=e2e, e2e_ms=e2e_ms, t_wall=t_wall, clocks=clocks, dq_elems=dq.numel(),
+                nbytes=nbytes, separate=c["separate"], merged=merged, alone=alone, fwd=fwd, others=others)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -663,6 +826,32 @@ def workload_config(pb, l2):
     return cfg
 
 
+def workloads_table(r, peak_tf, peak_hbm, world):
+    """Per workload: step time, the dominant tensor kernel's time and its fraction of the peak on
+    the method's work (2·(3D + 2Dv) flops per visible pair), and the executed-work fraction."""
+    rows = {r["w"].name: dict(pb=r["pb"], t={k: r[k] for k in ("ms_step", "ms_main", "ms_pre", "ms_conv")},
+                              separate=r["separate"], merged=r["merged"], dq_elems=r["dq_elems"])}
+    for name, o in r["others"].items():
+        co = o["co"]
+        rows[name] = dict(pb=co["pb"], t=o["t"], separate=co["separate"], merged=co["merged"],
+                          dq_elems=co["pb"].q.numel())
+    out = {}
+    for name, x in rows.items():
+        pb = x["pb"]
+        conv, alg = flop_counts(pb)
+        rr = dict(x["t"], separate=x["separate"], merged=x["merged"], dq_elems=x["dq_elems"])
+        stg = stage_table(pb, rr, peak_tf, peak_hbm)
+        dom = max((v for v in stg.values() if v["bound"] == "tensor"), key=lambda v: v["ms"])
+        out[name] = {"step_ms": x["t"]["ms_step"], "value": job_tflops(conv, world, x["t"]["ms_step"]),
+                     "kernel": dom["kernel"], "kernel_ms": dom["ms"], "method_TFLOP/s": dom["TFLOP/s"],
+                     "frac": dom["frac_of_peak"], "executed_frac": dom["executed_frac_of_peak"],
+                     "preprocess_ms": x["t"]["ms_pre"], "flops_convention": conv, "flops_algorithmic": alg,
+                     "dtype": pb.w.dtype}
+        if pb.w.layout == "TND":
+            out[name]["seq_lengths"] = np.diff(pb.cu_seqlens_q).tolist()
+    return out
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -702,8 +891,11 @@ def main():
                      "frac": dom["TFLOP/s"] / peak_tf, "traffic": profile_traffic(w.name, dom["kernel"]),
                      "kernel": dom["kernel"], "peak_kind": f"{peak_kind} bf16 dense (burst)",
                      "algorithmic_flops_per_launch": dom["flops"], "ms_per_launch": dom["ms"],
-                     "flops_per_pair": dom["flops_per_pair"]},
+                     "flops_per_pair": dom["flops_per_pair"],
+                     "executed_frac": dom["executed_frac_of_peak"],
+                     "executed_flops_per_pair": dom["executed_flops_per_pair"]},
         "kernels": stages,
+        "workloads": workloads_table(r, peak_tf, peak_hbm, world),
         "flops_convention": conv, "flops_algorithmic": alg,
         "gpu_launches": (2 if r["merged"] else 3) * args.steps,
         "clocks": r["clocks"],

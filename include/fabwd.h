@@ -210,27 +210,46 @@ fabwd_status fabwd_preprocess_stats(const fabwd_params* p, const float* softmax_
  * FABWD_DQ_AUTO.  Errors as fabwd_workspace_size. */
 fabwd_status fabwd_resolve_dq_mode(const fabwd_params* p, int32_t* mode);
 
+/* Size of the scratch array behind fabwd_run_static_workspace: 64 MiB on every GPU that loads the
+ * library.  A problem fits when its fabwd_workspace_size is at most this. */
+#define FABWD_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+
 /* Allocation-free form of fabwd_preprocess + fabwd_run (the pages have no counterpart; it is a
  * convenience of this library).  For callers that cannot call cudaMalloc when they run the
  * backward: code under a host framework that owns all device memory through its own pool (a
  * foreign allocation can fail or fragment it), or a loop whose rules forbid allocation after
  * start-up.  The caller still allocates and passes the inputs and the outputs dq, dk, dv; the
- * scratch lives in a fixed 64 MiB array inside the library (held on every GPU that loads the
- * library until the process exits).  A problem whose fabwd_workspace_size exceeds 64 MiB is
- * refused with FABWD_ERR_WORKSPACE before anything is enqueued; other argument errors as
- * fabwd_run.  Nothing is allocated: no cudaMalloc or cudaFree is called.  The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress, which may load the module)
- * and caches it; make that first call before any stream capture.  Every call on a device shares
- * the one array, which keeps the last call's contents (the kernels clear what must start at
- * zero): calls whose work overlaps on the GPU (other streams, other threads) race and must be
- * serialised by the caller.  Device-side status (FABWD_DEV_*) is not reported by this call. */
+ * scratch lives in a fixed FABWD_STATIC_WORKSPACE_BYTES array inside the library (held on every
+ * GPU that loads the library until the process exits).  A problem whose fabwd_workspace_size
+ * exceeds it is refused with FABWD_ERR_WORKSPACE before anything is enqueued; other argument
+ * errors as fabwd_run.  Nothing is allocated: no cudaMalloc or cudaFree is called.  The first
+ * call on each device looks up the array's device address (cudaGetSymbolAddress, which may load
+ * the module) and caches it; make that first call before any stream capture.  Every call on a
+ * device shares the one array, which keeps the last call's contents (the kernels clear what must
+ * start at zero): calls whose work overlaps on the GPU (other streams, other threads) race and
+ * must be serialised by the caller.  The device-side status (FABWD_DEV_*) of the last call is
+ * read with fabwd_static_workspace_status. */
 fabwd_status fabwd_run_static_workspace(const fabwd_params* p, void* stream);
+
+/* Host only: FABWD_STATIC_WORKSPACE_BYTES, the capacity of fabwd_run_static_workspace's array. */
+size_t fabwd_static_workspace_capacity(void);
+
+/* fabwd_read_device_status for fabwd_run_static_workspace: a synchronising read, on `stream`, of
+ * the status word the last such call on the current device left in the library's array (bad
+ * cu_seqlens, a bounded wait that gave up).  Returns as fabwd_read_device_status; CUDA when the
+ * array's address cannot be looked up. */
+fabwd_status fabwd_static_workspace_status(void* stream, uint32_t* device_status);
 
 /* Static description of a status code. */
 const char* fabwd_status_string(fabwd_status s);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int fabwd_version(void);
+
+/* Diagnostic: the binary architecture of the library's kernels as the CUDA runtime loaded them on
+ * the current device (cudaFuncGetAttributes' binaryVersion, major * 10 + minor: 103 for the
+ * sm_103a build).  Errors: NULLPTR, CUDA (no device, or no kernel image for it). */
+fabwd_status fabwd_kernel_binary_version(int32_t* version);
 
 #ifdef __cplusplus
 }

@@ -6,6 +6,8 @@ The reference side calls only the fp64 oracle; the GPU side calls only the libfa
 from __future__ import annotations
 
 import dataclasses
+import multiprocessing
+import os
 from typing import Optional
 
 import numpy as np
@@ -108,3 +110,82 @@ def assert_close(name, got, ref, rel=REL_L2, mabs=MAX_ABS_FRAC):
     assert e["rel_l2"] <= rel, f"{name}: relative L2 {e['rel_l2']:.3g} > {rel}"
     assert e["max_abs_frac"] <= mabs, f"{name}: max-abs/max|ref| {e['max_abs_frac']:.3g} > {mabs}"
     return e
+
+
+# ---------------------------------------------------------------------------------------------
+# full-size references: the oracle per (batch, kv-head group) in a pool of spawned processes
+# ---------------------------------------------------------------------------------------------
+
+
+def _group_slices(pb: inputs.Problem):
+    """Independent pieces of a problem: (batch or all sequences, kv-head n2 with its G q-heads).
+    Each piece is a whole problem of its own (N1 = G, N2 = 1), so the oracle's result on it is
+    exactly the matching slice of its result on the whole problem."""
+    w = pb.w
+    G = w.N1 // w.N2
+    out = []
+    for n2 in range(w.N2):
+        hq, hk = slice(n2 * G, (n2 + 1) * G), slice(n2, n2 + 1)
+        if w.layout == "TND":
+            out.append(((slice(None), hq), (slice(None), hk), (hq, slice(None))))
+        elif w.layout == "BSND":
+            for b in range(w.B):
+                bb = slice(b, b + 1)
+                out.append(((bb, slice(None), hq), (bb, slice(None), hk), (bb, hq, slice(None))))
+        else:
+            for b in range(w.B):
+                bb = slice(b, b + 1)
+                out.append(((bb, hq), (bb, hk), (bb, hq, slice(None))))
+    return out
+
+
+def _piece(args):
+    """Worker: oracle forward (Y rounded to the io dtype, lse to fp32) then oracle backward."""
+    q, k, v, dy, dtype, kw = args
+    y, lse = orc.forward(q, k, v, **kw)
+    y_io = inputs.to_f64(inputs.round_io(y, dtype))
+    lse32 = lse.astype(np.float32)
+    dq, dk, dv, sf = orc.backward(q, k, v, dy, y_io, lse32.astype(np.float64), **kw)
+    return y_io, lse32, dq, dk, dv, sf
+
+
+def _pool_size(bytes_per_worker: int) -> int:
+    n = min(os.cpu_count() or 1, 16)
+    try:
+        with open("/proc/meminfo") as f:
+            avail = next(int(line.split()[1]) * 1024 for line in f if line.startswith("MemAvailable"))
+        n = min(n, max(1, int(0.6 * avail // max(bytes_per_worker, 1))))
+    except (OSError, StopIteration, ValueError):
+        n = min(n, 4)
+    return max(1, n)
+
+
+def full_reference_parallel(pb: inputs.Problem) -> Reference:
+    """full_reference of a large problem: the same oracle calls, one per independent piece
+    (_group_slices), in a pool of spawned processes with single-threaded BLAS each."""
+    w = pb.w
+    q, k, v, dy = (inputs.to_f64(t) for t in (pb.q, pb.k, pb.v, pb.dout))
+    kw = oracle_kwargs(pb)
+    pieces = _group_slices(pb)
+    jobs = [(q[sq], k[sk], v[sk], dy[sq], w.dtype, kw) for sq, sk, _ in pieces]
+    # per worker: a handful of S1 x S2 fp64 matrices of the longest sequence
+    per = 6 * 8 * max(pb.S1, 1) * max(pb.S2, 1) + (1 << 28)
+    threads = {k_: os.environ.get(k_) for k_ in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    os.environ.update({k_: "1" for k_ in threads})
+    try:
+        with multiprocessing.get_context("spawn").Pool(_pool_size(per)) as pool:
+            res = pool.map(_piece, jobs, chunksize=1)
+    finally:
+        for k_, v_ in threads.items():
+            if v_ is None:
+                os.environ.pop(k_, None)
+            else:
+                os.environ[k_] = v_
+    y = np.zeros(dy.shape)
+    lse = np.zeros((w.N1, pb.T1) if w.layout == "TND" else (w.B, w.N1, pb.S1), np.float32)
+    dq, dk, dv, sf = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape), np.zeros(lse.shape)
+    for (sq, sk, sl), (y_, l_, dq_, dk_, dv_, sf_) in zip(pieces, res):
+        y[sq], lse[sl], dq[sq], dk[sk], dv[sk], sf[sl] = y_, l_, dq_, dk_, dv_, sf_
+    ref = Reference(attn_out=inputs.round_io(y, w.dtype), lse=torch.from_numpy(lse))
+    ref.dq, ref.dk, ref.dv, ref.sfmg = dq, dk, dv, sf
+    return ref

@@ -23,15 +23,23 @@ def test_stage_table_splits_the_five_products():
     assert set(sep) == {"preprocess", "dkdv", "dq"} and set(ato) == {"preprocess", "main", "convert"}
     # the fused kernel forms the method's five products once
     assert ato["main"]["flops"] == pytest.approx(alg)
-    # dK/dV kernel: S, dP, dV, dK; dQ kernel: S, dP again and dQ
+    # dK/dV kernel: S, dP, dV, dK; dQ kernel: S, dP again and dQ, credited with dQ only
     assert sep["dkdv"]["flops_per_pair"] == 2 * (2 * w.D + 2 * w.Dv)
-    assert sep["dq"]["flops_per_pair"] == 2 * (2 * w.D + w.Dv)
-    assert sep["dkdv"]["flops"] + sep["dq"]["flops"] == pytest.approx(alg * (4 * w.D + 3 * w.Dv) / (3 * w.D + 2 * w.Dv))
+    assert sep["dq"]["flops_per_pair"] == 2 * w.D
+    assert sep["dq"]["executed_flops_per_pair"] == 2 * (2 * w.D + w.Dv)
+    assert sep["dkdv"]["flops"] + sep["dq"]["flops"] == pytest.approx(alg)
+    assert sep["dkdv"]["executed_flops"] + sep["dq"]["executed_flops"] == \
+        pytest.approx(alg * (4 * w.D + 3 * w.Dv) / (3 * w.D + 2 * w.Dv))
     assert sep["dkdv"]["TFLOP/s"] == pytest.approx(sep["dkdv"]["flops"] / 0.2e-3 / 1e12)
-    # one grid for both separate-mode kernels: their products together
+    # one grid for both separate-mode kernels: the method's work once (frac), every product formed
+    # (executed_frac) beside it
     mer = bench.stage_table(pb, _r(True, merged=True), 1000.0, 5000.0)
     assert set(mer) == {"preprocess", "backward"}
-    assert mer["backward"]["flops"] == pytest.approx(sep["dkdv"]["flops"] + sep["dq"]["flops"])
+    assert mer["backward"]["flops"] == pytest.approx(alg)
+    assert mer["backward"]["flops_per_pair"] == 2 * (3 * w.D + 2 * w.Dv)
+    assert mer["backward"]["executed_flops"] == pytest.approx(sep["dkdv"]["executed_flops"] + sep["dq"]["executed_flops"])
+    assert mer["backward"]["frac_of_peak"] == pytest.approx(alg / 0.2e-3 / 1e12 / 1000.0)
+    assert mer["backward"]["executed_frac_of_peak"] > mer["backward"]["frac_of_peak"]
     # the separate mode has no fp32 accumulator to zero
     assert ato["preprocess"]["bytes"] - sep["preprocess"]["bytes"] == 4 * 1000
     assert ato["convert"]["bytes"] == 6 * 1000
@@ -56,3 +64,23 @@ def test_clock_summary_keeps_the_timed_window():
     assert s["samples"] == 2 and s["samples_in_timed_region"] == 2
     assert s["sm_mhz"] == pytest.approx(1750) and s["sm_max_mhz"] == 2070
     assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_nvml_sampler_summary_keeps_the_timed_window():
+    import bench
+    c = bench.NvmlClocks.__new__(bench.NvmlClocks)
+    c.available, c.sm_max, c.period_s = True, 2070, 0.002
+    base = time.time()
+    c.samples = [(base - 1, 900, 100.0, 0x1), (base + 0.1, 2070, 900.0, 0x0), (base + 0.2, 2000, 1000.0, 0x4),
+                 (base + 2, 1000, 50.0, 0x0)]
+    c.t0, c.t1 = base, base + 0.5
+    s = c.summary()
+    assert s["samples_in_timed_region"] == 2 and s["sm_mhz"] == pytest.approx(2035)
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1000.0 and s["source"] == "nvml"
+
+
+def test_nvml_sampler_without_a_gpu_is_unavailable():
+    import bench
+    c = bench.NvmlClocks("00000000:00:00.0")
+    if not c.available:
+        assert c.summary() is None

@@ -2,8 +2,8 @@
 
 Tolerances (the measurement statement's): per output tensor relative L2 <= 1e-2 and
 max-abs <= 2e-2 · max|ref|; the fp32 sfmg within 1e-5 relative.  Small cases compare every
-element and span several 128-row tiles with ragged tails; the full-size workloads compare
-sampled output rows that the oracle evaluates one at a time.
+element and span several 128-row tiles with ragged tails; the five full-size workloads compare
+every element too, with the oracle run per kv-head group in a pool of processes.
 """
 import math
 
@@ -300,70 +300,27 @@ def test_timeout_injection_returns_status_and_context_survives():
 
 
 # ---------------------------------------------------------------------------------------------
-# full-size workloads, sampled outputs
+# full-size workloads, every element
 # ---------------------------------------------------------------------------------------------
 
 
-def _sample_rows(rng, seqs, heads, edges, n):
-    out = set()
-    for s, L in seqs:
-        if L == 0:
-            continue
-        for h in (0, heads - 1):
-            for i in edges:
-                if 0 <= i < L:
-                    out.add((s, h, i))
-                if 0 <= L - 1 - i < L:
-                    out.add((s, h, L - 1 - i))
-    nonempty = [(s, L) for s, L in seqs if L > 0]
-    while len(out) < n and nonempty:
-        s, L = nonempty[rng.integers(len(nonempty))]
-        out.add((s, int(rng.integers(heads)), int(rng.integers(L))))
-    return sorted(out)
+FULL = [(name, "auto") for name in ("mha_s128_d64", "causal_b2_s2048_d128", "gqa_causal_s4096_d128",
+                                    "varlen_window_fp16_d128", "causal_s8192_d192_dv128")]
+FULL.append(("causal_b2_s2048_d128", "atomic"))
 
 
-FULL = ["mha_s128_d64", "causal_b2_s2048_d128", "gqa_causal_s4096_d128", "varlen_window_fp16_d128",
-        "causal_s8192_d192_dv128"]
-
-
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
+@pytest.mark.parametrize("name,dq_mode", FULL, ids=[f"{n}-{m}" for n, m in FULL])
+def test_full_size_elementwise(name, dq_mode, parity_report):
+    # The workload at its measured size, in the launch configuration the bench times (the
+    # library's default dQ mode, plus the atomic mode once): every element of dq, dk, dv and every
+    # sfmg row against the fp64 oracle, computed per kv-head group in a pool of processes.
     w = W[name]
     pb = inputs.make_problem(w)
-    ref = tl.forward_inputs(pb)
-    dq, dk, dv, sf = tl.run_gpu(pb, ref)  # the library's default dQ mode, as the bench runs it
-    kw = tl.oracle_kwargs(pb)
-    if w.layout == "TND":
-        seq_q = list(enumerate(np.diff(pb.cu_seqlens_q).tolist()))
-        seq_k = list(enumerate(np.diff(pb.cu_seqlens_kv).tolist()))
-    else:
-        seq_q = [(b, pb.S1) for b in range(w.B)]
-        seq_k = [(b, pb.S2) for b in range(w.B)]
-    rng = np.random.default_rng(5)
-    edges = [0, 1, 63, 64, 127, 128, 129]
-    q_rows = _sample_rows(rng, seq_q, w.N1, edges, 48)
-    kv_rows = _sample_rows(rng, seq_k, w.N2, edges, 48)
-    q, k, v, dy = (inputs.to_f64(t) for t in (pb.q, pb.k, pb.v, pb.dout))
-    gq, gk, gv = orc.backward_sampled(q, k, v, dy, inputs.to_f64(ref.attn_out), ref.lse.numpy().astype(np.float64),
-                                      q_rows=q_rows, kv_rows=kv_rows, **kw)
-
-    def pick(t, rows, cu):
-        x = inputs.to_f64(t)
-        if w.layout == "TND":
-            return np.stack([x[cu[s] + i, n] for s, n, i in rows])
-        return np.stack([x[s, i, n] for s, n, i in rows])
-
-    tl.assert_close("dq (sampled)", pick(dq, q_rows, pb.cu_seqlens_q), np.stack(gq))
-    tl.assert_close("dk (sampled)", pick(dk, kv_rows, pb.cu_seqlens_kv), np.stack(gk))
-    tl.assert_close("dv (sampled)", pick(dv, kv_rows, pb.cu_seqlens_kv), np.stack(gv))
-    # sfmg of every row: the oracle's rowsum(dY ⊙ Y) per head
-    y = inputs.to_f64(ref.attn_out)
-    if w.layout == "TND":
-        want = np.stack([orc._sfmg(dy[:, n], y[:, n]) for n in range(w.N1)])
-    else:
-        want = np.stack([np.stack([orc._sfmg(dy[b, :, n], y[b, :, n]) for n in range(w.N1)]) for b in range(w.B)])
-    e = tl.errors(sf, want)
-    assert e["rel_l2"] <= tl.SFMG_REL
+    ref = tl.full_reference_parallel(pb)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref, dq_mode=dq_mode)
+    errs = check_all(pb, ref, dq, dk, dv, sf)
+    errs["sfmg"] = tl.errors(sf, ref.sfmg)
+    parity_report(f"{name} [{dq_mode}]", errs)
 
 
 def test_unbuilt_head_dim_pair_is_unsupported():
