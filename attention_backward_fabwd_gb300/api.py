@@ -56,7 +56,7 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 def make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, *, cu_seqlens_q=None, cu_seqlens_kv=None,
                 softmax_scale=0.0, mask_mode=0, win_left=-1, win_right=-1, max_seqlen_q=-1, max_seqlen_kv=-1,
-                layout="BSND", dq_mode="auto") -> F.fabwd_params:
+                layout="BSND", dq_mode="auto", seqused_q=None, seqused_kv=None, sinks=None) -> F.fabwd_params:
     """Fill fabwd_params from tensors (shapes give B, S1, S2, N1, N2, D, Dv, T1, T2)."""
     if layout not in _LAYOUTS:
         raise ValueError(f"layout must be one of {sorted(_LAYOUTS)}, got {layout!r}")
@@ -95,10 +95,11 @@ def make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, *, cu_seqlens_
     p.win_left, p.win_right = int(win_left), int(win_right)
     p.dq_mode = dq_mode_value(dq_mode)
     p.dq, p.dk, p.dv = _ptr(dq), _ptr(dk), _ptr(dv)
+    p.seqused_q, p.seqused_kv, p.sinks = _ptr(seqused_q), _ptr(seqused_kv), _ptr(sinks)
     return p
 
 
-def _check_tensors(q, k, v, dout, attn_out, stats, cu_q, cu_kv):
+def _check_tensors(q, k, v, dout, attn_out, stats, cu_q, cu_kv, seqused=(), sinks=None, B=None, N1=None):
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("libfabwd runs on CUDA tensors only")
@@ -115,6 +116,24 @@ def _check_tensors(q, k, v, dout, attn_out, stats, cu_q, cu_kv):
     for name, t in (("cu_seqlens_q", cu_q), ("cu_seqlens_kv", cu_kv)):
         if t is not None and t.dtype != torch.int32:
             raise TypeError(f"{name} must be int32")
+    for name, t in seqused:
+        if t is None:
+            continue
+        if t.dtype != torch.int32 or t.device != dev:
+            raise TypeError(f"{name} must be an int32 tensor on {dev} ([FAG] §2.1)")
+        if B is not None and t.numel() != B:
+            raise ValueError(f"{name} needs one entry per sequence ({B}), got {t.numel()}")
+    if sinks is not None:
+        if sinks.dtype != torch.float32 or sinks.device != dev:
+            raise TypeError(f"sinks must be a float32 tensor on {dev} ([FAG] §2.1)")
+        if N1 is not None and sinks.numel() != N1:
+            raise ValueError(f"sinks needs one logit per q-head ({N1}), got {sinks.numel()}")
+
+
+def _batch_and_heads(q, layout, cu_q):
+    if layout == "TND":
+        return (cu_q.numel() - 1 if cu_q is not None else None), q.shape[1]
+    return q.shape[0], (q.shape[2] if layout == "BSND" else q.shape[1])
 
 
 def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_seqlens_kv=None, seqused_q=None,
@@ -124,9 +143,13 @@ def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_
                     check_status=False, return_workspace=False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Gradients (dq, dk, dv) of attention from the saved attn_out and softmax_lse.
 
-    Arguments follow [FAG] §4.2.  Differences: seqused_q/kv, sinks and attn_mask are not
-    supported (their semantics are not stated) and raise; `metadata` (an Ascend core-split plan)
-    is accepted and ignored, the GPU schedule is derived from the shapes.  The three layouts must
+    Arguments follow [FAG] §4.2.  The page states no semantics for seqused_q/kv and sinks; the
+    readings taken (include/fabwd.h, fabwd_params): seqused_q[b] / seqused_kv[b] (int32, one per
+    sequence) are the used query / key rows of sequence b, the rest are padding (zero gradient,
+    finite values required); sinks (fp32, one logit per q-head) are already inside softmax_lse,
+    so dq, dk and dv do not depend on them and they are only checked.  attn_mask (its layout is not
+    stated) raises; `metadata` (an Ascend core-split plan) is accepted and ignored, the GPU
+    schedule is derived from the shapes.  The three layouts must
     agree ([FAG] §4.6).  Non-contiguous inputs are made contiguous.  With TND and
     max_seqlen_* = -1 the lengths are read from cu_seqlens on the host (a synchronisation).
     dq_mode selects how dQ is formed: 'atomic' (fp32 reduce-adds into a workspace accumulator, then
@@ -137,8 +160,8 @@ def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_
     (..., 8) layout of the LaserAttentionGrad and FusedFloydAttentionGrad pages).
     check_status=True synchronises and raises if the kernels reported a device-side problem.
     """
-    if seqused_q is not None or seqused_kv is not None or sinks is not None or attn_mask is not None:
-        raise NotImplementedError("seqused_q/seqused_kv/sinks/attn_mask are not supported")
+    if attn_mask is not None:
+        raise NotImplementedError("attn_mask is not supported (its layout and meaning are not stated)")
     if not (layout_q == layout_kv == layout_out):
         raise ValueError("layout_q, layout_kv and layout_out must be the same ([FAG] §4.6)")
     use_stats = softmax_max is not None or softmax_sum is not None
@@ -161,12 +184,16 @@ def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_
     if cu_seqlens_kv is not None:
         cu_seqlens_kv = cu_seqlens_kv.contiguous()
     stats = [("softmax_max", softmax_max), ("softmax_sum", softmax_sum)] if use_stats else [("softmax_lse", softmax_lse)]
-    _check_tensors(q, k, v, dout, attn_out, stats, cu_seqlens_q, cu_seqlens_kv)
+    seqused_q, seqused_kv, sinks = (None if t is None else t.contiguous() for t in (seqused_q, seqused_kv, sinks))
+    B, N1 = _batch_and_heads(q, layout_q, cu_seqlens_q)
+    _check_tensors(q, k, v, dout, attn_out, stats, cu_seqlens_q, cu_seqlens_kv,
+                   (("seqused_q", seqused_q), ("seqused_kv", seqused_kv)), sinks, B, N1)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     p = make_params(q, k, v, dout, attn_out, softmax_lse, dq, dk, dv, cu_seqlens_q=cu_seqlens_q,
                     cu_seqlens_kv=cu_seqlens_kv, softmax_scale=softmax_scale, mask_mode=mask_mode,
                     win_left=win_left, win_right=win_right, max_seqlen_q=max_seqlen_q,
-                    max_seqlen_kv=max_seqlen_kv, layout=layout_q, dq_mode=dq_mode)
+                    max_seqlen_kv=max_seqlen_kv, layout=layout_q, dq_mode=dq_mode, seqused_q=seqused_q,
+                    seqused_kv=seqused_kv, sinks=sinks)
     nbytes = F.fabwd_workspace_size(p)
     ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
     stream = torch.cuda.current_stream(q.device).cuda_stream
@@ -187,26 +214,33 @@ def flash_attn_grad(q, k, v, dout, attn_out, softmax_lse, cu_seqlens_q=None, cu_
 
 def flash_attn_forward(q, k, v, cu_seqlens_q=None, cu_seqlens_kv=None, softmax_scale=0.0, mask_mode=0,
                        win_left=-1, win_right=-1, max_seqlen_q=-1, max_seqlen_kv=-1, layout="BSND",
-                       check_status=False) -> Tuple[torch.Tensor, torch.Tensor]:
+                       check_status=False, seqused_q=None, seqused_kv=None,
+                       sinks=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """(attn_out, softmax_lse) of the attention whose gradients flash_attn_grad computes, on the GPU.
 
     The forward of [FAG] §一 with the same masks, GQA map, layouts and scale rule as the backward:
     attn_out has q's layout with Dv, softmax_lse is fp32 [B][N1][S1] (BSND/BNSD) or [N1][T1] (TND),
     natural-log; a row with no visible key gets attn_out = 0 and softmax_lse = +inf.  The pair is
-    what flash_attn_grad takes as attn_out and softmax_lse.
+    what flash_attn_grad takes as attn_out and softmax_lse.  seqused_q / seqused_kv and sinks as
+    for flash_attn_grad: rows past seqused get attn_out = 0 and softmax_lse = +inf, and a sink
+    logit joins every row's normaliser (softmax_lse = ln(exp(sink) + Σ exp(S))).
     """
     q, k, v = (t.contiguous() for t in (q, k, v))
     if cu_seqlens_q is not None:
         cu_seqlens_q = cu_seqlens_q.contiguous()
     if cu_seqlens_kv is not None:
         cu_seqlens_kv = cu_seqlens_kv.contiguous()
-    _check_tensors(q, k, v, q, q, [], cu_seqlens_q, cu_seqlens_kv)
+    seqused_q, seqused_kv, sinks = (None if t is None else t.contiguous() for t in (seqused_q, seqused_kv, sinks))
+    B, N1 = _batch_and_heads(q, layout, cu_seqlens_q)
+    _check_tensors(q, k, v, q, q, [], cu_seqlens_q, cu_seqlens_kv, (("seqused_q", seqused_q), ("seqused_kv", seqused_kv)),
+                   sinks, B, N1)
     out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
     # make_params reads the shapes from q, k, v; dout/attn_out/lse/dq/dk/dv are unused by the forward.
     p = make_params(q, k, v, None, out, None, None, None, None, cu_seqlens_q=cu_seqlens_q,
                     cu_seqlens_kv=cu_seqlens_kv, softmax_scale=softmax_scale, mask_mode=mask_mode,
                     win_left=win_left, win_right=win_right, max_seqlen_q=max_seqlen_q,
-                    max_seqlen_kv=max_seqlen_kv, layout=layout)
+                    max_seqlen_kv=max_seqlen_kv, layout=layout, seqused_q=seqused_q, seqused_kv=seqused_kv,
+                    sinks=sinks)
     if layout == "TND":
         lse = torch.empty((p.N1, p.T1), dtype=torch.float32, device=q.device)
     else:

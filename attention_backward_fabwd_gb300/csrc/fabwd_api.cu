@@ -97,7 +97,37 @@ fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
     if (k_nonempty && (!aligned16(p->k) || !aligned16(p->v) || !aligned16(p->dk) || !aligned16(p->dv)))
       return FABWD_ERR_INVALID;
   }
+  // the optional inputs: int32 / fp32 device arrays
+  if ((reinterpret_cast<uintptr_t>(p->seqused_q) | reinterpret_cast<uintptr_t>(p->seqused_kv) |
+       reinterpret_cast<uintptr_t>(p->sinks)) & 3u)
+    return FABWD_ERR_INVALID;
   return FABWD_OK;
+}
+
+// Output rows past seqused (both entry points set them; the kernels never write them).
+cudaError_t unused_rows(const fabwd_params* p, void* dq, float* lse_out, bool fwd, cudaStream_t st) {
+  if (!p->seqused_q && (fwd || !p->seqused_kv)) return cudaSuccess;
+  UnusedArgs u;
+  u.layout = p->layout;
+  u.B = (int)p->B;
+  u.N1 = (int)p->N1;
+  u.N2 = (int)p->N2;
+  u.D = (int)p->D;
+  u.Dv = (int)p->Dv;
+  u.S1 = p->S1;
+  u.S2 = p->S2;
+  u.T1 = p->T1;
+  u.T2 = p->T2;
+  u.cu_q = p->cu_seqlens_q;
+  u.cu_kv = p->cu_seqlens_kv;
+  u.used_q = p->seqused_q;
+  u.used_kv = p->seqused_kv;
+  u.dq = dq;
+  u.dk = p->dk;
+  u.dv = p->dv;
+  u.lse_out = lse_out;
+  u.fwd = fwd;
+  return launch_unused_rows(u, st);
 }
 
 fabwd_status check_ws(const Plan& pl, const void* ws, size_t ws_bytes) {
@@ -240,12 +270,16 @@ fabwd_status preprocess_impl(const fabwd_params* p, const float* smax, const flo
   a.stat_stride = stat_stride;
   a.cu_q = p->cu_seqlens_q;
   a.cu_kv = p->cu_seqlens_kv;
+  a.used_q = p->seqused_q;
+  a.used_kv = p->seqused_kv;
   a.lse2 = reinterpret_cast<float*>(w + pl.off_lse2);
   a.sfmg = reinterpret_cast<float*>(w + pl.off_sfmg);
   a.dq_acc = reinterpret_cast<float*>(w + pl.off_dqacc);
   a.dq_acc_elems = pl.dq_elems;
   a.status = reinterpret_cast<unsigned*>(w + pl.off_status);
-  cudaError_t e = launch_preprocess(a, p->dtype == FABWD_FP16, static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_preprocess(a, p->dtype == FABWD_FP16, st);
+  if (e == cudaSuccess) e = unused_rows(p, p->dq, nullptr, false, st);
   return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
 }
 }  // namespace
@@ -265,6 +299,9 @@ MainArgs main_args(const fabwd_params* p, const Plan& pl, uint8_t* w, int inject
   a.T2 = p->T2;
   a.cu_q = p->cu_seqlens_q;
   a.cu_kv = p->cu_seqlens_kv;
+  a.used_q = p->seqused_q;
+  a.used_kv = p->seqused_kv;
+  a.sinks = nullptr;  // the backward does not read sinks (they are inside softmax_lse)
   a.mask_mode = p->mask_mode;
   a.win_left = (int)p->win_left;
   a.win_right = (int)p->win_right;
@@ -414,12 +451,14 @@ fabwd_status fabwd_forward(const fabwd_params* p, void* attn_out, float* softmax
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_zero(ws, 256, st) != cudaSuccess) return FABWD_ERR_CUDA;  // status word
   if (pl.rowsQ == 0) return FABWD_OK;
-  if (!any_pair(&f, pl)) {  // no key at all: Y = 0, lse = +inf
+  if (!any_pair(&f, pl)) {  // no key at all: Y = 0, lse = +inf (or the row's sink logit)
     const long long rows = pl.rowsQ * p->N1;
-    return launch_zero(attn_out, rows * p->Dv * 2, st) == cudaSuccess &&
-                   launch_fill_f32(softmax_lse, rows, INFINITY, st) == cudaSuccess
-               ? FABWD_OK
-               : FABWD_ERR_CUDA;
+    const bool ok = launch_zero(attn_out, rows * p->Dv * 2, st) == cudaSuccess &&
+                    (p->sinks ? launch_fill_lse_sinks(softmax_lse, p->sinks, p->layout == FABWD_TND ? p->T1 : p->S1,
+                                                      (int)p->N1, rows, p->layout == FABWD_TND, st)
+                              : launch_fill_f32(softmax_lse, rows, INFINITY, st)) == cudaSuccess &&
+                    unused_rows(p, attn_out, softmax_lse, true, st) == cudaSuccess;
+    return ok ? FABWD_OK : FABWD_ERR_CUDA;
   }
   const int inject = g_inject_timeout;
   g_inject_timeout = 0;
@@ -427,10 +466,12 @@ fabwd_status fabwd_forward(const fabwd_params* p, void* attn_out, float* softmax
   a.status = static_cast<unsigned*>(ws);
   a.dq = attn_out;
   a.lse_out = softmax_lse;
+  a.sinks = p->sinks;
   MainMaps maps;
   if (!make_maps(&f, &maps, 128, p->D > 128 ? 64 : 128)) return FABWD_ERR_CUDA;
-  const cudaError_t e = p->dtype == FABWD_FP16 ? launch_fwd_fp16(a, maps, (int)p->D, (int)p->Dv, st)
-                                               : launch_fwd_bf16(a, maps, (int)p->D, (int)p->Dv, st);
+  cudaError_t e = p->dtype == FABWD_FP16 ? launch_fwd_fp16(a, maps, (int)p->D, (int)p->Dv, st)
+                                         : launch_fwd_bf16(a, maps, (int)p->D, (int)p->Dv, st);
+  if (e == cudaSuccess) e = unused_rows(p, attn_out, softmax_lse, true, st);
   return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
 }
 

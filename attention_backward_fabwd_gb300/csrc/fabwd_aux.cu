@@ -19,18 +19,27 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <bool FP16, int DV, bool SMALL>
 __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    unsigned st = 0;
-    if (a.layout == kTND) {
-      if (a.cu_q[0] != 0 || a.cu_kv[0] != 0) st |= FABWD_DEV_BAD_SEQLENS;
-      for (int s = 0; s < a.B; ++s) {
-        const long long lq = (long long)a.cu_q[s + 1] - a.cu_q[s];
-        const long long lk = (long long)a.cu_kv[s + 1] - a.cu_kv[s];
-        if (lq < 0 || lq > a.S1 || lk < 0 || lk > a.S2) st |= FABWD_DEV_BAD_SEQLENS;
-      }
-      if (a.cu_q[a.B] != a.T1 || a.cu_kv[a.B] != a.T2) st |= FABWD_DEV_BAD_SEQLENS;
+  if (blockIdx.x == 0) {
+    // block 0 clears the status word, then its threads check the sequences in parallel
+    if (threadIdx.x == 0) {
+      unsigned st = 0;
+      if (a.layout == kTND && (a.cu_q[0] != 0 || a.cu_kv[0] != 0 || a.cu_q[a.B] != a.T1 || a.cu_kv[a.B] != a.T2))
+        st |= FABWD_DEV_BAD_SEQLENS;
+      *a.status = st;
     }
-    *a.status = st;
+    __syncthreads();
+    unsigned bad = 0;
+    for (int s = threadIdx.x; s < a.B; s += blockDim.x) {
+      long long lq = a.S1, lk = a.S2;
+      if (a.layout == kTND) {
+        lq = (long long)a.cu_q[s + 1] - a.cu_q[s];
+        lk = (long long)a.cu_kv[s + 1] - a.cu_kv[s];
+        if (lq < 0 || lq > a.S1 || lk < 0 || lk > a.S2) bad = 1;
+      }
+      if (a.used_q && (a.used_q[s] < 0 || a.used_q[s] > lq)) bad = 1;
+      if (a.used_kv && (a.used_kv[s] < 0 || a.used_kv[s] > lk)) bad = 1;
+    }
+    if (bad) atomicOr(a.status, FABWD_DEV_BAD_SEQLENS);
   }
 
   // Grid-stride over rows (b, i, n1) in the layout's row order over the padded length S1p; each
@@ -89,6 +98,10 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
         L1 = L1 < 0 ? 0 : (L1 > a.S1 ? a.S1 : L1);
         if (q0 + L1 > a.T1) L1 = a.T1 - q0 < 0 ? 0 : a.T1 - q0;
       }
+      if (act[u] && a.used_q) {  // rows past seqused are padding: lse2 = +inf, sfmg = 0
+        const long long us = a.used_q[b];
+        L1 = us < 0 ? 0 : (us < L1 ? us : L1);
+      }
       // rows past the sequence's last 128-row block are never read by the backward kernels
       if (tnd && i >= ((L1 + 127) / 128) * 128) act[u] = false;
       val[u] = act[u] && i < L1;
@@ -136,6 +149,62 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
     z[x] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Sequence s holding global token t: the last s with cu[s] <= t (cu non-decreasing from 0).
+__device__ __forceinline__ int seq_of(const int* cu, int B, long long t) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// One thread per (row, head) of the q side, then of the kv side; a row past its sequence's
+// seqused gets its output row written (see UnusedArgs).  Rows are located like the main kernels
+// do; with inconsistent cu_seqlens or seqused nothing is written (the preprocess reports it).
+__global__ void __launch_bounds__(256) unused_rows_kernel(UnusedArgs a) {
+  const bool tnd = a.layout == kTND;
+  const long long rq = tnd ? a.T1 : (long long)a.B * a.S1, rk = tnd ? a.T2 : (long long)a.B * a.S2;
+  const long long nq = a.used_q ? rq * a.N1 : 0, nk = a.used_kv && !a.fwd ? rk * a.N2 : 0;
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < nq + nk;
+       x += (long long)gridDim.x * blockDim.x) {
+    const bool qside = x < nq;
+    const long long u = qside ? x : x - nq;
+    const int N = qside ? a.N1 : a.N2;
+    const long long S = qside ? a.S1 : a.S2;
+    const int* cu = qside ? a.cu_q : a.cu_kv;
+    const int* used = qside ? a.used_q : a.used_kv;
+    int b, n;
+    long long i, t;
+    if (a.layout == kBNSD) {
+      i = u % S;
+      n = (int)((u / S) % N);
+      b = (int)(u / (S * N));
+    } else {
+      n = (int)(u % N);
+      t = u / N;
+      b = tnd ? seq_of(cu, a.B, t) : (int)(t / S);
+      i = tnd ? t - cu[b] : t % S;
+    }
+    const long long span = tnd ? (long long)cu[b + 1] - cu[b] : S;
+    const int us = used[b];
+    if (i < 0 || i >= span || us < 0 || us > span || i < us) continue;
+    const long long r = row_index(a.layout, b, tnd ? cu[b] + i : i, n, N, S);
+    if (qside) {
+      const int dim = a.fwd ? a.Dv : a.D;
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + r * dim);
+      for (int c = 0; c < dim / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (a.fwd) a.lse_out[tnd ? (long long)n * a.T1 + cu[b] + i : ((long long)b * a.N1 + n) * a.S1 + i] = INFINITY;
+    } else {
+      uint4* k = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dk) + r * a.D);
+      uint4* v = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dv) + r * a.Dv);
+      for (int c = 0; c < a.D / 8; ++c) k[c] = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < a.Dv / 8; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
 template <bool FP16>
 __global__ void __launch_bounds__(256) convert_kernel(ConvArgs a) {
   const long long n8 = a.elems / 8;
@@ -160,6 +229,12 @@ __global__ void __launch_bounds__(256) zero_kernel(uint4* p, long long n16) {
 __global__ void __launch_bounds__(256) fill_f32_kernel(float* p, long long n, float v) {
   for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (long long)gridDim.x * blockDim.x)
     p[x] = v;
+}
+
+__global__ void __launch_bounds__(256) fill_lse_sinks_kernel(float* lse, const float* sinks, long long S, int N1,
+                                                              long long n, bool tnd) {
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (long long)gridDim.x * blockDim.x)
+    lse[x] = sinks[tnd ? x / S : (x / S) % N1];
 }
 
 int grid_for(long long work_items, int per_block) {
@@ -194,6 +269,13 @@ cudaError_t launch_fill_f32(float* p, long long n, float v, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_fill_lse_sinks(float* lse, const float* sinks, long long S, int N1, long long n, bool tnd,
+                                  cudaStream_t st) {
+  if (n <= 0 || S <= 0) return cudaSuccess;
+  fill_lse_sinks_kernel<<<grid_for(n, 256), 256, 0, st>>>(lse, sinks, S, N1, n, tnd);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st) {
   const long long rows = (long long)a.B * a.N1 * a.S1p;
   const long long work = rows * (a.Dv / 8) > a.dq_acc_elems / 4 ? rows * (a.Dv / 8) : a.dq_acc_elems / 4;
@@ -208,6 +290,15 @@ cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st) {
   } else {
     return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unused_rows(const UnusedArgs& a, cudaStream_t st) {
+  const bool tnd = a.layout == kTND;
+  const long long rq = tnd ? a.T1 : (long long)a.B * a.S1, rk = tnd ? a.T2 : (long long)a.B * a.S2;
+  const long long n = (a.used_q ? rq * a.N1 : 0) + (a.used_kv && !a.fwd ? rk * a.N2 : 0);
+  if (n <= 0) return cudaSuccess;
+  unused_rows_kernel<<<grid_for(n, 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -326,9 +326,22 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
       tc_fence_after();
       const float mo = st_m[(1 - g) * BM + row], lo_ = st_l[(1 - g) * BM + row];
       const float m0 = g == 0 ? m : mo, m1 = g == 0 ? mo : m, l0 = g == 0 ? l : lo_, l1 = g == 0 ? lo_ : l;
-      const float M = fmaxf(m0, m1);
-      const float c0 = m0 == -INFINITY ? 0.f : ex2(m0 - M), c1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
-      const float L = l0 * c0 + l1 * c1;
+      float M = fmaxf(m0, m1);
+      float c0 = m0 == -INFINITY ? 0.f : ex2(m0 - M), c1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+      float L = l0 * c0 + l1 * c1;
+      if (a.sinks) {
+        // the q-head's sink logit joins the normaliser with no value: in the log2 units of M,
+        // L·2^(M − M') + 2^(sink·log2e − M') with M' = max(M, sink·log2e)
+        const float ks = a.sinks[n1] * 1.4426950408889634f;
+        const float Mn = fmaxf(M, ks);
+        if (Mn != -INFINITY) {
+          const float cs = M == -INFINITY ? 0.f : ex2(M - Mn);
+          c0 *= cs;
+          c1 *= cs;
+          L = L * cs + ex2(ks - Mn);
+          M = Mn;
+        }
+      }
       const float inv = L > 0.f ? 1.f / L : 0.f;
       const long long qrow = row_index(a.layout, b, (long long)(tnd ? sq.q0 : 0) + (i_valid ? ir : 0), n1, a.N1, a.S1);
       uint16_t* y = static_cast<uint16_t*>(a.dq) + qrow * DV;

@@ -53,6 +53,8 @@ struct PreArgs {
   long long stat_stride;
   const int* cu_q;
   const int* cu_kv;
+  const int* used_q;         // seqused_q / seqused_kv (B entries) or null
+  const int* used_kv;
   float* lse2;               // [B][N1][S1p]: lse * log2(e), +inf on padding rows
   float* sfmg;               // [B][N1][S1p]: rowsum(dout * attn_out), 0 on padding rows
   float* dq_acc;             // fp32, q's shape with D
@@ -73,6 +75,9 @@ struct MainArgs {
   long long T1, T2;
   const int* cu_q;
   const int* cu_kv;
+  const int* used_q;         // seqused_q / seqused_kv (B entries) or null: used rows per sequence
+  const int* used_kv;
+  const float* sinks;        // forward only: per-q-head sink logits or null
   int mask_mode, win_left, win_right;
   float scale, scale_log2;   // scale and scale * log2(e)
   int S1p;
@@ -88,16 +93,38 @@ struct MainArgs {
   int inject_timeout;
 };
 
+// Rows outside every sequence's used rows (seqused): their output rows are set here.  Backward:
+// dq rows (D elements) and dk / dv rows (D / Dv) to 0.  Forward (fwd = true): attn_out rows
+// (held in dq, Dv elements) to 0 and their lse entries to +inf.
+struct UnusedArgs {
+  int layout, B, N1, N2, D, Dv;
+  long long S1, S2, T1, T2;
+  const int* cu_q;
+  const int* cu_kv;
+  const int* used_q;
+  const int* used_kv;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* lse_out;
+  bool fwd;
+};
+
 struct MainMaps {
   CUtensorMap q, k, v, dout;
 };
 
 cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st);
 cudaError_t launch_convert(const ConvArgs& a, bool fp16, cudaStream_t st);
+// Writes the output rows of UnusedArgs; nothing when neither seqused pointer is given.
+cudaError_t launch_unused_rows(const UnusedArgs& a, cudaStream_t st);
 // Zero `bytes` (a multiple of 16) at a 16-byte-aligned device address.
 cudaError_t launch_zero(void* p, long long bytes, cudaStream_t st);
 // Set n fp32 values to v.
 cudaError_t launch_fill_f32(float* p, long long n, float v, cudaStream_t st);
+// Set the n entries of an lse array ([B][N1][S] or, tnd, [N1][S]) to their q-head's sink logit.
+cudaError_t launch_fill_lse_sinks(float* lse, const float* sinks, long long S, int N1, long long n, bool tnd,
+                                  cudaStream_t st);
 // Return cudaErrorInvalidValue when no kernel is built for (D, Dv).  fused: the kv-stationary
 // kernel also reduces dQ into the fp32 accumulator; otherwise it writes dK, dV only.
 cudaError_t launch_main_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, bool fused,

@@ -81,6 +81,9 @@ struct SeqRange {
   int q0, L1, k0, L2;
 };
 
+// Rows of sequence (TND) or batch row b: its first q row and key row, and the lengths that take
+// part, after seqused when given.  False when cu_seqlens or seqused are inconsistent (the
+// preprocess kernel reports that; the caller touches nothing).
 __device__ __forceinline__ bool seq_range(const MainArgs& a, int b, SeqRange& r) {
   if (a.layout == kTND) {
     const long long qa = a.cu_q[b], qb = a.cu_q[b + 1], ka = a.cu_kv[b], kb = a.cu_kv[b + 1];
@@ -95,6 +98,16 @@ __device__ __forceinline__ bool seq_range(const MainArgs& a, int b, SeqRange& r)
     r.L1 = a.S1;
     r.k0 = 0;
     r.L2 = a.S2;
+  }
+  if (a.used_q) {
+    const int u = a.used_q[b];
+    if (u < 0 || u > r.L1) return false;
+    r.L1 = u;
+  }
+  if (a.used_kv) {
+    const int u = a.used_kv[b];
+    if (u < 0 || u > r.L2) return false;
+    r.L2 = u;
   }
   return true;
 }

@@ -40,6 +40,7 @@ class fabwd_params(ctypes.Structure):
         ("mask_mode", ctypes.c_int32), ("dq_mode", ctypes.c_int32),
         ("win_left", ctypes.c_int64), ("win_right", ctypes.c_int64),
         ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("seqused_q", ctypes.c_void_p), ("seqused_kv", ctypes.c_void_p), ("sinks", ctypes.c_void_p),
     ]
 
 

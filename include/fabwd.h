@@ -85,7 +85,8 @@ typedef enum { FABWD_DQ_AUTO = 0, FABWD_DQ_ATOMIC = 1, FABWD_DQ_SEPARATE = 2 } f
 
 /* Device status bits (fabwd_read_device_status). */
 #define FABWD_DEV_TIMEOUT 0x1u     /* a bounded mbarrier wait gave up; outputs are not valid */
-#define FABWD_DEV_BAD_SEQLENS 0x2u /* cu_seqlens not non-decreasing from 0, or beyond T / max */
+#define FABWD_DEV_BAD_SEQLENS 0x2u /* cu_seqlens not non-decreasing from 0, or beyond T / max, or a
+                                      seqused entry outside [0, the sequence's length] */
 #define FABWD_DEV_INTERNAL 0x4u    /* a kernel found its shared memory misaligned; nothing computed */
 
 typedef struct {
@@ -116,6 +117,24 @@ typedef struct {
   void* dq;
   void* dk;
   void* dv;
+  /* Optional inputs of [FAG] §2.1 and §4.2; NULL when not given.  The page states no semantics
+   * for them; this library's readings:
+   *   seqused_q, seqused_kv: device int32, B entries, 4-byte aligned.  Sequence (TND) or batch
+   *     row (BSND/BNSD) b takes part with only its first seqused_q[b] query rows and first
+   *     seqused_kv[b] key rows, 0 <= seqused <= its length (else FABWD_DEV_BAD_SEQLENS); the
+   *     masks align to the used lengths.  The other rows see nothing and are seen by nothing:
+   *     their dq / dk / dv rows are written as 0 (fabwd_forward: attn_out 0, softmax_lse +inf).
+   *     They are read as parts of 128-row tiles and multiplied by zero, so they must hold finite
+   *     values.  Either pointer may be given alone.
+   *   sinks: device fp32, N1 entries, 4-byte aligned: one logit per q-head that joins every
+   *     row's softmax normaliser with no value vector, lse_i = ln(exp(sinks[n1]) + Σ_j exp(S_ij)).
+   *     fabwd_forward includes it in attn_out and softmax_lse.  The backward entry points do not
+   *     read it: given that softmax_lse, dq, dk and dv follow §一's formulas unchanged
+   *     (rowsum(dY ⊙ Y) still equals Σ_j P_ij dP_ij over the real keys), and the operator has no
+   *     sink gradient among its outputs ([FAG] §2.2). */
+  const int32_t* seqused_q;
+  const int32_t* seqused_kv;
+  const float* sinks;
 } fabwd_params;
 
 /* Host only.  Validates p (the same checks as fabwd_run, pointers excepted) and returns in

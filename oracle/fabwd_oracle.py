@@ -23,6 +23,14 @@ Readings where the page is silent (each is listed with its reasoning in the desi
 * a row with no visible key has lse = +inf, P = 0, Y = 0 and dQ = 0; a key seen by no row
   gets dK = dV = 0.
 * the GQA head map is q-head n1 -> kv-head n1 // (N1 / N2).
+* seqused_q / seqused_kv (the optional int32 inputs of §2.1 and §4.2): sequence b takes part
+  with only its first seqused_q[b] query rows and first seqused_kv[b] key rows; the masks are
+  aligned to those used lengths; the remaining rows see nothing and are seen by nothing, so
+  their lse is +inf, Y = 0 and their gradient rows are 0.
+* sinks (the optional fp32 input of §2.1 and §4.2): one logit per q-head that joins every row's
+  softmax normaliser and carries no value, lse_i = ln(exp(sink) + Σ_j exp(S_ij)).  It enters
+  the forward only; the backward from that lse is §一's unchanged, because sfmg = rowsum(dY⊙Y)
+  still equals Σ_j P_ij dP_ij over the real keys.
 
 The backward consumes exactly what the GPU path consumes: Y (attn_out) as given, lse as given
 (fp32 values promoted to fp64).  Everything is fp64 numpy; matrix products use numpy matmul as
@@ -114,19 +122,25 @@ def _dk(ds: np.ndarray, q: np.ndarray, scale: float) -> np.ndarray:
     return scale * (ds.T @ q)
 
 
-def forward_head(q, k, v, scale: float, ok) -> Tuple[np.ndarray, np.ndarray]:
+def forward_head(q, k, v, scale: float, ok, sink: Optional[float] = None) -> Tuple[np.ndarray, np.ndarray]:
     """[FAG §一] one head's forward: returns (Y [S1, Dv], lse [S1]).
 
     lse_i = log Σ_{visible j} exp(S_ij) (natural log), evaluated with the row maximum taken out;
-    rows with no visible key get lse = +inf and Y = 0.
+    rows with no visible key get lse = +inf and Y = 0.  With a sink logit (reading of the
+    optional `sinks` input, see the module notes) the normaliser gains exp(sink): lse_i =
+    log(exp(sink) + Σ_{visible j} exp(S_ij)), so a row with no visible key gets lse = sink.
     """
     s = _scores(q, k, scale)
     s = np.where(ok, s, -np.inf)
     m = s.max(axis=1) if s.shape[1] else np.full(s.shape[0], -np.inf)
+    if sink is not None:
+        m = np.maximum(m, float(sink))
     has = np.isfinite(m)
     m0 = np.where(has, m, 0.0)
     with np.errstate(invalid="ignore"):
         total = np.exp(s - m0[:, None]).sum(axis=1)
+    if sink is not None:
+        total = total + np.exp(float(sink) - m0)
     lse = np.where(has, m0 + np.log(np.where(has, total, 1.0)), np.inf)
     p = _probs(np.where(ok, s, 0.0), lse, ok)
     return p @ v, lse
@@ -206,18 +220,32 @@ class _View:
         return self.x.shape[2] if self.layout == "BSND" else self.x.shape[1]
 
 
-def _seq_list(layout, q, k, cu_q, cu_kv):
+def _seq_list(layout, q, k, cu_q, cu_kv, seqused_q=None, seqused_kv=None):
+    """(batch or None, q rows, kv rows) of every sequence; with seqused_q / seqused_kv only the
+    first seqused[b] rows of sequence b take part (reading of the optional inputs of [FAG §2.1])."""
     if layout == "TND":
-        return _tnd_sequences(cu_q, cu_kv)
-    if cu_q is not None or cu_kv is not None:
+        seqs = _tnd_sequences(cu_q, cu_kv)
+    elif cu_q is not None or cu_kv is not None:
         raise ValueError("cu_seqlens are only taken with the TND layout")
-    if layout == "BSND":
-        S1, S2 = q.shape[1], k.shape[1]
+    elif layout == "BSND":
+        seqs = [(b, slice(0, q.shape[1]), slice(0, k.shape[1])) for b in range(q.shape[0])]
     elif layout == "BNSD":
-        S1, S2 = q.shape[2], k.shape[2]
+        seqs = [(b, slice(0, q.shape[2]), slice(0, k.shape[2])) for b in range(q.shape[0])]
     else:
         raise ValueError(f"unknown layout {layout!r}")
-    return [(b, slice(0, S1), slice(0, S2)) for b in range(q.shape[0])]
+
+    def used(rows: slice, u, s) -> slice:
+        if u is None:
+            return rows
+        n = int(np.asarray(u)[s])
+        if not 0 <= n <= rows.stop - rows.start:
+            raise ValueError(f"seqused[{s}] = {n} is outside [0, {rows.stop - rows.start}]")
+        return slice(rows.start, rows.start + n)
+
+    for u in (seqused_q, seqused_kv):
+        if u is not None and len(np.asarray(u)) != len(seqs):
+            raise ValueError("seqused needs one entry per sequence")
+    return [(b, used(rq, seqused_q, s), used(rk, seqused_kv, s)) for s, (b, rq, rk) in enumerate(seqs)]
 
 
 def _lse_get(layout, lse, b, rows, n):
@@ -253,35 +281,42 @@ def _group(N1: int, N2: int) -> int:
 
 
 def forward(q, k, v, *, layout="BSND", cu_seqlens_q=None, cu_seqlens_kv=None, softmax_scale=0.0,
-            mask_mode=0, win_left=-1, win_right=-1):
+            mask_mode=0, win_left=-1, win_right=-1, seqused_q=None, seqused_kv=None, sinks=None):
     """Forward over all sequences and heads: returns (Y in q's layout with Dv, lse fp64).
 
-    lse has shape (B, N1, S1) for BSND/BNSD and (N1, T1) for TND [FAG §4.6].
+    lse has shape (B, N1, S1) for BSND/BNSD and (N1, T1) for TND [FAG §4.6]; rows outside every
+    sequence's used rows keep lse = +inf and Y = 0.  sinks: None or one logit per q-head.
     """
     Q, K, V = _View(layout, q), _View(layout, k), _View(layout, v)
     N1, N2 = Q.heads, K.heads
     G = _group(N1, N2)
     D, Dv = q.shape[-1], v.shape[-1]
     scale = resolve_scale(softmax_scale, D)
+    if sinks is not None and len(np.asarray(sinks)) != N1:
+        raise ValueError("sinks needs one logit per q-head")
     y = np.zeros(q.shape[:-1] + (Dv,), dtype=np.float64)
     Y = _View(layout, y)
-    lse = np.zeros(_lse_shape(layout, q, N1), dtype=np.float64)
-    for b, rq, rk in _seq_list(layout, q, k, cu_seqlens_q, cu_seqlens_kv):
+    lse = np.full(_lse_shape(layout, q, N1), np.inf, dtype=np.float64)
+    for b, rq, rk in _seq_list(layout, q, k, cu_seqlens_q, cu_seqlens_kv, seqused_q, seqused_kv):
         S1, S2 = rq.stop - rq.start, rk.stop - rk.start
         ok = visible(S1, S2, mask_mode, win_left, win_right)
         for n1 in range(N1):
             n2 = _kv_head(n1, N1, N2)
-            yh, lh = forward_head(Q.get(b, rq, n1), K.get(b, rk, n2), V.get(b, rk, n2), scale, ok)
+            sink = None if sinks is None else float(np.asarray(sinks)[n1])
+            yh, lh = forward_head(Q.get(b, rq, n1), K.get(b, rk, n2), V.get(b, rk, n2), scale, ok, sink)
             Y.add(b, rq, n1, yh)
             _lse_set(layout, lse, b, rq, n1, lh)
     return y, lse
 
 
 def backward(q, k, v, dout, attn_out, softmax_lse, *, layout="BSND", cu_seqlens_q=None,
-             cu_seqlens_kv=None, softmax_scale=0.0, mask_mode=0, win_left=-1, win_right=-1):
+             cu_seqlens_kv=None, softmax_scale=0.0, mask_mode=0, win_left=-1, win_right=-1, seqused_q=None,
+             seqused_kv=None):
     """Backward over all sequences and heads: returns (dq, dk, dv, sfmg), fp64.
 
-    dk/dv of kv-head n2 sum the contributions of its G q-heads; sfmg has lse's shape.
+    dk/dv of kv-head n2 sum the contributions of its G q-heads; sfmg has lse's shape.  Rows
+    outside every sequence's used rows get zero gradients (and sfmg 0).  There is no sinks
+    argument: under the reading in the module notes the sink is already inside softmax_lse.
     """
     Q, K, V = _View(layout, q), _View(layout, k), _View(layout, v)
     dY, Yv = _View(layout, dout), _View(layout, attn_out)
@@ -291,7 +326,7 @@ def backward(q, k, v, dout, attn_out, softmax_lse, *, layout="BSND", cu_seqlens_
     dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
     dQ, dK, dV = _View(layout, dq), _View(layout, dk), _View(layout, dv)
     sfmg = np.zeros(_lse_shape(layout, q, N1))
-    for b, rq, rk in _seq_list(layout, q, k, cu_seqlens_q, cu_seqlens_kv):
+    for b, rq, rk in _seq_list(layout, q, k, cu_seqlens_q, cu_seqlens_kv, seqused_q, seqused_kv):
         S1, S2 = rq.stop - rq.start, rk.stop - rk.start
         ok = visible(S1, S2, mask_mode, win_left, win_right)
         for n1 in range(N1):
@@ -314,7 +349,8 @@ def backward(q, k, v, dout, attn_out, softmax_lse, *, layout="BSND", cu_seqlens_
 
 def backward_sampled(q, k, v, dout, attn_out, softmax_lse, *, q_rows: Sequence[Tuple[int, int, int]],
                      kv_rows: Sequence[Tuple[int, int, int]], layout="BSND", cu_seqlens_q=None,
-                     cu_seqlens_kv=None, softmax_scale=0.0, mask_mode=0, win_left=-1, win_right=-1):
+                     cu_seqlens_kv=None, softmax_scale=0.0, mask_mode=0, win_left=-1, win_right=-1,
+                     seqused_q=None, seqused_kv=None):
     """dQ rows and dK/dV rows for chosen outputs, one at a time.
 
     q_rows: (sequence or batch s, q-head n1, row i within the sequence) -> dq row [D]
@@ -327,7 +363,7 @@ def backward_sampled(q, k, v, dout, attn_out, softmax_lse, *, q_rows: Sequence[T
     N1, N2 = Q.heads, K.heads
     G = _group(N1, N2)
     scale = resolve_scale(softmax_scale, q.shape[-1])
-    seqs = _seq_list(layout, q, k, cu_seqlens_q, cu_seqlens_kv)
+    seqs = _seq_list(layout, q, k, cu_seqlens_q, cu_seqlens_kv, seqused_q, seqused_kv)
     out_q: List[np.ndarray] = []
     for s, n1, i in q_rows:
         b, rq, rk = seqs[s]

@@ -136,6 +136,34 @@ def test_null_and_workspace_codes(lib):
     assert F.lib().fabwd_read_device_status(None, 256, None, ctypes.byref(v)) == F.FABWD_ERR_NULLPTR
 
 
+def test_optional_inputs_validation(lib):
+    # seqused_q / seqused_kv (int32) and sinks (fp32) must be 4-byte aligned; refused on the host
+    _, need = ws_size(base_params())
+    for name in ("seqused_q", "seqused_kv", "sinks"):
+        p = base_params(**{name: 0x20002})
+        assert ws_size(p)[0] == F.FABWD_ERR_INVALID, name
+        for fn in ("fabwd_preprocess", "fabwd_run"):
+            assert F.call_status(fn, p, 0x100000, need, None) == F.FABWD_ERR_INVALID, (fn, name)
+        assert ws_size(base_params(**{name: 0x20004}))[0] == F.FABWD_OK
+    # the sizes do not change with them
+    assert ws_size(base_params(seqused_q=0x20000, seqused_kv=0x20000, sinks=0x20000)) == ws_size(base_params())
+
+
+def test_params_struct_matches_the_header():
+    # the ctypes mirror ends with the optional inputs, in the header's order
+    import re
+    with open(F.HEADER) as f:
+        text = f.read()
+    body = text[text.index("typedef struct {"):text.index("} fabwd_params;")]
+    fields = []
+    for line in body.splitlines():
+        line = line.split("/*")[0].strip()
+        m = re.match(r"^(?:const\s+)?\w+\*?\s+\*?(.+);$", line)
+        if m:
+            fields += [x.strip().lstrip("*") for x in m.group(1).split(",")]
+    assert fields == [f[0] for f in F.fabwd_params._fields_], fields
+
+
 def test_statistics_preprocess_validation(lib):
     # every case below is refused on the host, before anything is enqueued
     p = base_params(softmax_lse=None)   # softmax_lse is not used by this entry point
@@ -240,7 +268,7 @@ def test_make_params_shapes_bsnd_tnd_bnsd():
 def test_api_rejects_unsupported_inputs():
     t = torch.zeros(1, 4, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(NotImplementedError):
-        api.flash_attn_grad(t, t, t, t, t, torch.zeros(1, 1, 4), sinks=torch.zeros(1))
+        api.flash_attn_grad(t, t, t, t, t, torch.zeros(1, 1, 4), attn_mask=torch.zeros(1, dtype=torch.int8))
     with pytest.raises(ValueError):
         api.flash_attn_grad(t, t, t, t, t, torch.zeros(1, 1, 4), layout_kv="TND")
     with pytest.raises(ValueError):   # CPU tensors: the library runs on CUDA only, no fallback

@@ -453,3 +453,205 @@ def test_stats_adapter_does_not_need_the_true_maximum():
     for c in (0.0, -5.0, 7.5):
         np.testing.assert_allclose(orc.lse_from_stats(np.full(6, c), np.exp(s - c).sum(axis=1)), ref, rtol=1e-13)
     assert orc.lse_from_stats(np.array([-np.inf]), np.array([0.0]))[0] == np.inf
+
+
+# ---------------------------------------------------------------------------------------------
+# seqused_q / seqused_kv and sinks (optional inputs of [FAG] §2.1 / §4.2; readings in the oracle)
+# ---------------------------------------------------------------------------------------------
+
+SEQUSED_CASES = [
+    # name, layout, B, S1, S2, N1, N2, kw, cu_q, cu_kv, seqused_q, seqused_kv
+    ("tnd_causal_used", "TND", 3, 0, 0, 4, 2, dict(mask_mode=1), np.array([0, 4, 9, 12]), np.array([0, 5, 9, 13]),
+     np.array([3, 5, 0]), np.array([4, 2, 3])),
+    ("tnd_window_q_only", "TND", 2, 0, 0, 2, 1, dict(mask_mode=1, win_left=1, win_right=0), np.array([0, 5, 9]),
+     np.array([0, 5, 9]), np.array([4, 2]), None),
+    ("bsnd_dense_used", "BSND", 2, 5, 6, 2, 2, dict(), None, None, np.array([5, 2]), np.array([3, 6])),
+    ("bnsd_band_kv_only", "BNSD", 2, 5, 5, 2, 1, dict(mask_mode=2, win_left=1, win_right=2), None, None, None,
+     np.array([4, 1])),
+]
+
+
+def seqused_inputs(case, seed=13):
+    name, layout, B, S1, S2, N1, N2, kw, cu_q, cu_kv, uq, ukv = case
+    q, k, v, dy = make(layout, B, S1, S2, N1, N2, 3, 2, seed, cu_q, cu_kv)
+    kw = dict(kw, layout=layout, seqused_q=uq, seqused_kv=ukv)
+    if layout == "TND":
+        kw.update(cu_seqlens_q=cu_q, cu_seqlens_kv=cu_kv)
+    return q, k, v, dy, kw
+
+
+@pytest.mark.parametrize("case", SEQUSED_CASES, ids=[c[0] for c in SEQUSED_CASES])
+def test_seqused_finite_differences(case):
+    # rows past seqused take no part in L, so their derivative (and the oracle's gradient) is 0
+    q, k, v, dy, kw = seqused_inputs(case)
+    assert fd_check(q, k, v, dy, kw)
+
+
+def _truncate(x, layout, cu, used, axis_rows):
+    """The used rows of every sequence only: TND rows re-packed, BSND/BNSD per batch."""
+    if layout == "TND":
+        return np.concatenate([x[cu[s]:cu[s] + used[s]] for s in range(len(cu) - 1)])
+    return [np.take(x[b:b + 1], np.arange(used[b]), axis=axis_rows) for b in range(x.shape[0])]
+
+
+@pytest.mark.parametrize("case", SEQUSED_CASES, ids=[c[0] for c in SEQUSED_CASES])
+def test_seqused_equals_truncated_sequences(case):
+    name, layout, B, S1, S2, N1, N2, mk, cu_q, cu_kv, uq, ukv = case
+    q, k, v, dy, kw = seqused_inputs(case, seed=17)
+    y, lse = orc.forward(q, k, v, **kw)
+    dq, dk, dv, sf = orc.backward(q, k, v, dy, y, lse, **kw)
+    nq = len(cu_q) - 1 if layout == "TND" else B
+    uq_ = uq if uq is not None else (np.diff(cu_q) if layout == "TND" else np.full(B, S1))
+    uk_ = ukv if ukv is not None else (np.diff(cu_kv) if layout == "TND" else np.full(B, S2))
+    ax = 1 if layout == "BSND" else 2
+    if layout == "TND":
+        tq, tdy, ty = (_truncate(x, layout, cu_q, uq_, 0) for x in (q, dy, y))
+        tk, tv = (_truncate(x, layout, cu_kv, uk_, 0) for x in (k, v))
+        tcq, tck = np.concatenate([[0], np.cumsum(uq_)]), np.concatenate([[0], np.cumsum(uk_)])
+        tkw = dict(mk, layout="TND", cu_seqlens_q=tcq, cu_seqlens_kv=tck)
+        y2, lse2 = orc.forward(tq, tk, tv, **tkw)
+        g = orc.backward(tq, tk, tv, tdy, y2, lse2, **tkw)
+        np.testing.assert_allclose(_truncate(y, layout, cu_q, uq_, 0), y2, rtol=1e-14, atol=1e-15)
+        for got, want, cu, u in ((dq, g[0], cu_q, uq_), (dk, g[1], cu_kv, uk_), (dv, g[2], cu_kv, uk_)):
+            np.testing.assert_allclose(_truncate(got, layout, cu, u, 0), want, rtol=1e-13, atol=1e-14)
+        # and the rows past seqused: zero gradients, +inf lse, Y = 0
+        for s in range(nq):
+            assert (dq[cu_q[s] + uq_[s]:cu_q[s + 1]] == 0).all() and (y[cu_q[s] + uq_[s]:cu_q[s + 1]] == 0).all()
+            assert np.isinf(lse[:, cu_q[s] + uq_[s]:cu_q[s + 1]]).all()
+            assert (dk[cu_kv[s] + uk_[s]:cu_kv[s + 1]] == 0).all() and (dv[cu_kv[s] + uk_[s]:cu_kv[s + 1]] == 0).all()
+    else:
+        for b in range(B):
+            pick = lambda x, n: np.take(x[b:b + 1], np.arange(n), axis=ax)
+            tq, tdy, tk, tv = pick(q, uq_[b]), pick(dy, uq_[b]), pick(k, uk_[b]), pick(v, uk_[b])
+            tkw = dict(mk, layout=layout)
+            y2, lse2 = orc.forward(tq, tk, tv, **tkw)
+            g = orc.backward(tq, tk, tv, tdy, y2, lse2, **tkw)
+            np.testing.assert_allclose(pick(y, uq_[b]), y2, rtol=1e-14, atol=1e-15)
+            np.testing.assert_allclose(pick(dq, uq_[b]), g[0], rtol=1e-13, atol=1e-14)
+            np.testing.assert_allclose(pick(dk, uk_[b]), g[1], rtol=1e-13, atol=1e-14)
+            np.testing.assert_allclose(pick(dv, uk_[b]), g[2], rtol=1e-13, atol=1e-14)
+            rest_q = lambda x: np.take(x[b:b + 1], np.arange(uq_[b], S1), axis=ax)
+            rest_k = lambda x: np.take(x[b:b + 1], np.arange(uk_[b], S2), axis=ax)
+            assert (rest_q(dq) == 0).all() and (rest_k(dk) == 0).all() and (rest_k(dv) == 0).all()
+
+
+def test_seqused_rows_are_never_read():
+    # anything in the rows past seqused (here NaN) leaves the used rows' results unchanged
+    case = SEQUSED_CASES[0]
+    q, k, v, dy, kw = seqused_inputs(case, seed=19)
+    y, lse = orc.forward(q, k, v, **kw)
+    ref = orc.backward(q, k, v, dy, y, lse, **kw)
+    cu_q, cu_kv, uq, ukv = case[8], case[9], case[10], case[11]
+    for s in range(len(cu_q) - 1):
+        for x in (q, dy, y):
+            x[cu_q[s] + uq[s]:cu_q[s + 1]] = np.nan
+        for x in (k, v):
+            x[cu_kv[s] + ukv[s]:cu_kv[s + 1]] = np.nan
+    got = orc.backward(q, k, v, dy, y, lse, **kw)
+    for a, b in zip(got, ref):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_seqused_bounds_are_checked():
+    q, k, v, dy, kw = seqused_inputs(SEQUSED_CASES[0])
+    with pytest.raises(ValueError):
+        orc.forward(q, k, v, **dict(kw, seqused_q=np.array([5, 5, 0])))   # 5 > span 4 of sequence 0
+    with pytest.raises(ValueError):
+        orc.forward(q, k, v, **dict(kw, seqused_kv=np.array([1, 1])))     # one entry per sequence
+
+
+def test_planted_seqused_alignment_is_caught(monkeypatch):
+    # a mask aligned to the stored span instead of the used lengths must fail the truncation pin
+    real = orc._seq_list
+
+    def span_aligned(layout, q, k, cu_q, cu_kv, seqused_q=None, seqused_kv=None):
+        return real(layout, q, k, cu_q, cu_kv, None, None) if seqused_q is not None or seqused_kv is not None \
+            else real(layout, q, k, cu_q, cu_kv)
+
+    monkeypatch.setattr(orc, "_seq_list", span_aligned)
+    with pytest.raises(AssertionError):
+        test_seqused_equals_truncated_sequences(SEQUSED_CASES[0])
+
+
+SINK_CASES = [
+    ("dense", "BSND", 1, 5, 5, 2, 2, 3, 2, dict(), None, None),
+    ("causal_gqa_empty_rows", "BSND", 1, 6, 4, 4, 2, 3, 2, dict(mask_mode=1), None, None),
+    ("tnd_window", "TND", 2, 0, 0, 2, 2, 2, 3, dict(mask_mode=1, win_left=1, win_right=0),
+     np.array([0, 5, 8]), np.array([0, 5, 8])),
+]
+
+
+def _sinks(N1, seed):
+    return np.random.default_rng(seed).standard_normal(N1) * 1.5
+
+
+@pytest.mark.parametrize("case", SINK_CASES, ids=[c[0] for c in SINK_CASES])
+def test_sinks_finite_differences(case):
+    # L = Σ dY ⊙ Y(q, k, v) of the forward with sink logits; the backward from that forward's lse
+    # must be its derivative (the sink only enters through lse)
+    q, k, v, dy, kw = case_inputs(case, seed=23)
+    N1 = case[5]
+    sk = _sinks(N1, 3)
+    y, lse = orc.forward(q, k, v, sinks=sk, **kw)
+    dq, dk, dv, _ = orc.backward(q, k, v, dy, y, lse, **kw)
+    f = lambda: float((dy * orc.forward(q, k, v, sinks=sk, **kw)[0]).sum())
+    for got, x in ((dq, q), (dk, k), (dv, v)):
+        ref = fd_grad(x, f)
+        np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-6 * max(1.0, np.abs(ref).max()))
+
+
+def test_sinks_closed_forms():
+    # one query, one key: lse = ln(e^s + e^sink), Y = v·σ(s − sink); a row with no key: lse = sink
+    rng = np.random.default_rng(29)
+    q, k, v = rng.normal(size=(1, 1, 1, 3)), rng.normal(size=(1, 1, 1, 3)), rng.normal(size=(1, 1, 1, 2))
+    sink = np.array([0.4])
+    y, lse = orc.forward(q, k, v, softmax_scale=0.5, sinks=sink)
+    s = 0.5 * float(q[0, 0, 0] @ k[0, 0, 0])
+    assert lse[0, 0, 0] == pytest.approx(math.log(math.exp(s) + math.exp(0.4)), rel=1e-14)
+    np.testing.assert_allclose(y[0, 0, 0], v[0, 0, 0] / (1 + math.exp(0.4 - s)), rtol=1e-14)
+    q, k, v, dy = make("BSND", 1, 6, 4, 2, 2, 3, 3, 33)
+    y, lse = orc.forward(q, k, v, mask_mode=1, sinks=np.array([0.25, -1.0]))
+    assert (lse[0, 0, :2] == 0.25).all() and (lse[0, 1, :2] == -1.0).all() and (y[0, :2] == 0).all()
+
+
+def test_sinks_take_the_missing_row_mass_and_vanish_at_minus_infinity():
+    q, k, v, dy = make("BSND", 1, 7, 7, 2, 1, 3, 2, 37)
+    sk = np.array([0.3, 2.0])
+    y, lse = orc.forward(q, k, v, mask_mode=1, sinks=sk)
+    ok = orc.visible(7, 7, 1, -1, -1)
+    for n in range(2):
+        p = orc._probs(orc._scores(q[0, :, n], k[0, :, 0], 1 / math.sqrt(3)), lse[0, n], ok)
+        np.testing.assert_allclose(p.sum(1), 1 - np.exp(sk[n] - lse[0, n]), rtol=1e-13)
+    y0, lse0 = orc.forward(q, k, v, mask_mode=1)
+    y1, lse1 = orc.forward(q, k, v, mask_mode=1, sinks=np.array([-np.inf, -np.inf]))
+    np.testing.assert_array_equal(lse1, lse0)
+    np.testing.assert_array_equal(y1, y0)
+
+
+def test_sinks_against_torch_autograd():
+    # softmax over [S, sink] with the sink column dropped from P·V, differentiated by torch
+    q, k, v, dy = make("BSND", 1, 6, 8, 2, 1, 4, 3, 41)
+    sk = np.array([0.7, -0.2])
+    ok = orc.visible(6, 8, 1, -1, -1)
+    y, lse = orc.forward(q, k, v, mask_mode=1, sinks=sk)
+    dq, dk, dv, _ = orc.backward(q, k, v, dy, y, lse, mask_mode=1)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    tot = 0
+    for n in range(2):
+        s = tq[0, :, n] @ tk[0, :, 0].T / math.sqrt(4)
+        s = s.masked_fill(~torch.tensor(ok), float("-inf"))
+        full = torch.cat([s, torch.full((6, 1), float(sk[n]), dtype=s.dtype)], dim=1)
+        p = torch.softmax(full, dim=1)[:, :-1]
+        tot = tot + (torch.tensor(dy[0, :, n]) * (p @ tv[0, :, 0])).sum()
+    tot.backward()
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_planted_sink_dropped_from_lse_is_caught(monkeypatch):
+    real = orc.forward_head
+    monkeypatch.setattr(orc, "forward_head", lambda q, k, v, scale, ok, sink=None: real(q, k, v, scale, ok, None)
+                        if sink is None else (real(q, k, v, scale, ok, sink)[0], real(q, k, v, scale, ok, None)[1]))
+    with pytest.raises(AssertionError):
+        test_sinks_finite_differences(SINK_CASES[1])
