@@ -19,6 +19,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <bool FP16, int DV, bool SMALL>
 __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
+  // the backward kernel that follows may start its set-up now; it waits for this grid to finish
+  // before it reads the rows written here
+  griddep_launch_dependents();
   if (blockIdx.x == 0) {
     // block 0 clears the status word, then its threads check the sequences in parallel
     if (threadIdx.x == 0) {
@@ -42,10 +45,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
     if (bad) atomicOr(a.status, FABWD_DEV_BAD_SEQLENS);
   }
 
-  // Grid-stride over rows (b, i, n1) in the layout's row order over the padded length S1p; each
-  // lane group of LPR lanes takes UN rows per iteration, whose dout, attn_out and lse loads are
-  // all issued before the arithmetic.  SMALL: every row index fits 32 bits, so the per-row
-  // index split uses 32-bit division.
+  // Grid-stride over rows (b, n1, i), i over the padded length S1p: the order of the lse, lse2 and
+  // sfmg rows, so that a warp's 4-byte reads and writes of them are contiguous (a row's dout and
+  // attn_out, 2·Dv bytes each, are whole 128-byte lines in any order).  Each lane group of LPR
+  // lanes takes UN rows per iteration, whose dout, attn_out and lse loads are all issued before
+  // the arithmetic.  SMALL: every row index fits 32 bits, so the index split uses 32-bit division.
   constexpr int LPR = DV / 8;    // lanes per row: one 16-byte chunk (8 elements) each
   constexpr int RPW = 32 / LPR;  // rows per warp step
   constexpr int UN = 2;          // row groups per iteration
@@ -54,7 +58,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
   const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, part = lane % LPR;
-  const bool bnsd = a.layout == kBNSD, tnd = a.layout == kTND;
+  const bool tnd = a.layout == kTND;
   for (long long base = gwarp * RPW * UN; base < nrows; base += nwarp * RPW * UN) {
     uint4 x[UN], y[UN];
     float l[UN];
@@ -69,25 +73,14 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
       if (act[u]) {
         if (SMALL) {
           const uint32_t w32 = (uint32_t)w, S1p = (uint32_t)a.S1p, N1 = (uint32_t)a.N1;
-          if (bnsd) {
-            const uint32_t hq = w32 / S1p;
-            i = w32 - hq * S1p;
-            b = (int)(hq / N1);
-            n1 = (int)(hq - (uint32_t)b * N1);
-          } else {
-            const uint32_t tq = w32 / N1;
-            n1 = (int)(w32 - tq * N1);
-            b = (int)(tq / S1p);
-            i = tq - (uint32_t)b * S1p;
-          }
-        } else if (bnsd) {
+          const uint32_t hq = w32 / S1p;
+          i = w32 - hq * S1p;
+          b = (int)(hq / N1);
+          n1 = (int)(hq - (uint32_t)b * N1);
+        } else {
           i = w % a.S1p;
           n1 = (int)((w / a.S1p) % a.N1);
           b = (int)(w / ((long long)a.S1p * a.N1));
-        } else {
-          n1 = (int)(w % a.N1);
-          i = (w / a.N1) % a.S1p;
-          b = (int)(w / ((long long)a.N1 * a.S1p));
         }
       }
       long long q0 = 0, L1 = a.S1;

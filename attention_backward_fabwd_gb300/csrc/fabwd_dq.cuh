@@ -72,6 +72,7 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
   const int i0 = qb * BM;
   if (i0 >= sq.L1) return;
   if ((smem_u32(smem) & 1023u) != 0) {
+    griddep_wait();  // the preprocess clears the status word
     if (tid == 0) atomicOr(a.status, FABWD_DEV_INTERNAL);
     return;
   }
@@ -107,6 +108,10 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tm_holder;
+  // The set-up above (barriers, tensor memory, tensor-map prefetch) overlaps the tail of the
+  // preceding preprocess kernel under programmatic dependent launch; nothing it wrote is read
+  // before this point.
+  griddep_wait();
   if (a.inject_timeout) {
     if (lane == 0) wait_bar(&bars[kDqNever], 0, abort_flag, a);
     __syncwarp();

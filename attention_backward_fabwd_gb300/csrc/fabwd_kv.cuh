@@ -70,6 +70,7 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
   const int j0 = jb * BC;
   if (j0 >= sq.L2) return;
   if ((smem_u32(smem) & 1023u) != 0) {
+    griddep_wait();  // the preprocess clears the status word
     if (tid == 0) atomicOr(a.status, FABWD_DEV_INTERNAL);
     return;
   }
@@ -108,6 +109,10 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tm_holder;
+  // The set-up above (barriers, tensor memory, tensor-map prefetch) overlaps the tail of the
+  // preceding preprocess kernel under programmatic dependent launch; nothing it wrote is read
+  // before this point.
+  griddep_wait();
   if (a.inject_timeout) {
     if (lane == 0) wait_bar(&bars[kKvNever], 0, abort_flag, a);
     __syncwarp();

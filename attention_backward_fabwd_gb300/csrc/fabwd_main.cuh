@@ -164,6 +164,7 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
   const int j0 = jb * BC;
   if (j0 >= sq.L2) return;
   if ((smem_u32(smem) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
+    griddep_wait();  // the preprocess clears the status word
     if (tid == 0) atomicOr(a.status, FABWD_DEV_INTERNAL);
     return;
   }
@@ -210,6 +211,10 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tm_holder;
+  // The set-up above (barriers, tensor memory, tensor-map prefetch) overlaps the tail of the
+  // preceding preprocess kernel under programmatic dependent launch; nothing it wrote is read
+  // before this point.
+  griddep_wait();
 
   if (a.inject_timeout) {  // fault injection for tests: a wait that nothing completes
     if (lane == 0) wait_bar(&bars[kNever], 0, abort_flag, a);

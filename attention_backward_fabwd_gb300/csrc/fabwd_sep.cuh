@@ -12,6 +12,22 @@
 
 namespace fabwd {
 
+// Launch configuration with programmatic stream serialisation: the grid may start while the
+// preceding kernel on the stream (the preprocess) finishes; its CTAs wait for it (griddep_wait)
+// after their set-up.  attr is the caller's, valid for the launch call.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, int threads, uint32_t smem, cudaStream_t st, cudaLaunchAttribute* attr) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -30,9 +46,9 @@ cudaError_t launch_bwd_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, 
   if (cudaError_t e = ensure_smem_limit<fabwd_bwd_kernel<D, DV, FP16>>((int)bytes); e != cudaSuccess) return e;
   const int kv_ctas = n_kv_blocks * a.N2;
   const int dq_ctas = ((a.S1 + DqCfg<D, DV>::BM - 1) / DqCfg<D, DV>::BM) * a.N1;
-  dim3 grid(kv_ctas + dq_ctas, a.B);
-  fabwd_bwd_kernel<D, DV, FP16><<<grid, kMainThreads, bytes, st>>>(m.q, m.k, m.v, m.dout, a, kv_ctas);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(kv_ctas + dq_ctas, a.B), kMainThreads, bytes, st, attr);
+  return cudaLaunchKernelEx(&cfg, fabwd_bwd_kernel<D, DV, FP16>, m.q, m.k, m.v, m.dout, a, kv_ctas);
 }
 
 // D > 128: the two CTA kinds take different tensor-map boxes (the kv-stationary kernel streams
@@ -59,10 +75,10 @@ cudaError_t launch_bwd_wide_t(const MainArgs& a, const MainMaps& mkv, const Main
   if (cudaError_t e = ensure_smem_limit<fabwd_bwd_wide_kernel<D, DV, FP16>>((int)bytes); e != cudaSuccess) return e;
   const int kv_ctas = n_kv_blocks * a.N2;
   const int dq_ctas = ((a.S1 + DqCfg<D, DV>::BM - 1) / DqCfg<D, DV>::BM) * a.N1;
-  dim3 grid(kv_ctas + dq_ctas, a.B);
-  fabwd_bwd_wide_kernel<D, DV, FP16><<<grid, kMainThreads, bytes, st>>>(mkv.q, mkv.k, mkv.v, mkv.dout, mdq.q, mdq.k,
-                                                                        mdq.v, mdq.dout, a, kv_ctas);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(kv_ctas + dq_ctas, a.B), kMainThreads, bytes, st, attr);
+  return cudaLaunchKernelEx(&cfg, fabwd_bwd_wide_kernel<D, DV, FP16>, mkv.q, mkv.k, mkv.v, mkv.dout, mdq.q, mdq.k,
+                            mdq.v, mdq.dout, a, kv_ctas);
 }
 
 }  // namespace fabwd
