@@ -348,11 +348,11 @@ fabwd_status fabwd_run_main(const fabwd_params* p, void* ws, size_t ws_bytes, vo
   const int inject = g_inject_timeout;
   g_inject_timeout = 0;
   if (any_pair(p, pl)) {
-    // separate mode with D <= 128: the dK/dV kernel with 128-row query steps; otherwise the
-    // kv-stationary kernel with 64-row steps (which also reduces dQ in atomic mode)
-    const bool kv128 = pl.separate && p->D <= 128;
+    // separate mode: the dK/dV kernel (128-row query steps up to D = 128, 64-row at D = 192);
+    // atomic mode: the fused kv-stationary kernel with 64-row steps, which also reduces dQ
+    const bool kv128 = pl.separate;
     MainMaps maps;
-    if (!make_maps(p, &maps, kv128 ? 128 : kBlockQ, kBlockKV)) return FABWD_ERR_CUDA;
+    if (!make_maps(p, &maps, pl.separate && p->D <= 128 ? 128 : kBlockQ, kBlockKV)) return FABWD_ERR_CUDA;
     const MainArgs a = main_args(p, pl, static_cast<uint8_t*>(ws), inject);
     const int n_kv_blocks = (int)((p->S2 + kBlockKV - 1) / kBlockKV);
     const bool fp16 = p->dtype == FABWD_FP16;

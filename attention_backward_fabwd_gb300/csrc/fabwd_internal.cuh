@@ -132,8 +132,8 @@ cudaError_t launch_main_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv
 cudaError_t launch_main_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, bool fused,
                              cudaStream_t st);
 cudaError_t launch_dq_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
-// dK/dV-only kernel with 128-row query steps (separate dQ mode, D <= 128); needs q-side maps with
-// 128-row boxes.  Returns cudaErrorInvalidValue for other head dims.
+// dK/dV-only kernel of the separate dQ mode; needs q-side maps with 128-row boxes up to D = 128 and
+// 64-row boxes at D = 192.  Returns cudaErrorInvalidValue for other head dims.
 cudaError_t launch_kv_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
 cudaError_t launch_kv_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
 cudaError_t launch_dq_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
@@ -141,8 +141,8 @@ cudaError_t launch_dq_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, 
 // 128-row boxes on both sides.  Returns cudaErrorInvalidValue for other head dims.
 cudaError_t launch_bwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
 cudaError_t launch_bwd_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
-// The same for D > 128 (D = 192, Dv = 128): mkv are the kv-stationary kernel's maps (64-row query,
-// 128-row key boxes), mdq the dQ kernel's (128-row query, 64-row key boxes).
+// The same for D > 128 (D = 192, Dv = 128): mkv are the dK/dV CTAs' maps (64-row query, 128-row
+// key boxes), mdq the dQ CTAs' (128-row query, 64-row key boxes).
 cudaError_t launch_bwd_wide_bf16(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int D, int Dv,
                                  int n_kv_blocks, cudaStream_t st);
 cudaError_t launch_bwd_wide_fp16(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int D, int Dv,

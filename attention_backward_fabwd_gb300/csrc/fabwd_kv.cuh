@@ -1,10 +1,11 @@
-// kv-stationary dK/dV kernel with 128-row query steps (separate dQ mode, D <= 128).
+// kv-stationary dK/dV kernel of the separate dQ mode: 128-row query steps up to D = 128, 64-row
+// steps at D = 192 (where dK alone takes 192 of the 512 TMEM columns).
 //
 // What it computes is dK and dV of the page "CANN ops-transformer FlashAttnGrad 算子详解"
 // (discosf.com/news/4863418), §一: dV = Pᵀ·dY and dK = scale·dSᵀ·Q with P = exp(scale·QKᵀ − lse)
 // and dS = P ⊙ (dY·Vᵀ − sfmg), summed over the query blocks and the G q-heads of a kv-head.
-// One CTA owns 128 keys of one kv-head; each step handles 128 query rows of one q-head:
-//     Sᵀ  = K·Qᵀ     tcgen05 M = 128 keys, N = 128 queries (a full-rate shape), TMEM slot S
+// One CTA owns 128 keys of one kv-head; each step handles BR query rows of one q-head:
+//     Sᵀ  = K·Qᵀ     tcgen05 M = 128 keys, N = BR queries (128: a full-rate shape), TMEM slot S
 //     dPᵀ = V·dOᵀ    same shape, TMEM slot dP
 //     Pᵀ  = exp2(Sᵀ·scale·log2e − lse·log2e) -> 16-bit pairs over the warpgroup's own Sᵀ columns
 //     −dSᵀ = Pᵀ ⊙ (sfmg − dPᵀ)              -> 16-bit pairs over its own dPᵀ columns
@@ -12,7 +13,8 @@
 //                                           epilogue writes −scale times the accumulator
 // The elementwise steps use packed fp32x2 FMA and multiply; the signs are chosen so that no
 // per-element negation of the lse and sfmg vectors is needed.
-// Warpgroup g (warps 4g..4g+3) handles query columns [64g, 64g+64) of every step.  Keeping dSᵀ in
+// Warpgroup g (warps 4g..4g+3) handles query columns [NCW·g, NCW·g + NCW) of every step, NCW = BR/2.
+// Keeping dSᵀ in
 // the dPᵀ columns frees the Sᵀ columns as soon as dV has read Pᵀ, so the MMA warp issues
 //     Sᵀ(t), dPᵀ(t), dV(t), Sᵀ(t+1), dK(t), dPᵀ(t+1), dV(t+1), ...
 // and the elementwise work of each step overlaps the previous step's dK and the next step's Sᵀ.
@@ -24,7 +26,7 @@
 // thread therefore waits only for the compute warps' P and dS handoffs; the compute warps wait
 // for the TMA stages the MMA thread reads next (Q(t+1) before they hand over P(t), dO(t+1) before
 // dS(t)), which falls where they would otherwise idle.
-// TMEM columns: dK [0, D), dV [D, D+Dv), Sᵀ/Pᵀ [D+Dv, +128), dPᵀ/dSᵀ [D+Dv+128, +128).
+// TMEM columns: dK [0, D), dV [D, D+Dv), Sᵀ/Pᵀ [D+Dv, +BR), dPᵀ/dSᵀ [D+Dv+BR, +BR).
 // Bounded waits, abort flag, drain and TMEM release as in the fused kernel.
 #pragma once
 
@@ -37,7 +39,9 @@ namespace fabwd {
 
 template <int D, int DV>
 struct KvCfg {
-  static constexpr int BR = 128, BC = kBlockKV, NQ = 3, NO = 2;  // Q ring and dO ring stages
+  // 128 query rows per step up to D = 128; 64 at D = 192, where dK alone takes 192 TMEM columns
+  static constexpr int BR = D > 128 ? 64 : 128, BC = kBlockKV, NQ = 3, NO = 2;  // Q ring and dO ring stages
+  static constexpr int NCW = BR / 2;  // query columns of each compute warpgroup
   static constexpr uint32_t kK = D * BC * 2, kV = DV * BC * 2, kQ = D * BR * 2, kdO = DV * BR * 2;
   static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + NQ * kQ;
   static constexpr uint32_t oL = odO + NO * kdO;     // [NQ][BR] fp32 lse·log2(e)
@@ -46,7 +50,7 @@ struct KvCfg {
   static constexpr uint32_t oMisc = oBar + 20 * 8;
   static constexpr uint32_t bytes = oMisc + 64;
   static constexpr uint32_t cDK = 0, cDV = D, cS = D + DV, cP = cS + BR;
-  static_assert(D % 64 == 0 && DV % 64 == 0 && D <= 128 && DV <= D, "head dims");
+  static_assert(D % 64 == 0 && DV % 64 == 0 && DV <= D && (D <= 128 || (D == 192 && DV == 128)), "head dims");
   static_assert(cP + BR <= 512, "TMEM budget");
   static_assert(bytes <= 232448, "shared memory budget");
 };
@@ -170,9 +174,10 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
       constexpr uint32_t ID_DK = idesc_f16(BC, D, kBF16, false, true);
       const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::oK), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::oV), 16, 1024);
-      // A operand columns of k-step kk (16 queries): warpgroup kk/4 holds queries 64·(kk/4)..,
-      // its 16-bit pairs at +0..31 of its own 64 columns
-      auto a_col = [](int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; };
+      // A operand columns of k-step kk (16 queries): warpgroup kk/KPW holds queries NCW·(kk/KPW)..,
+      // its 16-bit pairs at the start of its own NCW columns
+      constexpr int NCW = C::NCW, KPW = NCW / 16;
+      auto a_col = [](int kk) { return (kk / KPW) * NCW + (kk % KPW) * 8; };
       auto issue_s = [&](int t) {  // Q(t) landed: vouched for by the compute warps' P(t-1) handoff
         const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::oQ + (t % NQ) * C::kQ), 16, 1024);
 #pragma unroll
@@ -231,7 +236,9 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
     const int q4 = warp & 3, g = warp >> 2;
     const int row = q4 * 32 + lane;  // TMEM lane = key row j0 + row
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t sS = tmem + lane_off + C::cS + g * 64, sP = tmem + lane_off + C::cP + g * 64;
+    constexpr int NCW = C::NCW;
+    constexpr bool W2 = NCW == 64;  // two 32-column halves per thread (else one)
+    const uint32_t sS = tmem + lane_off + C::cS + g * NCW, sP = tmem + lane_off + C::cP + g * NCW;
     const int jr = j0 + row;
     const bool j_valid = jr < sq.L2;
     const long long vlo = (long long)jr - off - hi, vhi = (long long)jr - off - lo;
@@ -242,49 +249,57 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
     for (int t = 0; ok && t < T; ++t) {
       const int sq_ = t % NQ, so = t % NO;
       const int qb = qb_begin + t % nqb;
-      const int i0 = qb * BR, ic0 = i0 + g * 64;
+      const int i0 = qb * BR, ic0 = i0 + g * NCW;
       // lse(t) and sfmg(t) landed: observed before the previous step's handoffs (or above).  The
       // MMA thread issues Sᵀ(t+1) right after this step's P handoff: its Q stage (loaded long
       // ago) is confirmed here, while the warps would wait for Sᵀ(t) anyway.
       if (t + 1 < T && !(ok = wait_bar_warp(&bars[kKvQFull + (t + 1) % NQ], ((t + 1) / NQ) & 1, abort_flag, a))) break;
       if (!(ok = wait_bar_warp(&bars[kKvSFull], t & 1, abort_flag, a))) break;
       tc_fence_after();
-      const float4* sL4 = reinterpret_cast<const float4*>(smem + C::oL + sq_ * BR * 4 + g * 256);
-      const float4* sF4 = reinterpret_cast<const float4*>(smem + C::oF + so * BR * 4 + g * 256);
+      const float4* sL4 = reinterpret_cast<const float4*>(smem + C::oL + sq_ * BR * 4 + g * NCW * 4);
+      const float4* sF4 = reinterpret_cast<const float4*>(smem + C::oF + so * BR * 4 + g * NCW * 4);
       const long long dmin = (long long)j0 - (i0 + BR - 1) - off, dmax = (long long)(j1 - 1) - i0 - off;
       const bool full = dmin >= lo && dmax <= hi;
-      uint32_t p0[32], p1[32];  // Sᵀ row (64 queries), then P (fp32 bits)
+      uint32_t p0[32], p1[32];  // Sᵀ row (NCW queries), then P (fp32 bits)
       tmem_ld32(sS, p0);
-      tmem_ld32(sS + 32, p1);
+      if constexpr (W2) tmem_ld32(sS + 32, p1);
       tmem_wait_ld();
       reg_fence(p0);
-      reg_fence(p1);
+      if constexpr (W2) reg_fence(p1);
       // P = 2^(s·scale_log2 − lse2) as 2^−(lse2 − s·scale_log2): one packed fp32x2 FMA per
       // query pair against the lse vector as stored; the sign goes with the exponential's operand.
       // RN is sign-symmetric, so the value is the one the unpacked form gives, bit for bit.
       const float2 nsc2 = make_float2(-a.scale_log2, -a.scale_log2);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 l0 = sL4[c4], l1 = sL4[c4 + 8];
-        const float la[4] = {l0.x, l0.y, l0.z, l0.w}, lb[4] = {l1.x, l1.y, l1.z, l1.w};
+        const float4 l0 = sL4[c4];
+        const float la[4] = {l0.x, l0.y, l0.z, l0.w};
+        float lb[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (W2) {
+          const float4 l1 = sL4[c4 + 8];
+          lb[0] = l1.x, lb[1] = l1.y, lb[2] = l1.z, lb[3] = l1.w;
+        }
 #pragma unroll
         for (int e = 0; e < 4; e += 2) {
           const int c = 4 * c4 + e;
           const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(p0[c]), __uint_as_float(p0[c + 1])), nsc2,
                                        make_float2(la[e], la[e + 1]));
-          const float2 y1 = __ffma2_rn(make_float2(__uint_as_float(p1[c]), __uint_as_float(p1[c + 1])), nsc2,
-                                       make_float2(lb[e], lb[e + 1]));
           p0[c] = __float_as_uint(ex2(-y0.x));
           p0[c + 1] = __float_as_uint(ex2(-y0.y));
-          p1[c] = __float_as_uint(ex2(-y1.x));
-          p1[c + 1] = __float_as_uint(ex2(-y1.y));
+          if constexpr (W2) {
+            const float2 y1 = __ffma2_rn(make_float2(__uint_as_float(p1[c]), __uint_as_float(p1[c + 1])), nsc2,
+                                         make_float2(lb[e], lb[e + 1]));
+            p1[c] = __float_as_uint(ex2(-y1.x));
+            p1[c + 1] = __float_as_uint(ex2(-y1.y));
+          }
         }
       }
       if (!full) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           if (ic0 + c < i_vis_lo || ic0 + c > i_vis_hi) p0[c] = 0u;
-          if (ic0 + 32 + c < i_vis_lo || ic0 + 32 + c > i_vis_hi) p1[c] = 0u;
+          if constexpr (W2)
+            if (ic0 + 32 + c < i_vis_lo || ic0 + 32 + c > i_vis_hi) p1[c] = 0u;
         }
       }
       if (!j_valid) {
@@ -296,9 +311,11 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           pk[c] = pack2<FP16>(__uint_as_float(p0[2 * c]), __uint_as_float(p0[2 * c + 1]));
-          pk[16 + c] = pack2<FP16>(__uint_as_float(p1[2 * c]), __uint_as_float(p1[2 * c + 1]));
+          if constexpr (W2) pk[16 + c] = pack2<FP16>(__uint_as_float(p1[2 * c]), __uint_as_float(p1[2 * c + 1]));
         }
-        tmem_st32(sS, pk);  // Pᵀ over this warpgroup's own (already read) Sᵀ columns
+        // Pᵀ over this warpgroup's own (already read) Sᵀ columns
+        if constexpr (W2) tmem_st32(sS, pk);
+        else tmem_st16(sS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
         tmem_wait_st();
       }
       tc_fence_before();
@@ -311,10 +328,10 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
       {
         uint32_t r0[32], r1[32];
         tmem_ld32(sP, r0);
-        tmem_ld32(sP + 32, r1);
+        if constexpr (W2) tmem_ld32(sP + 32, r1);
         tmem_wait_ld();
         reg_fence(r0);
-        reg_fence(r1);
+        if constexpr (W2) reg_fence(r1);
         // −dS = P ⊙ (sfmg − dP), packed: (sfmg − dP) as one fp32x2 FMA with −1 (exactly the
         // negated difference), then a packed multiply.  dK accumulates −dS·Q and its epilogue
         // scales by −scale.
@@ -322,22 +339,31 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
         uint32_t dk[32];
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 f0 = sF4[c4], f1 = sF4[c4 + 8];
-          const float fa[4] = {f0.x, f0.y, f0.z, f0.w}, fb[4] = {f1.x, f1.y, f1.z, f1.w};
+          const float4 f0 = sF4[c4];
+          const float fa[4] = {f0.x, f0.y, f0.z, f0.w};
+          float fb[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (W2) {
+            const float4 f1 = sF4[c4 + 8];
+            fb[0] = f1.x, fb[1] = f1.y, fb[2] = f1.z, fb[3] = f1.w;
+          }
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const int c = 4 * c4 + e;
             const float2 n0 = __fmul2_rn(make_float2(__uint_as_float(p0[c]), __uint_as_float(p0[c + 1])),
                                          __ffma2_rn(make_float2(__uint_as_float(r0[c]), __uint_as_float(r0[c + 1])), m1,
                                                     make_float2(fa[e], fa[e + 1])));
-            const float2 n1 = __fmul2_rn(make_float2(__uint_as_float(p1[c]), __uint_as_float(p1[c + 1])),
-                                         __ffma2_rn(make_float2(__uint_as_float(r1[c]), __uint_as_float(r1[c + 1])), m1,
-                                                    make_float2(fb[e], fb[e + 1])));
             dk[c >> 1] = pack2<FP16>(n0.x, n0.y);
-            dk[16 + (c >> 1)] = pack2<FP16>(n1.x, n1.y);
+            if constexpr (W2) {
+              const float2 n1 = __fmul2_rn(make_float2(__uint_as_float(p1[c]), __uint_as_float(p1[c + 1])),
+                                           __ffma2_rn(make_float2(__uint_as_float(r1[c]), __uint_as_float(r1[c + 1])),
+                                                      m1, make_float2(fb[e], fb[e + 1])));
+              dk[16 + (c >> 1)] = pack2<FP16>(n1.x, n1.y);
+            }
           }
         }
-        tmem_st32(sP, dk);  // −dSᵀ over this warpgroup's own (already read) dPᵀ columns
+        // −dSᵀ over this warpgroup's own (already read) dPᵀ columns
+        if constexpr (W2) tmem_st32(sP, dk);
+        else tmem_st16(sP, *reinterpret_cast<uint32_t(*)[16]>(&dk[0]));
         tmem_wait_st();
       }
       tc_fence_before();

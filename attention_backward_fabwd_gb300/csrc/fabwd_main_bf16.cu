@@ -17,6 +17,7 @@ cudaError_t launch_dq_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, 
 cudaError_t launch_kv_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st) {
   if (D == 64 && Dv == 64) return launch_kv_t<64, 64, false>(a, m, n_kv_blocks, st);
   if (D == 128 && Dv == 128) return launch_kv_t<128, 128, false>(a, m, n_kv_blocks, st);
+  if (D == 192 && Dv == 128) return launch_kv_t<192, 128, false>(a, m, n_kv_blocks, st);
   return cudaErrorInvalidValue;
 }
 cudaError_t launch_bwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st) {

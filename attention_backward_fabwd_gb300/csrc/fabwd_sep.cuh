@@ -51,9 +51,9 @@ cudaError_t launch_bwd_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, 
   return cudaLaunchKernelEx(&cfg, fabwd_bwd_kernel<D, DV, FP16>, m.q, m.k, m.v, m.dout, a, kv_ctas);
 }
 
-// D > 128: the two CTA kinds take different tensor-map boxes (the kv-stationary kernel streams
-// 64-row query tiles against 128 resident keys, the dQ kernel 64-key tiles against 128 resident
-// queries), so this grid gets both sets of maps.
+// D > 128: the two CTA kinds take different tensor-map boxes (the dK/dV CTAs stream 64-row query
+// tiles against 128 resident keys, the dQ CTAs 64-key tiles against 128 resident queries), so
+// this grid gets both sets of maps.
 template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_bwd_wide_kernel(const __grid_constant__ CUtensorMap kq, const __grid_constant__ CUtensorMap kk,
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                           const __grid_constant__ CUtensorMap qv, const __grid_constant__ CUtensorMap qdo,
                           const MainArgs a, int kv_ctas) {
   if ((int)blockIdx.x < kv_ctas)
-    main_block<D, DV, FP16, false>(kq, kk, kvv, kdo, a, blockIdx.x, blockIdx.y);
+    kv_block<D, DV, FP16>(kq, kk, kvv, kdo, a, blockIdx.x, blockIdx.y);
   else
     dq_block<D, DV, FP16>(qq, qk, qv, qdo, a, blockIdx.x - kv_ctas, blockIdx.y);
 }
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 template <int D, int DV, bool FP16>
 cudaError_t launch_bwd_wide_t(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int n_kv_blocks,
                               cudaStream_t st) {
-  constexpr uint32_t kb = MainCfg<D, DV, false>::bytes, qb = DqCfg<D, DV>::bytes;
+  constexpr uint32_t kb = KvCfg<D, DV>::bytes, qb = DqCfg<D, DV>::bytes;
   constexpr uint32_t bytes = kb > qb ? kb : qb;
   if (cudaError_t e = ensure_smem_limit<fabwd_bwd_wide_kernel<D, DV, FP16>>((int)bytes); e != cudaSuccess) return e;
   const int kv_ctas = n_kv_blocks * a.N2;
