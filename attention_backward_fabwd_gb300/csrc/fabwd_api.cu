@@ -388,7 +388,7 @@ fabwd_status fabwd_run_dq(const fabwd_params* p, void* ws, size_t ws_bytes, void
     e = launch_convert(c, p->dtype == FABWD_FP16, st);
   } else if (any_pair(p, pl)) {
     MainMaps maps;
-    if (!make_maps(p, &maps, kDqBlockQ, p->D > 128 ? 64 : 128)) return FABWD_ERR_CUDA;
+    if (!make_maps(p, &maps, kDqBlockQ, dq_block_kv((int)p->D))) return FABWD_ERR_CUDA;
     const MainArgs a = main_args(p, pl, w, 0);
     e = p->dtype == FABWD_FP16 ? launch_dq_fp16(a, maps, (int)p->D, (int)p->Dv, st)
                                : launch_dq_bf16(a, maps, (int)p->D, (int)p->Dv, st);
@@ -420,7 +420,7 @@ fabwd_status fabwd_run(const fabwd_params* p, void* ws, size_t ws_bytes, void* s
       e = fp16 ? launch_bwd_fp16(a, maps, D, Dv, n_kv_blocks, st) : launch_bwd_bf16(a, maps, D, Dv, n_kv_blocks, st);
     } else {
       MainMaps mkv, mdq;
-      if (!make_maps(p, &mkv, kBlockQ, kBlockKV) || !make_maps(p, &mdq, kDqBlockQ, 64)) return FABWD_ERR_CUDA;
+      if (!make_maps(p, &mkv, kBlockQ, kBlockKV) || !make_maps(p, &mdq, kDqBlockQ, dq_block_kv(D))) return FABWD_ERR_CUDA;
       e = fp16 ? launch_bwd_wide_fp16(a, mkv, mdq, D, Dv, n_kv_blocks, st)
                : launch_bwd_wide_bf16(a, mkv, mdq, D, Dv, n_kv_blocks, st);
     }

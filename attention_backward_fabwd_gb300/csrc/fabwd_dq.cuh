@@ -15,8 +15,11 @@
 //
 // Warp roles (320 threads): warps 0-7 compute (warp w reads TMEM lanes 32·(w%4)..+31; warps 0-3
 // take key columns [0, BN/2), warps 4-7 [BN/2, BN)), warp 8 issues TMA loads (Q, dO once; K
-// through a 3-stage ring released after dQ, V through a 2-stage ring released after dP), warp 9
-// allocates TMEM and issues the MMAs.  One thread issues every tcgen05.mma, and an MMA of these
+// through a 3-stage ring released after dQ, V through a ring of NV stages released after dP), warp 9
+// allocates TMEM and issues the MMAs.  BN = 128 keys and NV = 2 up to D = 128; at D = 192, BN = 96
+// and NV = 1 (a second V stage does not fit beside Q, dO and three 36 KB K stages): V(t+1) then
+// loads once dP(t) has read V(t), while dQ(t−1) and S(t+1), queued behind dP(t), keep the tensor
+// pipe busy.  One thread issues every tcgen05.mma, and an MMA of these
 // shapes occupies it about as long as the tensor pipe takes to run it, so each barrier wait
 // between MMA groups idles the pipe.  The MMA thread therefore issues
 //     [dS(t) written] dP(t+1), dQ(t), [K(t+2) landed] S(t+2)
@@ -38,9 +41,10 @@ namespace fabwd {
 template <int D, int DV>
 struct DqCfg {
   static constexpr int BM = 128;                 // query rows per CTA (TMEM lanes)
-  static constexpr int BN = D > 128 ? 64 : 128;  // keys per step
-  static constexpr int NK = 3, NV = 2;           // K ring and V ring stages
+  static constexpr int BN = dq_block_kv(D);      // keys per step
+  static constexpr int NK = 3, NV = D > 128 ? 1 : 2;  // K ring and V ring stages
   static constexpr int NC = BN / 2;              // key columns per compute thread
+  static_assert(NC % 16 == 0, "dS k-steps of 16 keys stay within one warpgroup's columns");
   static constexpr uint32_t kQ = D * BM * 2, kdO = DV * BM * 2, kK = D * BN * 2, kV = DV * BN * 2;
   static constexpr uint32_t oQ = 0, odO = oQ + kQ, oK = odO + kdO, oV = oK + NK * kK;
   static constexpr uint32_t oBar = oV + NV * kV;
@@ -243,9 +247,11 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
       uint32_t p[NC];
       tmem_ld32(sb, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
       if constexpr (NC == 64) tmem_ld32(sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      if constexpr (NC == 48) tmem_ld16(sb + 32, *reinterpret_cast<uint32_t(*)[16]>(&p[32]));
       tmem_wait_ld();
       reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[0]));
       if constexpr (NC == 64) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      if constexpr (NC == 48) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&p[32]));
       // P = 2^(s·scale_log2 − lse2): one packed fp32x2 FMA per key pair (lse2 is this row's)
 #pragma unroll
       for (int c = 0; c < NC; c += 2) {
@@ -277,6 +283,21 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
           ds[c >> 1] = pack2<FP16>(d.x, d.y);
         }
         tmem_st16(sb + hh * 16, ds);  // dS over this warpgroup's own (already read) S columns
+      }
+      if constexpr (NC % 32 == 16) {  // the last 16 key columns
+        constexpr int c0 = NC - 16;
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_off + C::cP + g * NC + c0, r);
+        tmem_wait_ld();
+        reg_fence16(r);
+        uint32_t ds[8];
+#pragma unroll
+        for (int c = 0; c < 16; c += 2) {
+          const float2 d = __fmul2_rn(make_float2(__uint_as_float(p[c0 + c]), __uint_as_float(p[c0 + c + 1])),
+                                      __fadd2_rn(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), nsf2));
+          ds[c >> 1] = pack2<FP16>(d.x, d.y);
+        }
+        tmem_st8(sb + c0 / 2, ds);
       }
       tmem_wait_st();
       tc_fence_before();

@@ -29,6 +29,9 @@ constexpr int kBlockKV = 128;  // kv rows per CTA of the main kernel (M of the k
 constexpr int kBlockQ = 64;    // q rows per main-loop step (N of S^T / dP^T / dQ^T)
 constexpr int kRowPad = 128;   // padding of the per-(sequence, q-head) lse2 / sfmg rows
 constexpr int kDqBlockQ = 128; // q rows per CTA of the q-stationary dQ kernel
+// keys per step of the q-stationary dQ kernel: 96 at D = 192, where the dQ accumulator leaves
+// 320 TMEM columns for the two S buffers and dP
+constexpr int dq_block_kv(int D) { return D > 128 ? 96 : 128; }
 
 enum Layout : int { kBSND = 0, kTND = 1, kBNSD = 2 };
 

@@ -52,7 +52,7 @@ cudaError_t launch_bwd_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, 
 }
 
 // D > 128: the two CTA kinds take different tensor-map boxes (the dK/dV CTAs stream 64-row query
-// tiles against 128 resident keys, the dQ CTAs 64-key tiles against 128 resident queries), so
+// tiles against 128 resident keys, the dQ CTAs 96-key tiles against 128 resident queries), so
 // this grid gets both sets of maps.
 template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
