@@ -12,7 +12,13 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libfabwd.so")
 
-SOURCES = ["fabwd_api.cu", "fabwd_aux.cu", "fabwd_main_bf16.cu", "fabwd_main_fp16.cu", "fabwd_static_ws.cu"]
+# (source, object, defines): the kernel families are compiled once per io dtype
+_PLAIN = ["fabwd_api.cu", "fabwd_aux.cu", "fabwd_static_ws.cu"]
+_PER_DTYPE = ["fabwd_onegrid.cu", "fabwd_split.cu", "fabwd_fused.cu", "fabwd_forward.cu"]
+UNITS = [(src, src.replace(".cu", ".o"), []) for src in _PLAIN] + [
+    (src, src.replace(".cu", f"_{dt}.o"), [f"-DFABWD_INST_FP16={int(dt == 'fp16')}"])
+    for src in _PER_DTYPE for dt in ("bf16", "fp16")]
+SOURCES = _PLAIN + _PER_DTYPE
 HEADERS = ["fabwd_ptx.cuh", "fabwd_internal.cuh", "fabwd_main.cuh", "fabwd_dq.cuh", "fabwd_kv.cuh", "fabwd_sep.cuh", "fabwd_fwd.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -42,10 +48,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     cc = nvcc()
     procs = []
     objs = []
-    for src in SOURCES:
-        obj = os.path.join(OUT, src.replace(".cu", ".o"))
+    for src, o, defines in UNITS:
+        obj = os.path.join(OUT, o)
         objs.append(obj)
-        cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [cc, *ARCH, *FLAGS, *defines, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))

@@ -60,7 +60,7 @@ fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
     if (p->cu_seqlens_q || p->cu_seqlens_kv) return FABWD_ERR_INVALID;
     if (p->B * p->S1 >= (1ll << 31) || p->B * p->S2 >= (1ll << 31)) return FABWD_ERR_INVALID;
   }
-  if (!main_supported((int)p->D, (int)p->Dv)) return FABWD_ERR_UNSUPPORTED;
+  if (!dims_supported((int)p->D, (int)p->Dv, p->dq_mode == FABWD_DQ_ATOMIC)) return FABWD_ERR_UNSUPPORTED;
   // The workspace holds B·N1·roundup(S1, 128) fp32 rows twice.  With TND, B, N1 and the
   // max_seqlen_q bound S1 are limited only one by one, so the product could wrap size_t;
   // refuse more than 2^40 rows (4 TiB each) before any size is computed.
@@ -180,8 +180,11 @@ bool make_map(CUtensorMap* m, const void* base, bool fp16, int layout, long long
 }  // namespace
 
 namespace fabwd {
-bool main_supported(int D, int Dv) {
-  return (D == 64 && Dv == 64) || (D == 128 && Dv == 128) || (D == 192 && Dv == 128);
+bool dims_supported(int D, int Dv, bool atomic) {
+  // row strides of D·2 and Dv·2 bytes must be multiples of 16 for the TMA tensor maps and the
+  // 16-byte row stores
+  if (D % 8 != 0 || Dv % 8 != 0) return false;
+  return !(atomic && pad_dim(D) == 192 && pad_dim(Dv) == 192);
 }
 }  // namespace fabwd
 
@@ -293,6 +296,8 @@ MainArgs main_args(const fabwd_params* p, const Plan& pl, uint8_t* w, int inject
   a.N1 = (int)p->N1;
   a.N2 = (int)p->N2;
   a.G = (int)(p->N1 / p->N2);
+  a.io_d = (int)p->D;
+  a.io_dv = (int)p->Dv;
   a.S1 = (int)p->S1;
   a.S2 = (int)p->S2;
   a.T1 = p->T1;
@@ -350,17 +355,16 @@ fabwd_status fabwd_run_main(const fabwd_params* p, void* ws, size_t ws_bytes, vo
   if (any_pair(p, pl)) {
     // separate mode: the dK/dV kernel (128-row query steps up to D = 128, 64-row at D = 192);
     // atomic mode: the fused kv-stationary kernel with 64-row steps, which also reduces dQ
-    const bool kv128 = pl.separate;
+    const int D = pad_dim((int)p->D), Dv = pad_dim((int)p->Dv);
     MainMaps maps;
-    if (!make_maps(p, &maps, pl.separate && p->D <= 128 ? 128 : kBlockQ, kBlockKV)) return FABWD_ERR_CUDA;
+    if (!make_maps(p, &maps, pl.separate && D <= 128 ? 128 : kBlockQ, kBlockKV)) return FABWD_ERR_CUDA;
     const MainArgs a = main_args(p, pl, static_cast<uint8_t*>(ws), inject);
     const int n_kv_blocks = (int)((p->S2 + kBlockKV - 1) / kBlockKV);
     const bool fp16 = p->dtype == FABWD_FP16;
-    const int D = (int)p->D, Dv = (int)p->Dv;
-    cudaError_t e = kv128 ? (fp16 ? launch_kv_fp16(a, maps, D, Dv, n_kv_blocks, st)
-                                  : launch_kv_bf16(a, maps, D, Dv, n_kv_blocks, st))
-                          : (fp16 ? launch_main_fp16(a, maps, D, Dv, n_kv_blocks, !pl.separate, st)
-                                  : launch_main_bf16(a, maps, D, Dv, n_kv_blocks, !pl.separate, st));
+    cudaError_t e = pl.separate ? (fp16 ? launch_kv<true>(a, maps, D, Dv, n_kv_blocks, st)
+                                        : launch_kv<false>(a, maps, D, Dv, n_kv_blocks, st))
+                                : (fp16 ? launch_main<true>(a, maps, D, Dv, n_kv_blocks, st)
+                                        : launch_main<false>(a, maps, D, Dv, n_kv_blocks, st));
     if (e != cudaSuccess) return FABWD_ERR_CUDA;
   } else if (pl.rowsK > 0) {
     // no visible pair at all: dk = dv = 0
@@ -388,10 +392,10 @@ fabwd_status fabwd_run_dq(const fabwd_params* p, void* ws, size_t ws_bytes, void
     e = launch_convert(c, p->dtype == FABWD_FP16, st);
   } else if (any_pair(p, pl)) {
     MainMaps maps;
-    if (!make_maps(p, &maps, kDqBlockQ, dq_block_kv((int)p->D))) return FABWD_ERR_CUDA;
+    const int D = pad_dim((int)p->D), Dv = pad_dim((int)p->Dv);
+    if (!make_maps(p, &maps, kDqBlockQ, dq_block_kv(D, Dv))) return FABWD_ERR_CUDA;
     const MainArgs a = main_args(p, pl, w, 0);
-    e = p->dtype == FABWD_FP16 ? launch_dq_fp16(a, maps, (int)p->D, (int)p->Dv, st)
-                               : launch_dq_bf16(a, maps, (int)p->D, (int)p->Dv, st);
+    e = p->dtype == FABWD_FP16 ? launch_dq<true>(a, maps, D, Dv, st) : launch_dq<false>(a, maps, D, Dv, st);
   } else if (pl.rowsQ > 0) {
     e = launch_zero(p->dq, pl.rowsQ * p->N1 * p->D * 2, st);  // no visible pair: dq = 0
   }
@@ -412,17 +416,18 @@ fabwd_status fabwd_run(const fabwd_params* p, void* ws, size_t ws_bytes, void* s
     const MainArgs a = main_args(p, pl, static_cast<uint8_t*>(ws), inject);
     const int n_kv_blocks = (int)((p->S2 + kBlockKV - 1) / kBlockKV);
     const bool fp16 = p->dtype == FABWD_FP16;
-    const int D = (int)p->D, Dv = (int)p->Dv;
+    const int D = pad_dim((int)p->D), Dv = pad_dim((int)p->Dv);
     cudaError_t e;
     if (D <= 128) {
       MainMaps maps;
       if (!make_maps(p, &maps, 128, kBlockKV)) return FABWD_ERR_CUDA;
-      e = fp16 ? launch_bwd_fp16(a, maps, D, Dv, n_kv_blocks, st) : launch_bwd_bf16(a, maps, D, Dv, n_kv_blocks, st);
+      e = fp16 ? launch_bwd<true>(a, maps, D, Dv, n_kv_blocks, st) : launch_bwd<false>(a, maps, D, Dv, n_kv_blocks, st);
     } else {
       MainMaps mkv, mdq;
-      if (!make_maps(p, &mkv, kBlockQ, kBlockKV) || !make_maps(p, &mdq, kDqBlockQ, dq_block_kv(D))) return FABWD_ERR_CUDA;
-      e = fp16 ? launch_bwd_wide_fp16(a, mkv, mdq, D, Dv, n_kv_blocks, st)
-               : launch_bwd_wide_bf16(a, mkv, mdq, D, Dv, n_kv_blocks, st);
+      if (!make_maps(p, &mkv, kBlockQ, kBlockKV) || !make_maps(p, &mdq, kDqBlockQ, dq_block_kv(D, Dv)))
+        return FABWD_ERR_CUDA;
+      e = fp16 ? launch_bwd_wide<true>(a, mkv, mdq, D, Dv, n_kv_blocks, st)
+               : launch_bwd_wide<false>(a, mkv, mdq, D, Dv, n_kv_blocks, st);
     }
     return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
   }
@@ -468,9 +473,9 @@ fabwd_status fabwd_forward(const fabwd_params* p, void* attn_out, float* softmax
   a.lse_out = softmax_lse;
   a.sinks = p->sinks;
   MainMaps maps;
-  if (!make_maps(&f, &maps, 128, p->D > 128 ? 64 : 128)) return FABWD_ERR_CUDA;
-  cudaError_t e = p->dtype == FABWD_FP16 ? launch_fwd_fp16(a, maps, (int)p->D, (int)p->Dv, st)
-                                         : launch_fwd_bf16(a, maps, (int)p->D, (int)p->Dv, st);
+  const int D = pad_dim((int)p->D), Dv = pad_dim((int)p->Dv);
+  if (!make_maps(&f, &maps, 128, D > 128 ? 64 : 128)) return FABWD_ERR_CUDA;
+  cudaError_t e = p->dtype == FABWD_FP16 ? launch_fwd<true>(a, maps, D, Dv, st) : launch_fwd<false>(a, maps, D, Dv, st);
   if (e == cudaSuccess) e = unused_rows(p, attn_out, softmax_lse, true, st);
   return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;
 }
@@ -505,7 +510,7 @@ const char* fabwd_status_string(fabwd_status s) {
     case FABWD_OK: return "ok";
     case FABWD_ERR_NULLPTR: return "a required pointer is NULL";
     case FABWD_ERR_INVALID: return "invalid argument (dtype, shape, layout, mask, window or alignment)";
-    case FABWD_ERR_UNSUPPORTED: return "valid but unsupported (no kernel built for this head-dim pair)";
+    case FABWD_ERR_UNSUPPORTED: return "valid but unsupported (head dims not multiples of 8, atomic dQ with D and Dv > 128, or too many CTAs)";
     case FABWD_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
     case FABWD_ERR_CUDA: return "CUDA call or kernel launch failed";
     case FABWD_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up (device status)";

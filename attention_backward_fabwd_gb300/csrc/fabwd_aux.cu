@@ -10,6 +10,7 @@
 #include "../../include/fabwd.h"
 
 #include <cmath>
+#include <type_traits>
 
 namespace fabwd {
 
@@ -50,9 +51,12 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
   // attn_out, 2·Dv bytes each, are whole 128-byte lines in any order).  Each lane group of LPR
   // lanes takes UN rows per iteration, whose dout, attn_out and lse loads are all issued before
   // the arithmetic.  SMALL: every row index fits 32 bits, so the index split uses 32-bit division.
-  constexpr int LPR = DV / 8;    // lanes per row: one 16-byte chunk (8 elements) each
-  constexpr int RPW = 32 / LPR;  // rows per warp step
-  constexpr int UN = 2;          // row groups per iteration
+  // DV is the kernel's row width (64, 128 or 192); a.Dv (a multiple of 8, at most DV) the rows'
+  // own length: chunks past it are not read.
+  constexpr int CPL = DV == 192 ? 3 : 1;  // 16-byte chunks (8 elements) per lane and row
+  constexpr int LPR = DV / (8 * CPL);     // lanes per row (a power of two)
+  constexpr int RPW = 32 / LPR;           // rows per warp step
+  constexpr int UN = 2;                   // row groups per iteration
   const long long nrows = (long long)a.B * a.N1 * a.S1p;
   const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -60,7 +64,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
   const int sub = lane / LPR, part = lane % LPR;
   const bool tnd = a.layout == kTND;
   for (long long base = gwarp * RPW * UN; base < nrows; base += nwarp * RPW * UN) {
-    uint4 x[UN], y[UN];
+    uint4 x[UN][CPL], y[UN][CPL];
     float l[UN];
     bool act[UN], val[UN];
     long long o[UN];
@@ -99,12 +103,19 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
       if (tnd && i >= ((L1 + 127) / 128) * 128) act[u] = false;
       val[u] = act[u] && i < L1;
       o[u] = ((long long)b * a.N1 + n1) * a.S1p + i;
-      x[u] = y[u] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) x[u][k] = y[u][k] = make_uint4(0u, 0u, 0u, 0u);
       l[u] = 0.f;
       if (val[u]) {
         const long long r = row_index(a.layout, b, q0 + i, n1, a.N1, a.S1);
-        x[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * DV + part * 8);
-        y[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.attn_out) + r * DV + part * 8);
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+          const int col = (k * LPR + part) * 8;
+          if (col < a.Dv) {
+            x[u][k] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + r * a.Dv + col);
+            y[u][k] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.attn_out) + r * a.Dv + col);
+          }
+        }
         if (part == 0) {
           const long long li = tnd ? (long long)n1 * a.T1 + q0 + i : ((long long)b * a.N1 + n1) * a.S1 + i;
           if (a.smax) {
@@ -119,13 +130,17 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
     }
 #pragma unroll
     for (int u = 0; u < UN; ++u) {
-      const uint32_t xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w}, ys[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
       float acc = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 xf = unpack2<FP16>(xs[e]), yf = unpack2<FP16>(ys[e]);
-        acc = fmaf(xf.x, yf.x, acc);
-        acc = fmaf(xf.y, yf.y, acc);
+      for (int k = 0; k < CPL; ++k) {
+        const uint32_t xs[4] = {x[u][k].x, x[u][k].y, x[u][k].z, x[u][k].w};
+        const uint32_t ys[4] = {y[u][k].x, y[u][k].y, y[u][k].z, y[u][k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 xf = unpack2<FP16>(xs[e]), yf = unpack2<FP16>(ys[e]);
+          acc = fmaf(xf.x, yf.x, acc);
+          acc = fmaf(xf.y, yf.y, acc);
+        }
       }
 #pragma unroll
       for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -271,18 +286,23 @@ cudaError_t launch_fill_lse_sinks(float* lse, const float* sinks, long long S, i
 
 cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st) {
   const long long rows = (long long)a.B * a.N1 * a.S1p;
-  const long long work = rows * (a.Dv / 8) > a.dq_acc_elems / 4 ? rows * (a.Dv / 8) : a.dq_acc_elems / 4;
+  const int dv = pad_dim(a.Dv);
+  const long long lanes = rows * (dv == 192 ? 8 : dv / 8);
+  const long long work = lanes > a.dq_acc_elems / 4 ? lanes : a.dq_acc_elems / 4;
   const bool small = rows < (1ll << 31);
   const int grid = grid_for(work, 256);
-  if (a.Dv == 128) {
-    if (fp16) small ? preprocess_kernel<true, 128, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<true, 128, false><<<grid, 256, 0, st>>>(a);
-    else small ? preprocess_kernel<false, 128, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<false, 128, false><<<grid, 256, 0, st>>>(a);
-  } else if (a.Dv == 64) {
-    if (fp16) small ? preprocess_kernel<true, 64, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<true, 64, false><<<grid, 256, 0, st>>>(a);
-    else small ? preprocess_kernel<false, 64, true><<<grid, 256, 0, st>>>(a) : preprocess_kernel<false, 64, false><<<grid, 256, 0, st>>>(a);
-  } else {
-    return cudaErrorInvalidValue;
-  }
+  if (a.Dv % 8 != 0 || a.Dv > 192) return cudaErrorInvalidValue;
+  auto go = [&](auto fp16_c, auto dv_c) {
+    constexpr bool F = decltype(fp16_c)::value;
+    constexpr int V = decltype(dv_c)::value;
+    if (small) preprocess_kernel<F, V, true><<<grid, 256, 0, st>>>(a);
+    else preprocess_kernel<F, V, false><<<grid, 256, 0, st>>>(a);
+  };
+  using T = std::true_type;
+  using Fa = std::false_type;
+  if (dv == 64) fp16 ? go(T{}, std::integral_constant<int, 64>{}) : go(Fa{}, std::integral_constant<int, 64>{});
+  else if (dv == 128) fp16 ? go(T{}, std::integral_constant<int, 128>{}) : go(Fa{}, std::integral_constant<int, 128>{});
+  else fp16 ? go(T{}, std::integral_constant<int, 192>{}) : go(Fa{}, std::integral_constant<int, 192>{});
   return cudaGetLastError();
 }
 

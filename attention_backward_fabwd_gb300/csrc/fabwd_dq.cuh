@@ -41,11 +41,13 @@ namespace fabwd {
 template <int D, int DV>
 struct DqCfg {
   static constexpr int BM = 128;                 // query rows per CTA (TMEM lanes)
-  static constexpr int BN = dq_block_kv(D);      // keys per step
-  static constexpr int NK = 3, NV = D > 128 ? 1 : 2;  // K ring and V ring stages
+  static constexpr int BN = dq_block_kv(D, DV);  // keys per step
+  static constexpr int NK = 3;                   // K ring stages
+  static constexpr uint32_t kQ = D * BM * 2, kdO = DV * BM * 2, kK = D * BN * 2, kV = DV * BN * 2;
+  // V ring stages: two where they fit beside Q, dO and the K ring (one at D = 192, Dv = 128)
+  static constexpr int NV = kQ + kdO + NK * kK + 2 * kV + 20 * 8 + 64 <= 232448 ? 2 : 1;
   static constexpr int NC = BN / 2;              // key columns per compute thread
   static_assert(NC % 16 == 0, "dS k-steps of 16 keys stay within one warpgroup's columns");
-  static constexpr uint32_t kQ = D * BM * 2, kdO = DV * BM * 2, kK = D * BN * 2, kV = DV * BN * 2;
   static constexpr uint32_t oQ = 0, odO = oQ + kQ, oK = odO + kdO, oV = oK + NK * kK;
   static constexpr uint32_t oBar = oV + NV * kV;
   static constexpr uint32_t oMisc = oBar + 20 * 8;
@@ -310,7 +312,7 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
       tc_fence_after();
       const bool i_valid = ir < sq.L1;
       const long long qrow = row_index(a.layout, b, (long long)(tnd ? sq.q0 : 0) + (i_valid ? ir : 0), n1, a.N1, a.S1);
-      uint16_t* dq = static_cast<uint16_t*>(a.dq) + qrow * D;
+      uint16_t* dq = static_cast<uint16_t*>(a.dq) + qrow * a.io_d;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         const int col = g * (D / 2) + c * 32;
@@ -325,7 +327,8 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
         if (i_valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
-            *reinterpret_cast<uint4*>(dq + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+            if (col + v4 * 8 < a.io_d)
+              *reinterpret_cast<uint4*>(dq + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
         }
       }
     }
@@ -361,14 +364,6 @@ cudaError_t launch_dq_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) {
   dim3 grid(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B);
   fabwd_dq_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
   return cudaGetLastError();
-}
-
-template <bool FP16>
-cudaError_t launch_dq_dispatch(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st) {
-  if (D == 64 && Dv == 64) return launch_dq_t<64, 64, FP16>(a, m, st);
-  if (D == 128 && Dv == 128) return launch_dq_t<128, 128, FP16>(a, m, st);
-  if (D == 192 && Dv == 128) return launch_dq_t<192, 128, FP16>(a, m, st);
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace fabwd

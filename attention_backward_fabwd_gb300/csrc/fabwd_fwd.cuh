@@ -344,7 +344,7 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
       const long long qrow = row_index(a.layout, b, (long long)(tnd ? sq.q0 : 0) + (i_valid ? ir : 0), n1, a.N1, a.S1);
-      uint16_t* y = static_cast<uint16_t*>(a.dq) + qrow * DV;
+      uint16_t* y = static_cast<uint16_t*>(a.dq) + qrow * a.io_dv;
 #pragma unroll 1
       for (int c = 0; c < DV / 64; ++c) {
         const int col = g * (DV / 2) + c * 32;
@@ -365,7 +365,8 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
         if (i_valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
-            *reinterpret_cast<uint4*>(y + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+            if (col + v4 * 8 < a.io_dv)
+              *reinterpret_cast<uint4*>(y + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
         }
       }
       if (g == 0 && i_valid) {
@@ -404,14 +405,6 @@ cudaError_t launch_fwd_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) 
   dim3 grid(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B);
   fabwd_fwd_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, a);
   return cudaGetLastError();
-}
-
-template <bool FP16>
-cudaError_t launch_fwd_dispatch(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st) {
-  if (D == 64 && Dv == 64) return launch_fwd_t<64, 64, FP16>(a, m, st);
-  if (D == 128 && Dv == 128) return launch_fwd_t<128, 128, FP16>(a, m, st);
-  if (D == 192 && Dv == 128) return launch_fwd_t<192, 128, FP16>(a, m, st);
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace fabwd

@@ -29,9 +29,14 @@ constexpr int kBlockKV = 128;  // kv rows per CTA of the main kernel (M of the k
 constexpr int kBlockQ = 64;    // q rows per main-loop step (N of S^T / dP^T / dQ^T)
 constexpr int kRowPad = 128;   // padding of the per-(sequence, q-head) lse2 / sfmg rows
 constexpr int kDqBlockQ = 128; // q rows per CTA of the q-stationary dQ kernel
+// Head dims are built as 64, 128 and 192; any other D (or Dv), a multiple of 8, runs in the next
+// larger kernel: its TMA boxes read zeros past the row's last element, which add nothing to any
+// product, and the epilogues write the row's own elements only.
+constexpr int pad_dim(int d) { return d <= 64 ? 64 : d <= 128 ? 128 : 192; }
 // keys per step of the q-stationary dQ kernel: 96 at D = 192, where the dQ accumulator leaves
-// 320 TMEM columns for the two S buffers and dP
-constexpr int dq_block_kv(int D) { return D > 128 ? 96 : 128; }
+// 320 TMEM columns for the two S buffers and dP; 64 when Dv = 192 as well (the 48 KB dO tile
+// leaves shared memory for three 24 KB K stages and two V stages only)
+constexpr int dq_block_kv(int D, int DV) { return D > 128 ? (DV > 128 ? 64 : 96) : 128; }
 
 enum Layout : int { kBSND = 0, kTND = 1, kBNSD = 2 };
 
@@ -74,6 +79,8 @@ struct ConvArgs {
 
 struct MainArgs {
   int layout, B, N1, N2, G;
+  int io_d, io_dv;           // head dims of the io tensors: their row lengths (the kernel's
+                             // template dims are these rounded up by pad_dim)
   int S1, S2;                // sequence lengths (BSND/BNSD) or max_seqlen (TND)
   long long T1, T2;
   const int* cu_q;
@@ -128,33 +135,35 @@ cudaError_t launch_fill_f32(float* p, long long n, float v, cudaStream_t st);
 // Set the n entries of an lse array ([B][N1][S] or, tnd, [N1][S]) to their q-head's sink logit.
 cudaError_t launch_fill_lse_sinks(float* lse, const float* sinks, long long S, int N1, long long n, bool tnd,
                                   cudaStream_t st);
-// Return cudaErrorInvalidValue when no kernel is built for (D, Dv).  fused: the kv-stationary
-// kernel also reduces dQ into the fp32 accumulator; otherwise it writes dK, dV only.
-cudaError_t launch_main_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, bool fused,
-                             cudaStream_t st);
-cudaError_t launch_main_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, bool fused,
-                             cudaStream_t st);
-cudaError_t launch_dq_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
-// dK/dV-only kernel of the separate dQ mode; needs q-side maps with 128-row boxes up to D = 128 and
-// 64-row boxes at D = 192.  Returns cudaErrorInvalidValue for other head dims.
-cudaError_t launch_kv_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
-cudaError_t launch_kv_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
-cudaError_t launch_dq_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
+// Kernel launchers, one explicit instantiation per io dtype (FP16: fp16, else bf16), each in its
+// own translation unit.  D and Dv are kernel dims (pad_dim of the io dims); a launcher returns
+// cudaErrorInvalidValue when no kernel is built for them.
+// The fused kv-stationary kernel of the atomic dQ mode: dK, dV and the fp32 dQ accumulator.
+template <bool FP16>
+cudaError_t launch_main(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
+// The dK/dV kernel of the separate dQ mode; q-side maps with 128-row boxes up to D = 128 and
+// 64-row boxes at D = 192, kv-side maps with 128-row boxes.
+template <bool FP16>
+cudaError_t launch_kv(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
+// The q-stationary dQ kernel; q-side maps with 128-row boxes, kv-side with dq_block_kv(D, Dv).
+template <bool FP16>
+cudaError_t launch_dq(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
 // Both separate-mode kernels in one launch (dK/dV CTAs, then dQ CTAs); D <= 128, maps with
-// 128-row boxes on both sides.  Returns cudaErrorInvalidValue for other head dims.
-cudaError_t launch_bwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
-cudaError_t launch_bwd_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
-// The same for D > 128 (D = 192, Dv = 128): mkv are the dK/dV CTAs' maps (64-row query, 128-row
-// key boxes), mdq the dQ CTAs' (128-row query, 64-row key boxes).
-cudaError_t launch_bwd_wide_bf16(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int D, int Dv,
-                                 int n_kv_blocks, cudaStream_t st);
-cudaError_t launch_bwd_wide_fp16(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int D, int Dv,
-                                 int n_kv_blocks, cudaStream_t st);
+// 128-row boxes on both sides.
+template <bool FP16>
+cudaError_t launch_bwd(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks, cudaStream_t st);
+// The same for D = 192: mkv are the dK/dV CTAs' maps (64-row query, 128-row key boxes), mdq the
+// dQ CTAs' (128-row query boxes, dq_block_kv(D, Dv)-row key boxes).
+template <bool FP16>
+cudaError_t launch_bwd_wide(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int D, int Dv,
+                            int n_kv_blocks, cudaStream_t st);
 // Forward kernel (attn_out and softmax_lse); a.dq is attn_out, a.lse_out the lse rows, a.status the
 // status word.  Maps: q with 128-row boxes, k and v with 128-row (D <= 128) or 64-row boxes.
-cudaError_t launch_fwd_bf16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
-cudaError_t launch_fwd_fp16(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
-bool main_supported(int D, int Dv);
+template <bool FP16>
+cudaError_t launch_fwd(const MainArgs& a, const MainMaps& m, int D, int Dv, cudaStream_t st);
+// A kernel exists for (D, Dv) (before rounding by pad_dim); atomic: the fused dQ-reducing kernel,
+// whose TMEM plan leaves no room for Dv > 128 beside a dK of more than 128 columns.
+bool dims_supported(int D, int Dv, bool atomic);
 // binaryVersion (major * 10 + minor) of the library's kernels as loaded on the current device.
 cudaError_t kernel_binary_version(int* version);
 

@@ -50,7 +50,7 @@ struct KvCfg {
   static constexpr uint32_t oMisc = oBar + 20 * 8;
   static constexpr uint32_t bytes = oMisc + 64;
   static constexpr uint32_t cDK = 0, cDV = D, cS = D + DV, cP = cS + BR;
-  static_assert(D % 64 == 0 && DV % 64 == 0 && DV <= D && (D <= 128 || (D == 192 && DV == 128)), "head dims");
+  static_assert(D % 64 == 0 && DV % 64 == 0 && DV <= D && D <= 192, "head dims");
   static_assert(cP + BR <= 512, "TMEM budget");
   static_assert(bytes <= 232448, "shared memory budget");
 };
@@ -378,8 +378,8 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
     if (ok) {
       tc_fence_after();
       const long long krow = row_index(a.layout, b, (long long)(tnd ? sq.k0 : 0) + (j_valid ? jr : 0), n2, a.N2, a.S2);
-      uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * D;
-      uint16_t* dv = static_cast<uint16_t*>(a.dv) + krow * DV;
+      uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * a.io_d;
+      uint16_t* dv = static_cast<uint16_t*>(a.dv) + krow * a.io_dv;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         const int col = g * (D / 2) + c * 32;
@@ -394,7 +394,8 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
         if (j_valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
-            *reinterpret_cast<uint4*>(dk + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+            if (col + v4 * 8 < a.io_d)
+              *reinterpret_cast<uint4*>(dk + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
         }
       }
 #pragma unroll 1
@@ -411,7 +412,8 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
         if (j_valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
-            *reinterpret_cast<uint4*>(dv + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+            if (col + v4 * 8 < a.io_dv)
+              *reinterpret_cast<uint4*>(dv + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
         }
       }
     }

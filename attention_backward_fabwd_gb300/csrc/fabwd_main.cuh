@@ -1,5 +1,7 @@
-// Main FlashAttention backward kernel for sm_103a: warp-specialised tcgen05 + TMEM + TMA with two
-// ping-ponged TMEM slots.
+// Fused FlashAttention backward kernel of the atomic dQ mode for sm_103a: warp-specialised
+// tcgen05 + TMEM + TMA with two ping-ponged TMEM slots; all five products in one CTA, dQ reduced
+// into an fp32 workspace accumulator.  It also holds the helpers (sequence ranges, mask bounds,
+// bounded waits) that the other backward kernels share.
 //
 // What it computes is the backward of the page "CANN ops-transformer FlashAttnGrad 算子详解"
 // (discosf.com/news/4863418), §一.  One CTA owns a block of 128 keys of one kv-head and loops
@@ -45,7 +47,7 @@ constexpr unsigned long long kDrainNs = 100ull * 1000ull * 1000ull;  // 100 ms
 constexpr unsigned long long kGraceNs = 2ull * 1000ull * 1000ull;    // 2 ms
 constexpr int kMainThreads = 320;
 
-template <int D, int DV, bool FUSED>
+template <int D, int DV>
 struct MainCfg {
   static constexpr int BR = kBlockQ, BC = kBlockKV;
   // Head dims up to 128 leave TMEM room for two slots (ping-pong between the warpgroups); D = 192
@@ -54,12 +56,12 @@ struct MainCfg {
   static constexpr int NSLOT = D > 128 ? 1 : 2;
   static constexpr int NC = NSLOT == 2 ? 64 : 32;       // query columns per compute thread per step
   static constexpr int NS = D > 128 ? 3 : 4;            // Q/dO/lse/sfmg ring stages
-  static constexpr bool DQ2 = FUSED && D > 128;         // second dQᵀ product for head-dim rows 128..D-1
-  static constexpr int DK = FUSED && D < 128 ? 128 : D;  // K rows padded so dQᵀ = Kᵀ·dSᵀ has M = 128
+  static constexpr bool DQ2 = D > 128;               // second dQᵀ product for head-dim rows 128..D-1
+  static constexpr int DK = D < 128 ? 128 : D;           // K rows padded so dQᵀ = Kᵀ·dSᵀ has M = 128
   static constexpr uint32_t kK = DK * BC * 2, kV = DV * BC * 2, kQ = D * BR * 2, kdO = DV * BR * 2;
   static constexpr uint32_t kdS = BC * BR * 2;
   static constexpr uint32_t oK = 0, oV = oK + kK, oQ = oV + kV, odO = oQ + NS * kQ, odS = odO + NS * kdO;
-  static constexpr uint32_t oL = odS + (FUSED ? NSLOT * kdS : 0);  // [NS][BR] fp32 lse·log2(e)
+  static constexpr uint32_t oL = odS + NSLOT * kdS;  // [NS][BR] fp32 lse·log2(e)
   static constexpr uint32_t oF = oL + NS * BR * 4;    // [NS][BR] fp32 sfmg
   static constexpr uint32_t oBar = oF + NS * BR * 4;  // mbarriers
   static constexpr uint32_t oMisc = oBar + 48 * 8;    // TMEM base holder, abort flag
@@ -146,13 +148,12 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, vo
   return __all_sync(0xffffffffu, ok);
 }
 
-// FUSED: also compute dQᵀ and reduce it into the fp32 workspace accumulator (atomic dQ mode);
-// otherwise the kernel produces dK and dV only and a separate q-stationary kernel computes dQ.
-// One CTA of the kv-stationary kernel: key block bx / N2 of kv-head bx % N2, batch (or sequence) by.
-template <int D, int DV, bool FP16, bool FUSED>
+// One CTA of the fused kernel (atomic dQ mode): key block bx / N2 of kv-head bx % N2, batch (or
+// sequence) by; dK and dV into the outputs, dQᵀ reduced into the fp32 workspace accumulator.
+template <int D, int DV, bool FP16>
 __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                            const CUtensorMap& tm_do, const MainArgs& a, int bx, int by) {
-  using C = MainCfg<D, DV, FUSED>;
+  using C = MainCfg<D, DV>;
   constexpr int BR = C::BR, BC = C::BC, NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -282,9 +283,8 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
           mma_ss(slot, sdesc_sw128(aK + (kk >> 2) * BC * 128 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(aQ + (kk >> 2) * BR * 128 + (kk & 3) * 32, 16, 1024), ID_S, kk > 0);
         mma_commit(&bars[kSFull + g]);
-        // dPᵀ reuses the slot's dPᵀ/dQᵀ columns: wait until the previous dQᵀ was read (without
-        // dQ, the compute warps read the previous dPᵀ before their dS arrival, already awaited)
-        if (FUSED && use >= 1 && !wait_bar(&bars[kDqEmpty + g], (use - 1) & 1, abort_flag, a)) return false;
+        // dPᵀ reuses the slot's dPᵀ/dQᵀ columns: wait until the previous dQᵀ was read
+        if (use >= 1 && !wait_bar(&bars[kDqEmpty + g], (use - 1) & 1, abort_flag, a)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
@@ -317,7 +317,7 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
         for (int kk = 0; kk < BR / 16; ++kk)  // dSᵀ from TMEM (next to Pᵀ)
           mma_ts(tmem + C::cDK, slot + ds_col(kk), sdesc_sw128(aQ + kk * 2048, BR * 128, 1024), ID_DK,
                  (t > 0 || kk > 0) ? 1u : 0u);
-        if constexpr (FUSED) {
+        {
 #pragma unroll
           for (int kk = 0; kk < BC / 16; ++kk)
             mma_ss(slot + 64, sdesc_sw128(aK + kk * 2048, BC * 128, 1024), sdesc_sw128(adS + kk * 2048, BC * 128, 1024),
@@ -364,7 +364,7 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
     const int i_vis_lo = (int)(vlo < -1 ? -1 : (vlo > (1 << 30) ? (1 << 30) : vlo));
     const int i_vis_hi = (int)(vhi < -1 ? -1 : (vhi > (1 << 30) ? (1 << 30) : vhi));
     const uint32_t adS_row = smem_u32(smem + C::odS) + row * 128;
-    const long long i_stride = bnsd ? D : (long long)a.N1 * D;
+    const long long i_stride = bnsd ? a.io_d : (long long)a.N1 * a.io_d;
     bool ok = true;
     const int sg = C::NSLOT == 2 ? g : 0;  // the slot this warpgroup works on
     const uint32_t slot = tmem + lane_off + C::cSlot + sg * 128;
@@ -441,7 +441,7 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
           }
         }
         tmem_st16(ds_tmem + hh * 16, dk);  // dSᵀ (A operand of dK) next to Pᵀ
-        if constexpr (FUSED) {  // dSᵀ also in shared memory: the B operand of dQᵀ
+        {  // dSᵀ also in shared memory: the B operand of dQᵀ
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             st_shared_v4(adS + ((((cb / 8 + hh * 4 + v4) ^ (row & 7))) << 4), dk[4 * v4], dk[4 * v4 + 1],
@@ -449,11 +449,10 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
         }
       }
       tmem_wait_st();
-      if constexpr (FUSED) fence_proxy_async_smem();
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kDsFull + sg]);
-      if constexpr (!FUSED) continue;
       if (!(ok = wait_bar_warp(&bars[kDqFull + sg], u, abort_flag, a))) break;
       tc_fence_after();
       {
@@ -469,9 +468,9 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
           if (lane == 0) mbar_arrive(&bars[kDqEmpty + sg]);
         }
         const int nvalid = min(NC, sq.L1 - (i0 + cb));
-        if (row < D) {  // lane = head-dim index d; columns = queries i0 + cb .. + NC - 1
+        if (row < a.io_d) {  // lane = head-dim index d; columns = queries i0 + cb .. + NC - 1
           float* dst = a.dq_acc +
-                       row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 + cb : 0), n1, a.N1, a.S1) * D + row;
+                       row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 + cb : 0), n1, a.N1, a.S1) * a.io_d + row;
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (c < nvalid) red_add_f32(dst + c * i_stride, __uint_as_float(r0[c]));
@@ -490,9 +489,9 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kDqEmpty + sg]);
-          if (q4 >= 2) {
+          if (q4 >= 2 && 64 + row < a.io_d) {
             float* dst = a.dq_acc +
-                         row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 + cb : 0), n1, a.N1, a.S1) * D +
+                         row_index(a.layout, b, (long long)q_rowbase + (nvalid > 0 ? i0 + cb : 0), n1, a.N1, a.S1) * a.io_d +
                          64 + row;
 #pragma unroll
             for (int c = 0; c < 32; ++c)
@@ -506,8 +505,8 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
     if (ok) {
       tc_fence_after();
       const long long krow = row_index(a.layout, b, (long long)(tnd ? sq.k0 : 0) + (j_valid ? jr : 0), n2, a.N2, a.S2);
-      uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * D;
-      uint16_t* dv = static_cast<uint16_t*>(a.dv) + krow * DV;
+      uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * a.io_d;
+      uint16_t* dv = static_cast<uint16_t*>(a.dv) + krow * a.io_dv;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         const int col = g * (D / 2) + c * 32;
@@ -522,8 +521,9 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
         if (j_valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
-            *reinterpret_cast<uint4*>(dk + col + v4 * 8) =
-                make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+            if (col + v4 * 8 < a.io_d)
+              *reinterpret_cast<uint4*>(dk + col + v4 * 8) =
+                  make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
         }
       }
 #pragma unroll 1
@@ -540,8 +540,9 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
         if (j_valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
-            *reinterpret_cast<uint4*>(dv + col + v4 * 8) =
-                make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
+            if (col + v4 * 8 < a.io_dv)
+              *reinterpret_cast<uint4*>(dv + col + v4 * 8) =
+                  make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
         }
       }
     }
@@ -562,32 +563,23 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
   }
 }
 
-template <int D, int DV, bool FP16, bool FUSED>
+template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const MainArgs a) {
-  main_block<D, DV, FP16, FUSED>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
+  main_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
 }
 
-template <int D, int DV, bool FP16, bool FUSED>
+template <int D, int DV, bool FP16>
 cudaError_t launch_main_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
-  using C = MainCfg<D, DV, FUSED>;
-  if (cudaError_t e = ensure_smem_limit<fabwd_main_kernel<D, DV, FP16, FUSED>>((int)C::bytes); e != cudaSuccess) return e;
+  using C = MainCfg<D, DV>;
+  if (cudaError_t e = ensure_smem_limit<fabwd_main_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
   // blockIdx.x = kv-block * N2 + kv-head: the heaviest kv-blocks (earliest keys under a causal
   // mask) of every head launch first.
   dim3 grid(n_kv_blocks * a.N2, a.B);
-  fabwd_main_kernel<D, DV, FP16, FUSED><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
+  fabwd_main_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
   return cudaGetLastError();
-}
-
-template <bool FP16, bool FUSED>
-cudaError_t launch_main_dispatch(const MainArgs& a, const MainMaps& m, int D, int Dv, int n_kv_blocks,
-                                 cudaStream_t st) {
-  if (D == 64 && Dv == 64) return launch_main_t<64, 64, FP16, FUSED>(a, m, n_kv_blocks, st);
-  if (D == 128 && Dv == 128) return launch_main_t<128, 128, FP16, FUSED>(a, m, n_kv_blocks, st);
-  if (D == 192 && Dv == 128) return launch_main_t<192, 128, FP16, FUSED>(a, m, n_kv_blocks, st);
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace fabwd

@@ -95,7 +95,14 @@ typedef struct {
   /* Sizes ([FAG] §一 notation).  BSND/BNSD: S1, S2 are the sequence lengths.  TND: B is the
    * number of sequences, S1/S2 are max_seqlen_q/max_seqlen_kv (upper bounds of every
    * sequence's length) and T1/T2 the total token counts.  S1 = 0 or S2 = 0 (and empty TND
-   * sequences) are accepted: no pair is visible, so dq = dk = dv = 0. */
+   * sequences) are accepted: no pair is visible, so dq = dk = dv = 0.
+   * Head dims: 0 < Dv <= D <= 192 ([FAG] §4.6, else INVALID), and D, Dv multiples of 8 (rows of
+   * a multiple of 16 bytes for the TMA tensor maps and the 16-byte row stores; else
+   * UNSUPPORTED).  Kernels are built for 64, 128 and 192 ([FAG] §5.1's d_align / dv_align
+   * classes); another D or Dv runs in the next larger kernel, which reads zeros past the row's
+   * end and writes the row's own elements only.  FABWD_DQ_ATOMIC with both D > 128 and
+   * Dv > 128 is UNSUPPORTED (its fused kernel's accumulators leave no tensor memory for the
+   * step's products); the separate mode takes every pair. */
   int64_t B, S1, S2, N1, N2, D, Dv;
   int64_t T1, T2;
   /* Inputs: device pointers, io dtype, contiguous in the layout above, 16-byte aligned. */

@@ -105,9 +105,10 @@ def test_resolve_dq_mode(lib):
     (dict(softmax_scale=float("nan")), F.FABWD_ERR_INVALID),
     (dict(cu_seqlens_q=0x20000, cu_seqlens_kv=0x20000), F.FABWD_ERR_INVALID),  # non-TND with cu_seqlens
     (dict(layout=F.FABWD_TND), F.FABWD_ERR_INVALID),                            # TND without cu_seqlens
-    (dict(D=96, Dv=96), F.FABWD_ERR_UNSUPPORTED),    # valid per the statement, no kernel built
-    (dict(D=128, Dv=64), F.FABWD_ERR_UNSUPPORTED),
-    (dict(D=192, Dv=192), F.FABWD_ERR_UNSUPPORTED),
+    (dict(D=100, Dv=96), F.FABWD_ERR_UNSUPPORTED),   # valid per the statement; rows not 16-byte multiples
+    (dict(D=128, Dv=60), F.FABWD_ERR_UNSUPPORTED),
+    (dict(D=192, Dv=192, dq_mode=F.FABWD_DQ_ATOMIC), F.FABWD_ERR_UNSUPPORTED),   # no fused kernel for it
+    (dict(D=136, Dv=136, dq_mode=F.FABWD_DQ_ATOMIC), F.FABWD_ERR_UNSUPPORTED),
     (dict(dq_mode=3), F.FABWD_ERR_INVALID),
 ])
 def test_validation_codes(lib, change, code):
@@ -115,6 +116,16 @@ def test_validation_codes(lib, change, code):
     assert ws_size(p)[0] == code
     for fn in ("fabwd_preprocess", "fabwd_run", "fabwd_run_main", "fabwd_run_dq"):
         assert F.call_status(fn, p, 0x100000, 1 << 30, None) == code
+
+
+@pytest.mark.parametrize("D,Dv", [(64, 64), (128, 64), (128, 128), (192, 64), (192, 128), (192, 192), (8, 8),
+                                  (40, 8), (96, 96), (80, 48), (136, 72), (160, 136), (184, 176)])
+def test_head_dims_accepted(lib, D, Dv):
+    # every D, Dv <= D that is a multiple of 8 has a kernel (its own class or the next larger one);
+    # the atomic mode too unless both exceed 128
+    for mode in (F.FABWD_DQ_AUTO, F.FABWD_DQ_SEPARATE, F.FABWD_DQ_ATOMIC):
+        want = F.FABWD_ERR_UNSUPPORTED if mode == F.FABWD_DQ_ATOMIC and D > 128 and Dv > 128 else F.FABWD_OK
+        assert ws_size(base_params(D=D, Dv=Dv, dq_mode=mode))[0] == want, (D, Dv, mode)
 
 
 def test_null_and_workspace_codes(lib):
@@ -192,7 +203,7 @@ def test_forward_validation(lib):
     assert fw(0x30000, 0x30000, 0x100010, 256) == F.FABWD_ERR_WORKSPACE
     assert fw(0x30008, 0x30000, 0x100000, 256) == F.FABWD_ERR_INVALID       # attn_out not 16-byte aligned
     assert fw(0x30000, 0x30000, 0x100000, 256, pp=base_params(N1=3)) == F.FABWD_ERR_INVALID
-    assert fw(0x30000, 0x30000, 0x100000, 256, pp=base_params(D=96, Dv=96)) == F.FABWD_ERR_UNSUPPORTED
+    assert fw(0x30000, 0x30000, 0x100000, 256, pp=base_params(D=100, Dv=100)) == F.FABWD_ERR_UNSUPPORTED
     assert F.call_status("fabwd_forward", None, 0x30000, 0x30000, 0x100000, 256, None) == F.FABWD_ERR_NULLPTR
 
 

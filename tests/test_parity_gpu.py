@@ -70,7 +70,32 @@ SMALL = [
                                               S2=390, mask_mode=2, win_left=100, win_right=30), None),
     ("d192_tnd", inputs.sized(W["varlen_window_fp16_d128"], D=192, Dv=128, B=3, N1=2, N2=2, win_left=64),
      ([70, 1, 200], None)),
+    # the other head-dim classes of [FAG] §5.1 (d_align 64/128/192, Dv <= D), and dims between
+    # them, which run in the next larger kernel
+    ("d128_dv64_causal", inputs.sized(W["causal_b2_s2048_d128"], B=1, N1=2, N2=2, S1=300, S2=300, Dv=64), None),
+    ("d192_dv64_gqa_fp16_band", inputs.sized(W["causal_s8192_d192_dv128"], dtype="fp16", Dv=64, N1=4, N2=2, S1=260,
+                                             S2=390, mask_mode=2, win_left=100, win_right=30), None),
+    ("d192_dv192_causal", inputs.sized(W["causal_s8192_d192_dv128"], Dv=192, N1=2, N2=2, S1=300, S2=300), None),
+    ("d192_dv192_tnd_gqa", inputs.sized(W["varlen_window_fp16_d128"], D=192, Dv=192, B=3, N1=4, N2=2, win_left=64),
+     ([70, 1, 200], None)),
+    ("d96_causal", inputs.sized(W["causal_b2_s2048_d128"], B=1, N1=2, N2=2, S1=300, S2=300, D=96, Dv=96), None),
+    ("d80_dv48_bnsd_band", inputs.sized(W["mha_s128_d64"], layout="BNSD", S1=190, S2=250, D=80, Dv=48,
+                                        mask_mode=2, win_left=20, win_right=7), None),
+    ("d40_dv8_dense", inputs.sized(W["mha_s128_d64"], S1=150, S2=200, D=40, Dv=8), None),
+    ("d160_dv136_tnd_fp16", inputs.sized(W["varlen_window_fp16_d128"], D=160, Dv=136, B=3, N1=4, N2=2, win_left=64),
+     ([200, 33, 129], None)),
+    ("d136_dv72_gqa_causal", inputs.sized(W["gqa_causal_s4096_d128"], D=136, Dv=72, N1=4, N2=2, S1=260, S2=260,
+                                          dout_std=1.0), None),
 ]
+
+
+def _pad(d):
+    return 64 if d <= 64 else 128 if d <= 128 else 192
+
+
+def atomic_unsupported(w):
+    """The atomic mode's fused kernel has no room in tensor memory for D and Dv both above 128."""
+    return _pad(w.D) == 192 and _pad(w.Dv) == 192
 
 
 @pytest.mark.parametrize("dq_mode", ["separate", "atomic"])
@@ -78,6 +103,11 @@ SMALL = [
 def test_small_elementwise(name, w, lens, dq_mode):
     pb = inputs.make_problem(w, *(lens or ()))
     ref = tl.full_reference(pb)
+    if dq_mode == "atomic" and atomic_unsupported(w):
+        with pytest.raises(F.FabwdError) as ei:
+            tl.run_gpu(pb, ref, dq_mode=dq_mode)
+        assert ei.value.status == F.FABWD_ERR_UNSUPPORTED
+        return
     dq, dk, dv, sf = tl.run_gpu(pb, ref, dq_mode=dq_mode)
     check_all(pb, ref, dq, dk, dv, sf)
 
@@ -323,8 +353,8 @@ def test_full_size_elementwise(name, dq_mode, parity_report):
     parity_report(f"{name} [{dq_mode}]", errs)
 
 
-def test_unbuilt_head_dim_pair_is_unsupported():
-    q = torch.zeros(1, 256, 2, 96, dtype=torch.bfloat16, device="cuda")
+def test_head_dim_not_multiple_of_8_is_unsupported():
+    q = torch.zeros(1, 256, 2, 100, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(F.FabwdError) as ei:
         api.flash_attn_grad(q, q, q, q, q, torch.zeros(1, 2, 256, device="cuda"), mask_mode=1)
     assert ei.value.status == F.FABWD_ERR_UNSUPPORTED
