@@ -48,66 +48,70 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
 
   // Grid-stride over rows (b, n1, i), i over the padded length S1p: the order of the lse, lse2 and
   // sfmg rows, so that a warp's 4-byte reads and writes of them are contiguous (a row's dout and
-  // attn_out, 2·Dv bytes each, are whole 128-byte lines in any order).  Each lane group of LPR
-  // lanes takes UN rows per iteration, whose dout, attn_out and lse loads are all issued before
-  // the arithmetic.  SMALL: every row index fits 32 bits, so the index split uses 32-bit division.
+  // attn_out, 2·Dv bytes each, are whole 128-byte lines in any order).  A warp takes RPI
+  // consecutive rows per iteration, UN groups of RPW rows with LPR lanes per row, whose dout,
+  // attn_out and lse loads are all issued before the arithmetic.  RPI divides S1p (a multiple of
+  // 128), so the rows of an iteration share (b, n1) and one 128-row block: the index split, the
+  // sequence bounds and the first row's addresses are worked out once per iteration and stepped
+  // per row.  SMALL: every row index fits 32 bits, so the split uses 32-bit division.
   // DV is the kernel's row width (64, 128 or 192); a.Dv (a multiple of 8, at most DV) the rows'
   // own length: chunks past it are not read.
   constexpr int CPL = DV == 192 ? 3 : 1;  // 16-byte chunks (8 elements) per lane and row
   constexpr int LPR = DV / (8 * CPL);     // lanes per row (a power of two)
   constexpr int RPW = 32 / LPR;           // rows per warp step
-  constexpr int UN = 2;                   // row groups per iteration
-  const long long nrows = (long long)a.B * a.N1 * a.S1p;
+  constexpr int UN = 4;                   // row groups per iteration
+  constexpr int RPI = RPW * UN;           // rows per warp iteration
+  static_assert(kRowPad % RPI == 0, "an iteration's rows stay within one padded row block");
+  const long long ngroups = (long long)a.B * a.N1 * a.S1p / RPI;
   const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, part = lane % LPR;
   const bool tnd = a.layout == kTND;
-  for (long long base = gwarp * RPW * UN; base < nrows; base += nwarp * RPW * UN) {
+  const long long rstep = a.layout == kBNSD ? 1 : a.N1;  // row_index step from row i to i + 1
+  for (long long grp = gwarp; grp < ngroups; grp += nwarp) {
+    const long long base = grp * RPI;
+    int b, n1;
+    long long i0;
+    if (SMALL) {
+      const uint32_t w32 = (uint32_t)base, S1p = (uint32_t)a.S1p, N1 = (uint32_t)a.N1;
+      const uint32_t hq = w32 / S1p;
+      i0 = w32 - hq * S1p;
+      b = (int)(hq / N1);
+      n1 = (int)(hq - (uint32_t)b * N1);
+    } else {
+      i0 = base % a.S1p;
+      n1 = (int)((base / a.S1p) % a.N1);
+      b = (int)(base / ((long long)a.S1p * a.N1));
+    }
+    long long q0 = 0, L1 = a.S1;
+    if (tnd) {
+      q0 = a.cu_q[b];
+      L1 = (long long)a.cu_q[b + 1] - q0;
+      if (q0 < 0 || q0 > a.T1) L1 = 0;                 // bad cu_seqlens: touch nothing
+      L1 = L1 < 0 ? 0 : (L1 > a.S1 ? a.S1 : L1);
+      if (q0 + L1 > a.T1) L1 = a.T1 - q0 < 0 ? 0 : a.T1 - q0;
+    }
+    if (a.used_q) {  // rows past seqused are padding: lse2 = +inf, sfmg = 0
+      const long long us = a.used_q[b];
+      L1 = us < 0 ? 0 : (us < L1 ? us : L1);
+    }
+    // rows past the sequence's last 128-row block are never read by the backward kernels
+    if (tnd && i0 >= ((L1 + 127) / 128) * 128) continue;
+    const long long r0 = row_index(a.layout, b, q0 + i0, n1, a.N1, a.S1);
+    const long long li0 = tnd ? (long long)n1 * a.T1 + q0 + i0 : ((long long)b * a.N1 + n1) * a.S1 + i0;
     uint4 x[UN][CPL], y[UN][CPL];
     float l[UN];
-    bool act[UN], val[UN];
-    long long o[UN];
+    bool val[UN];
 #pragma unroll
     for (int u = 0; u < UN; ++u) {
-      const long long w = base + u * RPW + sub;
-      act[u] = w < nrows;
-      int b = 0, n1 = 0;
-      long long i = 0;
-      if (act[u]) {
-        if (SMALL) {
-          const uint32_t w32 = (uint32_t)w, S1p = (uint32_t)a.S1p, N1 = (uint32_t)a.N1;
-          const uint32_t hq = w32 / S1p;
-          i = w32 - hq * S1p;
-          b = (int)(hq / N1);
-          n1 = (int)(hq - (uint32_t)b * N1);
-        } else {
-          i = w % a.S1p;
-          n1 = (int)((w / a.S1p) % a.N1);
-          b = (int)(w / ((long long)a.S1p * a.N1));
-        }
-      }
-      long long q0 = 0, L1 = a.S1;
-      if (act[u] && tnd) {
-        q0 = a.cu_q[b];
-        L1 = (long long)a.cu_q[b + 1] - q0;
-        if (q0 < 0 || q0 > a.T1) L1 = 0;                 // bad cu_seqlens: touch nothing
-        L1 = L1 < 0 ? 0 : (L1 > a.S1 ? a.S1 : L1);
-        if (q0 + L1 > a.T1) L1 = a.T1 - q0 < 0 ? 0 : a.T1 - q0;
-      }
-      if (act[u] && a.used_q) {  // rows past seqused are padding: lse2 = +inf, sfmg = 0
-        const long long us = a.used_q[b];
-        L1 = us < 0 ? 0 : (us < L1 ? us : L1);
-      }
-      // rows past the sequence's last 128-row block are never read by the backward kernels
-      if (tnd && i >= ((L1 + 127) / 128) * 128) act[u] = false;
-      val[u] = act[u] && i < L1;
-      o[u] = ((long long)b * a.N1 + n1) * a.S1p + i;
+      const int di = u * RPW + sub;  // this lane group's row: i0 + di
+      val[u] = i0 + di < L1;
 #pragma unroll
       for (int k = 0; k < CPL; ++k) x[u][k] = y[u][k] = make_uint4(0u, 0u, 0u, 0u);
       l[u] = 0.f;
       if (val[u]) {
-        const long long r = row_index(a.layout, b, q0 + i, n1, a.N1, a.S1);
+        const long long r = r0 + di * rstep;
 #pragma unroll
         for (int k = 0; k < CPL; ++k) {
           const int col = (k * LPR + part) * 8;
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
           }
         }
         if (part == 0) {
-          const long long li = tnd ? (long long)n1 * a.T1 + q0 + i : ((long long)b * a.N1 + n1) * a.S1 + i;
+          const long long li = li0 + di;
           if (a.smax) {
             // (row maximum, row sum of exp(S - max)) -> lse; no visible key (sum <= 0) -> +inf
             const float m = a.smax[li * a.stat_stride], sm = a.ssum[li * a.stat_stride];
@@ -144,9 +148,10 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
       }
 #pragma unroll
       for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (act[u] && part == 0) {
-        a.lse2[o[u]] = val[u] ? l[u] * kLog2e : INFINITY;
-        a.sfmg[o[u]] = val[u] ? acc : 0.f;
+      if (part == 0) {
+        const long long o = base + u * RPW + sub;
+        a.lse2[o] = val[u] ? l[u] * kLog2e : INFINITY;
+        a.sfmg[o] = val[u] ? acc : 0.f;
       }
     }
   }

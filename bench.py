@@ -447,8 +447,8 @@ def stage_table(pb, r, peak_tf, peak_hbm):
 
 
 # revision of each kernel's code that profiles/traffic.json must match
-KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v3", "fabwd_kv_kernel": "kv-v5", "fabwd_dq_kernel": "dq-v5",
-              "fabwd_main_kernel": "main-v4"}
+KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v4", "fabwd_bwd_wide_kernel": "wide-v2", "fabwd_kv_kernel": "kv-v6",
+              "fabwd_dq_kernel": "dq-v6", "fabwd_main_kernel": "main-v5"}
 
 
 def max_over_ranks(values, world, device="cpu"):
