@@ -337,7 +337,10 @@ bool make_maps(const fabwd_params* p, MainMaps* maps, int q_rows, int kv_rows) {
   return make_map(&maps->q, p->q, fp16, p->layout, p->D, p->N1, Sq, Bn, q_rows) &&
          make_map(&maps->dout, p->dout, fp16, p->layout, p->Dv, p->N1, Sq, Bn, q_rows) &&
          make_map(&maps->k, p->k, fp16, p->layout, p->D, p->N2, Sk, Bn, kv_rows) &&
-         make_map(&maps->v, p->v, fp16, p->layout, p->Dv, p->N2, Sk, Bn, kv_rows);
+         make_map(&maps->v, p->v, fp16, p->layout, p->Dv, p->N2, Sk, Bn, kv_rows) &&
+         make_map(&maps->dq, p->dq, fp16, p->layout, p->D, p->N1, Sq, Bn, q_rows) &&
+         make_map(&maps->dk, p->dk, fp16, p->layout, p->D, p->N2, Sk, Bn, kv_rows) &&
+         make_map(&maps->dv, p->dv, fp16, p->layout, p->Dv, p->N2, Sk, Bn, kv_rows);
 }
 
 }  // namespace

@@ -54,6 +54,7 @@ struct DqCfg {
   static constexpr uint32_t bytes = oMisc + 64;
   static constexpr uint32_t cDQ = 0, cS0 = D, cP = D + 2 * BN;  // S buffer b at cS0 + b·BN
   static_assert(cP + BN <= 512, "TMEM budget");
+  static_assert(D / 64 * BM * 128 <= NK * kK, "dQ staging fits in the K ring");
   static_assert(bytes <= 232448, "shared memory budget");
 };
 
@@ -64,7 +65,8 @@ constexpr int kDqQdoFull = 0, kDqKFull = 1 /*+3*/, kDqKEmpty = 4 /*+3*/, kDqVFul
 // One CTA of the dQ kernel: query block (latest first) bx / N1 of q-head bx % N1, batch by.
 template <int D, int DV, bool FP16>
 __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                         const CUtensorMap& tm_do, const MainArgs& a, int bx, int by) {
+                                         const CUtensorMap& tm_do, const CUtensorMap& tm_dq, const MainArgs& a, int bx,
+                                         int by) {
   using C = DqCfg<D, DV>;
   constexpr int BM = C::BM, BN = C::BN, NK = C::NK, NV = C::NV, NC = C::NC;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -308,7 +310,43 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
     }
     // ---- epilogue: dq = scale · dQ (zeros when the row block sees no key)
     if (ok && T > 0) ok = wait_bar_warp(&bars[kDqAccDone], 0, abort_flag, a);
-    if (ok) {
+    // As in the dK/dV CTAs: a block whose 128 rows lie inside its sequence is staged in the
+    // drained K ring as 128-byte-swizzled 64-column tiles and written by TMA stores; the last
+    // block of a TND sequence is written row by row.
+    const bool staged = !tnd || i0 + BM <= sq.span_q;  // the same in every thread of the CTA
+    if (staged) {
+      tc_fence_after();
+      uint8_t* stage = smem + C::oK;  // D/64 tiles of BM·128 bytes
+#pragma unroll 1
+      for (int c = 0; ok && c < D / 64; ++c) {
+        const int col = g * (D / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cDQ + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * a.scale, __uint_as_float(r[e + 1]) * a.scale) : 0u;
+        uint8_t* rowp = stage + (col / 64) * BM * 128 + row * 128;
+        const int unit0 = (col % 64) / 8;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          st_shared_v4(smem_u32(rowp + (((unit0 + v4) ^ (row & 7)) << 4)), o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2],
+                       o[4 * v4 + 3]);
+      }
+      fence_proxy_async_smem();
+      // every compute thread reaches this barrier; the tiles are stored only if every warp wrote
+      // its part
+      const bool all_ok = compute_warps_all(ok);
+      if (all_ok && warp == 0 && lane == 0) {
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c)
+          tma_store_4d(&tm_dq, stage + c * BM * 128, c * 64, bnsd ? q_row : n1, bnsd ? n1 : q_row, bcoord);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the tiles are read before the CTA's shared memory is released
+      }
+    } else if (ok) {
       tc_fence_after();
       const bool i_valid = ir < sq.L1;
       const long long qrow = row_index(a.layout, b, (long long)(tnd ? sq.q0 : 0) + (i_valid ? ir : 0), n1, a.N1, a.S1);
@@ -353,8 +391,8 @@ template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const MainArgs a) {
-  dq_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
+                    const __grid_constant__ CUtensorMap tm_dq, const MainArgs a) {
+  dq_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dq, a, blockIdx.x, blockIdx.y);
 }
 
 template <int D, int DV, bool FP16>
@@ -362,7 +400,7 @@ cudaError_t launch_dq_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) {
   using C = DqCfg<D, DV>;
   if (cudaError_t e = ensure_smem_limit<fabwd_dq_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
   dim3 grid(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B);
-  fabwd_dq_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
+  fabwd_dq_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, m.dq, a);
   return cudaGetLastError();
 }
 

@@ -122,6 +122,7 @@ struct UnusedArgs {
 
 struct MainMaps {
   CUtensorMap q, k, v, dout;
+  CUtensorMap dq, dk, dv;  // outputs: dq with q's box, dk and dv with k's (TMA-stored epilogues)
 };
 
 cudaError_t launch_preprocess(const PreArgs& a, bool fp16, cudaStream_t st);

@@ -52,6 +52,7 @@ struct KvCfg {
   static constexpr uint32_t cDK = 0, cDV = D, cS = D + DV, cP = cS + BR;
   static_assert(D % 64 == 0 && DV % 64 == 0 && DV <= D && D <= 192, "head dims");
   static_assert(cP + BR <= 512, "TMEM budget");
+  static_assert((D / 64 + DV / 64) * BC * 128 <= NQ * kQ + NO * kdO, "dK/dV staging fits in the Q and dO rings");
   static_assert(bytes <= 232448, "shared memory budget");
 };
 
@@ -62,7 +63,8 @@ constexpr int kKvKvFull = 0, kKvQFull = 1 /*+3*/, kKvQEmpty = 4 /*+3*/, kKvOFull
 // One CTA of the dK/dV kernel: key block bx / N2 of kv-head bx % N2, batch (or sequence) by.
 template <int D, int DV, bool FP16>
 __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                         const CUtensorMap& tm_do, const MainArgs& a, int bx, int by) {
+                                         const CUtensorMap& tm_do, const CUtensorMap& tm_dk, const CUtensorMap& tm_dv,
+                                         const MainArgs& a, int bx, int by) {
   using C = KvCfg<D, DV>;
   constexpr int BR = C::BR, BC = C::BC, NQ = C::NQ, NO = C::NO;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -375,7 +377,63 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
     }
     // ---- epilogue: dK = scale · acc, dV = acc; zeros when no query sees this block
     if (ok && T > 0) ok = wait_bar_warp(&bars[kKvAccDone], 0, abort_flag, a);
-    if (ok) {
+    // A block whose 128 rows lie inside its sequence is staged in shared memory (the drained
+    // Q/dO rings) as 128-byte-swizzled 64-column tiles and written by TMA stores, one per tile;
+    // the last block of a TND sequence, whose box would reach into the next sequence's rows,
+    // is written row by row.  A thread's 16-byte stores to rows 2 KB or more apart would
+    // otherwise take one request each.
+    const bool staged = !tnd || j0 + BC <= sq.span_k;  // the same in every thread of the CTA
+    if (staged) {
+      tc_fence_after();
+      uint8_t* stage = smem + C::oQ;  // D/64 dK tiles, then Dv/64 dV tiles, BC·128 bytes each
+      auto put = [&](int tile, int unit0, const uint32_t (&o)[16]) {
+        uint8_t* rowp = stage + tile * BC * 128 + row * 128;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          st_shared_v4(smem_u32(rowp + (((unit0 + v4) ^ (row & 7)) << 4)), o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2],
+                       o[4 * v4 + 3]);
+      };
+#pragma unroll 1
+      for (int c = 0; ok && c < D / 64; ++c) {
+        const int col = g * (D / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cDK + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * -a.scale, __uint_as_float(r[e + 1]) * -a.scale) : 0u;
+        put(col / 64, (col % 64) / 8, o);
+      }
+#pragma unroll 1
+      for (int c = 0; ok && c < DV / 64; ++c) {
+        const int col = g * (DV / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cDV + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]), __uint_as_float(r[e + 1])) : 0u;
+        put(D / 64 + col / 64, (col % 64) / 8, o);
+      }
+      fence_proxy_async_smem();
+      // every compute thread reaches this barrier (staged is CTA-uniform); the tiles are stored
+      // only if every warp wrote its part
+      const bool all_ok = compute_warps_all(ok);
+      if (all_ok && warp == 0 && lane == 0) {
+#pragma unroll 1
+        for (int c = 0; c < D / 64 + DV / 64; ++c) {
+          const CUtensorMap* m = c < D / 64 ? &tm_dk : &tm_dv;
+          const int x = (c < D / 64 ? c : c - D / 64) * 64;
+          tma_store_4d(m, stage + c * BC * 128, x, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the tiles are read before the CTA's shared memory is released
+      }
+    } else if (ok) {
       tc_fence_after();
       const long long krow = row_index(a.layout, b, (long long)(tnd ? sq.k0 : 0) + (j_valid ? jr : 0), n2, a.N2, a.S2);
       uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * a.io_d;
@@ -438,8 +496,9 @@ template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const MainArgs a) {
-  kv_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
+  kv_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, blockIdx.x, blockIdx.y);
 }
 
 template <int D, int DV, bool FP16>
@@ -447,7 +506,7 @@ cudaError_t launch_kv_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, c
   using C = KvCfg<D, DV>;
   if (cudaError_t e = ensure_smem_limit<fabwd_kv_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
   dim3 grid(n_kv_blocks * a.N2, a.B);
-  fabwd_kv_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
+  fabwd_kv_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
   return cudaGetLastError();
 }
 

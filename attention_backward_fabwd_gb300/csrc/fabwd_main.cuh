@@ -81,6 +81,7 @@ constexpr int kKvFull = 0, kQFull = 1 /*+NS*/, kQEmpty = 5 /*+NS*/, kSFull = 9 /
 
 struct SeqRange {
   int q0, L1, k0, L2;
+  int span_q, span_k;  // the sequence's rows (TND: from cu_seqlens; else S1, S2), before seqused
 };
 
 // Rows of sequence (TND) or batch row b: its first q row and key row, and the lengths that take
@@ -101,6 +102,8 @@ __device__ __forceinline__ bool seq_range(const MainArgs& a, int b, SeqRange& r)
     r.k0 = 0;
     r.L2 = a.S2;
   }
+  r.span_q = r.L1;
+  r.span_k = r.L2;
   if (a.used_q) {
     const int u = a.used_q[b];
     if (u < 0 || u > r.L1) return false;

@@ -32,11 +32,12 @@ template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                     const MainArgs a, int kv_ctas) {
+                     const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                     const __grid_constant__ CUtensorMap tm_dv, const MainArgs a, int kv_ctas) {
   if ((int)blockIdx.x < kv_ctas)
-    kv_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
+    kv_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, blockIdx.x, blockIdx.y);
   else
-    dq_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x - kv_ctas, blockIdx.y);
+    dq_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dq, a, blockIdx.x - kv_ctas, blockIdx.y);
 }
 
 template <int D, int DV, bool FP16>
@@ -48,7 +49,7 @@ cudaError_t launch_bwd_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, 
   const int dq_ctas = ((a.S1 + DqCfg<D, DV>::BM - 1) / DqCfg<D, DV>::BM) * a.N1;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(kv_ctas + dq_ctas, a.B), kMainThreads, bytes, st, attr);
-  return cudaLaunchKernelEx(&cfg, fabwd_bwd_kernel<D, DV, FP16>, m.q, m.k, m.v, m.dout, a, kv_ctas);
+  return cudaLaunchKernelEx(&cfg, fabwd_bwd_kernel<D, DV, FP16>, m.q, m.k, m.v, m.dout, m.dq, m.dk, m.dv, a, kv_ctas);
 }
 
 // D > 128: the two CTA kinds take different tensor-map boxes (the dK/dV CTAs stream 64-row query
@@ -60,11 +61,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                           const __grid_constant__ CUtensorMap kvv, const __grid_constant__ CUtensorMap kdo,
                           const __grid_constant__ CUtensorMap qq, const __grid_constant__ CUtensorMap qk,
                           const __grid_constant__ CUtensorMap qv, const __grid_constant__ CUtensorMap qdo,
-                          const MainArgs a, int kv_ctas) {
+                          const __grid_constant__ CUtensorMap out_dq, const __grid_constant__ CUtensorMap out_dk,
+                          const __grid_constant__ CUtensorMap out_dv, const MainArgs a, int kv_ctas) {
   if ((int)blockIdx.x < kv_ctas)
-    kv_block<D, DV, FP16>(kq, kk, kvv, kdo, a, blockIdx.x, blockIdx.y);
+    kv_block<D, DV, FP16>(kq, kk, kvv, kdo, out_dk, out_dv, a, blockIdx.x, blockIdx.y);
   else
-    dq_block<D, DV, FP16>(qq, qk, qv, qdo, a, blockIdx.x - kv_ctas, blockIdx.y);
+    dq_block<D, DV, FP16>(qq, qk, qv, qdo, out_dq, a, blockIdx.x - kv_ctas, blockIdx.y);
 }
 
 template <int D, int DV, bool FP16>
@@ -78,7 +80,7 @@ cudaError_t launch_bwd_wide_t(const MainArgs& a, const MainMaps& mkv, const Main
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(kv_ctas + dq_ctas, a.B), kMainThreads, bytes, st, attr);
   return cudaLaunchKernelEx(&cfg, fabwd_bwd_wide_kernel<D, DV, FP16>, mkv.q, mkv.k, mkv.v, mkv.dout, mdq.q, mdq.k,
-                            mdq.v, mdq.dout, a, kv_ctas);
+                            mdq.v, mdq.dout, mdq.dq, mkv.dk, mkv.dv, a, kv_ctas);
 }
 
 }  // namespace fabwd
