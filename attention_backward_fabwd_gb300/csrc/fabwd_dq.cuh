@@ -17,16 +17,18 @@
 // take key columns [0, BN/2), warps 4-7 [BN/2, BN)), warp 8 issues TMA loads (Q, dO once; K
 // through a 3-stage ring released after dQ, V through a ring of NV stages released after dP), warp 9
 // allocates TMEM and issues the MMAs.  BN = 128 keys and NV = 2 up to D = 128; at D = 192, BN = 96
-// and NV = 1 (a second V stage does not fit beside Q, dO and three 36 KB K stages): V(t+1) then
-// loads once dP(t) has read V(t), while dQ(t−1) and S(t+1), queued behind dP(t), keep the tensor
-// pipe busy.  One thread issues every tcgen05.mma, and an MMA of these
+// and NV = 1 at Dv = 128 (a second V stage does not fit beside Q, dO and three 36 KB K stages).
+// One thread issues every tcgen05.mma, and an MMA of these
 // shapes occupies it about as long as the tensor pipe takes to run it, so each barrier wait
 // between MMA groups idles the pipe.  The MMA thread therefore issues
 //     [dS(t) written] dP(t+1), dQ(t), [K(t+2) landed] S(t+2)
 // (S is double-buffered, so S(t+2) reuses the buffer whose dS dQ(t) has just read), and the
 // compute warps, not the MMA thread, wait for V(t+1) before they signal dS(t): that wait falls
 // while the warps wait for dP anyway.  K(t+2) stays with the MMA thread: its stage is freed by
-// dQ(t-1), too late for the compute warps to vouch for it by dS(t).
+// dQ(t-1), too late for the compute warps to vouch for it by dS(t).  With one V stage, V(t+1)
+// can load only once dP(t) has read V(t), so the order is [dS(t)] dQ(t), [V(t+1)] dP(t+1),
+// [K(t+2)] S(t+2): the load overlaps dQ(t) and the MMA thread, not the compute warps, waits for
+// it (a phase trace had the compute warps waiting ~1000 clk per step for V(t+1) before dS(t)).
 // TMEM columns: dQ [0, D), S buffer 0 [D, D+BN), S buffer 1 [D+BN, D+2BN), dP [D+2BN, D+3BN).
 // Every mbarrier wait is bounded as in the kv-stationary kernel.
 #pragma once
@@ -199,10 +201,10 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
         if (T > 1) issue_s(1);
       }
       for (int t = 0; ok && t < T; ++t) {
-        // dS(t) written, dP(t) read by every compute warp, V(t+1) landed
+        // dS(t) written, dP(t) read by every compute warp (and, with two V stages, V(t+1) landed)
         if (!(ok = wait_bar(&bars[kDqDsFull], t & 1, abort_flag, a))) break;
         tc_fence_after();
-        if (t + 1 < T) issue_dp(t + 1);
+        if (NV > 1 && t + 1 < T) issue_dp(t + 1);
         const uint64_t dKt = sdesc_sw128(smem_u32(smem + C::oK + (t % NK) * C::kK), BN * 128, 1024);
         const uint32_t sb = tmem + C::cS0 + (t & 1) * BN;
 #pragma unroll
@@ -210,6 +212,11 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
           mma_ts(tmem + C::cDQ, sb + (kk / (NC / 16)) * NC + (kk % (NC / 16)) * 8,
                  sdesc_at(dKt, kk * 2048), ID_DQ, (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kDqKEmpty + (t % NK)]);
+        if (NV == 1 && t + 1 < T) {  // one V stage: V(t+1) has loaded while dQ(t) runs
+          if (!(ok = wait_bar(&bars[kDqVFull], (t + 1) & 1, abort_flag, a))) break;
+          tc_fence_after();
+          issue_dp(t + 1);
+        }
         if (t + 2 < T) {  // into the S buffer whose dS the dQ product above has read
           if (!(ok = wait_bar(&bars[kDqKFull + (t + 2) % NK], ((t + 2) / NK) & 1, abort_flag, a))) break;
           tc_fence_after();
@@ -269,8 +276,10 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
         for (int c = 0; c < NC; ++c)
           if (jc + c < j_vis_lo || jc + c > j_vis_hi) p[c] = 0u;
       }
-      // the MMA thread issues dP(t+1) right after the dS(t) handoff below: its V stage must have landed
-      if (t + 1 < T && !(ok = wait_bar_warp(&bars[kDqVFull + (t + 1) % NV], ((t + 1) / NV) & 1, abort_flag, a))) break;
+      // with two V stages the MMA thread issues dP(t+1) right after the dS(t) handoff below: its V
+      // stage must have landed
+      if (NV > 1 && t + 1 < T && !(ok = wait_bar_warp(&bars[kDqVFull + (t + 1) % NV], ((t + 1) / NV) & 1, abort_flag, a)))
+        break;
       if (!(ok = wait_bar_warp(&bars[kDqDpFull], t & 1, abort_flag, a))) break;
       tc_fence_after();
 #pragma unroll
