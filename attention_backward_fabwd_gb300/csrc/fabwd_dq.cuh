@@ -101,16 +101,57 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBar);
   uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::oMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oMisc + 16);
-  if (tid == 0) {
+  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
+  const int q_row = (tnd ? sq.q0 : 0) + i0;
+  const int kv_rowbase = tnd ? sq.k0 : 0;
+  const int bcoord = tnd ? 0 : b;
+  // key-block steps whose K and V tiles load during the set-up (the first NV: no stage to wait for)
+  const int early = T < NV ? T : NV;
+  auto load_k = [&](int t) {
+    const int sk = t % NK;
+    const int row = kv_rowbase + (kb_begin + t) * BN;
+    uint64_t* kfull = &bars[kDqKFull + sk];
+    mbar_arrive_expect_tx(kfull, D * BN * 2);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c)
+      tma_load_4d(smem + C::oK + sk * C::kK + c * BN * 128, &tm_k, kfull, c * 64, bnsd ? row : n2, bnsd ? n2 : row,
+                  bcoord);
+  };
+  auto load_v = [&](int t) {
+    const int sv = t % NV;
+    const int row = kv_rowbase + (kb_begin + t) * BN;
+    uint64_t* vfull = &bars[kDqVFull + sv];
+    mbar_arrive_expect_tx(vfull, DV * BN * 2);
+#pragma unroll
+    for (int c = 0; c < DV / 64; ++c)
+      tma_load_4d(smem + C::oV + sv * C::kV + c * BN * 128, &tm_v, vfull, c * 64, bnsd ? row : n2, bnsd ? n2 : row,
+                  bcoord);
+  };
+  if (warp == 8 && lane == 0) {
     for (int i = 0; i < kDqNumBars; ++i) mbar_init(&bars[i], i == kDqDsFull ? 8 : 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 8 && lane == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_do);
+    if (T > 0) {
+      // Q, dO and the first K, V tiles are inputs (the preprocess writes none of them): they load
+      // while the CTA allocates TMEM and waits for the preprocess
+      mbar_arrive_expect_tx(&bars[kDqQdoFull], (D + DV) * BM * 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_4d(smem + C::oQ + c * BM * 128, &tm_q, &bars[kDqQdoFull], c * 64, bnsd ? q_row : n1,
+                    bnsd ? n1 : q_row, bcoord);
+#pragma unroll
+      for (int c = 0; c < DV / 64; ++c)
+        tma_load_4d(smem + C::odO + c * BM * 128, &tm_do, &bars[kDqQdoFull], c * 64, bnsd ? q_row : n1,
+                    bnsd ? n1 : q_row, bcoord);
+      for (int t = 0; t < early; ++t) {
+        load_k(t);
+        load_v(t);
+      }
+    }
   }
   __syncwarp();
   if (warp == 9) tmem_alloc(tm_holder, 512);
@@ -128,41 +169,17 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
   }
   __syncthreads();
 
-  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
-  const int q_row = (tnd ? sq.q0 : 0) + i0;
-  const int kv_rowbase = tnd ? sq.k0 : 0;
-  const int bcoord = tnd ? 0 : b;
   constexpr bool kBF16 = !FP16;
 
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0 && T > 0 && !*abort_flag) {
-      mbar_arrive_expect_tx(&bars[kDqQdoFull], (D + DV) * BM * 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_4d(smem + C::oQ + c * BM * 128, &tm_q, &bars[kDqQdoFull], c * 64, bnsd ? q_row : n1,
-                    bnsd ? n1 : q_row, bcoord);
-#pragma unroll
-      for (int c = 0; c < DV / 64; ++c)
-        tma_load_4d(smem + C::odO + c * BM * 128, &tm_do, &bars[kDqQdoFull], c * 64, bnsd ? q_row : n1,
-                    bnsd ? n1 : q_row, bcoord);
-      for (int t = 0; t < T; ++t) {
+      for (int t = early; t < T; ++t) {  // the first `early` steps' tiles were issued above
         const int sk = t % NK, sv = t % NV;
-        const int row = kv_rowbase + (kb_begin + t) * BN;
         if (t >= NK && !wait_bar(&bars[kDqKEmpty + sk], ((t / NK) - 1) & 1, abort_flag, a)) break;
-        uint64_t* kfull = &bars[kDqKFull + sk];
-        mbar_arrive_expect_tx(kfull, D * BN * 2);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(smem + C::oK + sk * C::kK + c * BN * 128, &tm_k, kfull, c * 64, bnsd ? row : n2, bnsd ? n2 : row,
-                      bcoord);
+        load_k(t);
         if (t >= NV && !wait_bar(&bars[kDqVEmpty + sv], ((t / NV) - 1) & 1, abort_flag, a)) break;
-        uint64_t* vfull = &bars[kDqVFull + sv];
-        mbar_arrive_expect_tx(vfull, DV * BN * 2);
-#pragma unroll
-        for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(smem + C::oV + sv * C::kV + c * BN * 128, &tm_v, vfull, c * 64, bnsd ? row : n2,
-                      bnsd ? n2 : row, bcoord);
+        load_v(t);
       }
     }
     __syncwarp();

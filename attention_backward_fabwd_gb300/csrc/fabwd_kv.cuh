@@ -94,7 +94,11 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBar);
   uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::oMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oMisc + 16);
-  if (tid == 0) {
+  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
+  const int kv_row0 = tnd ? sq.k0 + j0 : j0;
+  const int q_rowbase = tnd ? sq.q0 : 0;
+  const int bcoord = tnd ? 0 : b;
+  if (warp == 8 && lane == 0) {
     for (int i = 0; i < kKvNumBars; ++i) {
       // P/dS handoffs: one arrival per compute warp; a dO stage: the dV commit + 8 compute warps
       const bool oe = i >= kKvOEmpty && i < kKvOEmpty + NO;
@@ -102,12 +106,35 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
     }
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 8 && lane == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_do);
+    if (T > 0) {
+      // K, V and the Q and dO tiles of step 0 are inputs (the preprocess writes none of them):
+      // they load while the CTA allocates TMEM and waits for the preprocess; step 0's lse and
+      // sfmg rows follow after that wait (the stages' byte counts include them)
+      mbar_arrive_expect_tx(&bars[kKvKvFull], (D + DV) * BC * 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_4d(smem + C::oK + c * BC * 128, &tm_k, &bars[kKvKvFull], c * 64, bnsd ? kv_row0 : n2,
+                    bnsd ? n2 : kv_row0, bcoord);
+#pragma unroll
+      for (int c = 0; c < DV / 64; ++c)
+        tma_load_4d(smem + C::oV + c * BC * 128, &tm_v, &bars[kKvKvFull], c * 64, bnsd ? kv_row0 : n2,
+                    bnsd ? n2 : kv_row0, bcoord);
+      const int row = q_rowbase + qb_begin * BR, n1 = n2 * a.G;
+      mbar_arrive_expect_tx(&bars[kKvQFull], D * BR * 2 + BR * 4);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_4d(smem + C::oQ + c * BR * 128, &tm_q, &bars[kKvQFull], c * 64, bnsd ? row : n1, bnsd ? n1 : row,
+                    bcoord);
+      mbar_arrive_expect_tx(&bars[kKvOFull], DV * BR * 2 + BR * 4);
+#pragma unroll
+      for (int c = 0; c < DV / 64; ++c)
+        tma_load_4d(smem + C::odO + c * BR * 128, &tm_do, &bars[kKvOFull], c * 64, bnsd ? row : n1,
+                    bnsd ? n1 : row, bcoord);
+    }
   }
   __syncwarp();
   if (warp == 9) tmem_alloc(tm_holder, 512);
@@ -125,25 +152,12 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
   }
   __syncthreads();
 
-  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
-  const int kv_row0 = tnd ? sq.k0 + j0 : j0;
-  const int q_rowbase = tnd ? sq.q0 : 0;
-  const int bcoord = tnd ? 0 : b;
   constexpr bool kBF16 = !FP16;
 
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0 && T > 0 && !*abort_flag) {
-      mbar_arrive_expect_tx(&bars[kKvKvFull], (D + DV) * BC * 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_4d(smem + C::oK + c * BC * 128, &tm_k, &bars[kKvKvFull], c * 64, bnsd ? kv_row0 : n2,
-                    bnsd ? n2 : kv_row0, bcoord);
-#pragma unroll
-      for (int c = 0; c < DV / 64; ++c)
-        tma_load_4d(smem + C::oV + c * BC * 128, &tm_v, &bars[kKvKvFull], c * 64, bnsd ? kv_row0 : n2,
-                    bnsd ? n2 : kv_row0, bcoord);
-      for (int t = 0; t < T; ++t) {
+      for (int t = 0; t < T; ++t) {  // step 0's tiles were issued during the set-up (above)
         const int sq_ = t % NQ, so = t % NO;
         const int h = t / nqb, qb = qb_begin + t % nqb;
         const int n1 = n2 * a.G + h, i0 = qb * BR;
@@ -151,19 +165,23 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
         const long long rbase = ((long long)b * a.N1 + n1) * a.S1p + i0;
         if (t >= NQ && !wait_bar(&bars[kKvQEmpty + sq_], ((t / NQ) - 1) & 1, abort_flag, a)) break;
         uint64_t* qfull = &bars[kKvQFull + sq_];
-        mbar_arrive_expect_tx(qfull, D * BR * 2 + BR * 4);
+        if (t > 0) {
+          mbar_arrive_expect_tx(qfull, D * BR * 2 + BR * 4);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(smem + C::oQ + sq_ * C::kQ + c * BR * 128, &tm_q, qfull, c * 64, bnsd ? row : n1,
-                      bnsd ? n1 : row, bcoord);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(smem + C::oQ + sq_ * C::kQ + c * BR * 128, &tm_q, qfull, c * 64, bnsd ? row : n1,
+                        bnsd ? n1 : row, bcoord);
+        }
         bulk_load(smem + C::oL + sq_ * BR * 4, a.lse2 + rbase, BR * 4, qfull);
         if (t >= NO && !wait_bar(&bars[kKvOEmpty + so], ((t / NO) - 1) & 1, abort_flag, a)) break;
         uint64_t* ofull = &bars[kKvOFull + so];
-        mbar_arrive_expect_tx(ofull, DV * BR * 2 + BR * 4);
+        if (t > 0) {
+          mbar_arrive_expect_tx(ofull, DV * BR * 2 + BR * 4);
 #pragma unroll
-        for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(smem + C::odO + so * C::kdO + c * BR * 128, &tm_do, ofull, c * 64, bnsd ? row : n1,
-                      bnsd ? n1 : row, bcoord);
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_4d(smem + C::odO + so * C::kdO + c * BR * 128, &tm_do, ofull, c * 64, bnsd ? row : n1,
+                        bnsd ? n1 : row, bcoord);
+        }
         bulk_load(smem + C::oF + so * BR * 4, a.sfmg + rbase, BR * 4, ofull);
       }
     }
