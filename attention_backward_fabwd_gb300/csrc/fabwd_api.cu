@@ -478,6 +478,13 @@ fabwd_status fabwd_forward(const fabwd_params* p, void* attn_out, float* softmax
   MainMaps maps;
   const int D = pad_dim((int)p->D), Dv = pad_dim((int)p->Dv);
   if (!make_maps(&f, &maps, 128, D > 128 ? 64 : 128)) return FABWD_ERR_CUDA;
+  // attn_out is written through the dq map's slot: rows of Dv elements, q's row count and box
+  {
+    const bool tnd = p->layout == FABWD_TND;
+    if (!make_map(&maps.dq, attn_out, p->dtype == FABWD_FP16, p->layout, p->Dv, p->N1, tnd ? p->T1 : p->S1,
+                  tnd ? 1 : p->B, 128))
+      return FABWD_ERR_CUDA;
+  }
   cudaError_t e = p->dtype == FABWD_FP16 ? launch_fwd<true>(a, maps, D, Dv, st) : launch_fwd<false>(a, maps, D, Dv, st);
   if (e == cudaSuccess) e = unused_rows(p, attn_out, softmax_lse, true, st);
   return e == cudaSuccess ? FABWD_OK : FABWD_ERR_CUDA;

@@ -48,6 +48,7 @@ struct FwdCfg {
   static_assert(cO + 2 * DV <= 512, "TMEM budget");
   static_assert(bytes <= 232448, "shared memory budget");
   static_assert(NC % 16 == 0 && DV % 64 == 0, "tile shapes");
+  static_assert(DV / 64 * BM * 128 <= NK * kK, "attn_out staging fits in the K ring");
 };
 
 constexpr int kFwQFull = 0, kFwKFull = 1 /*+3*/, kFwKEmpty = 4 /*+3*/, kFwVFull = 7 /*+3*/, kFwVEmpty = 10 /*+3*/,
@@ -56,7 +57,7 @@ constexpr int kFwQFull = 0, kFwKFull = 1 /*+3*/, kFwKEmpty = 4 /*+3*/, kFwVFull 
 // One CTA of the forward: query block (latest first) bx / N1 of q-head bx % N1, batch (or sequence) by.
 template <int D, int DV, bool FP16>
 __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                          const MainArgs& a, int bx, int by) {
+                                          const CUtensorMap& tm_y, const MainArgs& a, int bx, int by) {
   using C = FwdCfg<D, DV>;
   constexpr int BM = C::BM, BN = C::BN, NK = C::NK, NV = C::NV, NC = C::NC;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -91,15 +92,42 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBar);
   uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::oMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oMisc + 16);
-  if (tid == 0) {
+  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
+  const int q_row = (tnd ? sq.q0 : 0) + i0;
+  const int kv_rowbase = tnd ? sq.k0 : 0;
+  const int bcoord = tnd ? 0 : b;
+  auto load_k = [&](int t) {
+    const int sk = t % NK, row = kv_rowbase + (kb_begin + t) * BN;
+    mbar_arrive_expect_tx(&bars[kFwKFull + sk], D * BN * 2);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c)
+      tma_load_4d(smem + C::oK + sk * C::kK + c * BN * 128, &tm_k, &bars[kFwKFull + sk], c * 64, bnsd ? row : n2,
+                  bnsd ? n2 : row, bcoord);
+  };
+  auto load_v = [&](int t) {
+    const int sv = t % NV, row = kv_rowbase + (kb_begin + t) * BN;
+    mbar_arrive_expect_tx(&bars[kFwVFull + sv], DV * BN * 2);
+#pragma unroll
+    for (int c = 0; c < DV / 64; ++c)
+      tma_load_4d(smem + C::oV + sv * C::kV + c * BN * 128, &tm_v, &bars[kFwVFull + sv], c * 64, bnsd ? row : n2,
+                  bnsd ? n2 : row, bcoord);
+  };
+  if (warp == 8 && lane == 0) {
     for (int i = 0; i < kFwNumBars; ++i) mbar_init(&bars[i], i == kFwPFull ? 8 : 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 8 && lane == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    if (T > 0) {  // Q and the first K, V tiles load while the CTA allocates TMEM
+      mbar_arrive_expect_tx(&bars[kFwQFull], D * BM * 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_4d(smem + C::oQ + c * BM * 128, &tm_q, &bars[kFwQFull], c * 64, bnsd ? q_row : n1,
+                    bnsd ? n1 : q_row, bcoord);
+      load_k(0);
+      load_v(0);
+    }
   }
   __syncwarp();
   if (warp == 9) tmem_alloc(tm_holder, 512);
@@ -113,35 +141,17 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
   }
   __syncthreads();
 
-  const bool tnd = a.layout == kTND, bnsd = a.layout == kBNSD;
-  const int q_row = (tnd ? sq.q0 : 0) + i0;
-  const int kv_rowbase = tnd ? sq.k0 : 0;
-  const int bcoord = tnd ? 0 : b;
   constexpr bool kBF16 = !FP16;
 
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0 && T > 0 && !*abort_flag) {
-      mbar_arrive_expect_tx(&bars[kFwQFull], D * BM * 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_4d(smem + C::oQ + c * BM * 128, &tm_q, &bars[kFwQFull], c * 64, bnsd ? q_row : n1,
-                    bnsd ? n1 : q_row, bcoord);
-      for (int t = 0; t < T; ++t) {
+      for (int t = 1; t < T; ++t) {  // Q and step 0's K, V were issued during the set-up
         const int sk = t % NK, sv = t % NV;
-        const int row = kv_rowbase + (kb_begin + t) * BN;
         if (t >= NK && !wait_bar(&bars[kFwKEmpty + sk], ((t / NK) - 1) & 1, abort_flag, a)) break;
-        mbar_arrive_expect_tx(&bars[kFwKFull + sk], D * BN * 2);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(smem + C::oK + sk * C::kK + c * BN * 128, &tm_k, &bars[kFwKFull + sk], c * 64,
-                      bnsd ? row : n2, bnsd ? n2 : row, bcoord);
+        load_k(t);
         if (t >= NV && !wait_bar(&bars[kFwVEmpty + sv], ((t / NV) - 1) & 1, abort_flag, a)) break;
-        mbar_arrive_expect_tx(&bars[kFwVFull + sv], DV * BN * 2);
-#pragma unroll
-        for (int c = 0; c < DV / 64; ++c)
-          tma_load_4d(smem + C::oV + sv * C::kV + c * BN * 128, &tm_v, &bars[kFwVFull + sv], c * 64,
-                      bnsd ? row : n2, bnsd ? n2 : row, bcoord);
+        load_v(t);
       }
     }
     __syncwarp();
@@ -345,6 +355,11 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
       const float inv = L > 0.f ? 1.f / L : 0.f;
       const long long qrow = row_index(a.layout, b, (long long)(tnd ? sq.q0 : 0) + (i_valid ? ir : 0), n1, a.N1, a.S1);
       uint16_t* y = static_cast<uint16_t*>(a.dq) + qrow * a.io_dv;
+      // A block whose 128 rows lie inside its sequence is staged in the drained K ring as
+      // 128-byte-swizzled 64-column tiles and written by TMA stores (as the backward's epilogues);
+      // the last block of a TND sequence is written row by row.
+      const bool staged = !tnd || i0 + BM <= sq.span_q;
+      uint8_t* stage = smem + C::oK;
 #pragma unroll 1
       for (int c = 0; c < DV / 64; ++c) {
         const int col = g * (DV / 2) + c * 32;
@@ -362,16 +377,36 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
           o[e >> 1] = T > 0 ? pack2<FP16>((__uint_as_float(r0[e]) * c0 + __uint_as_float(r1[e]) * c1) * inv,
                                           (__uint_as_float(r0[e + 1]) * c0 + __uint_as_float(r1[e + 1]) * c1) * inv)
                             : 0u;
-        if (i_valid) {
+        if (staged) {
+          uint8_t* rowp = stage + (col / 64) * BM * 128 + row * 128;
+          const int unit0 = (col % 64) / 8;
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            st_shared_v4(smem_u32(rowp + (((unit0 + v4) ^ (row & 7)) << 4)), o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2],
+                         o[4 * v4 + 3]);
+        } else if (i_valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             if (col + v4 * 8 < a.io_dv)
               *reinterpret_cast<uint4*>(y + col + v4 * 8) = make_uint4(o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2], o[4 * v4 + 3]);
         }
       }
+      if (staged) fence_proxy_async_smem();
       if (g == 0 && i_valid) {
         const long long li = tnd ? (long long)n1 * a.T1 + sq.q0 + ir : ((long long)b * a.N1 + n1) * a.S1 + ir;
         a.lse_out[li] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : INFINITY;
+      }
+    }
+    // every compute thread reaches this barrier; the tiles are stored only if every warp wrote
+    // its part (staged is the same in every thread of the CTA)
+    if (!tnd || i0 + BM <= sq.span_q) {
+      const bool all_ok = compute_warps_all(ok);
+      if (all_ok && warp == 0 && lane == 0) {
+#pragma unroll 1
+        for (int c = 0; c < DV / 64; ++c)
+          tma_store_4d(&tm_y, smem + C::oK + c * BM * 128, c * 64, bnsd ? q_row : n1, bnsd ? n1 : q_row, bcoord);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the tiles are read before the CTA's shared memory is released
       }
     }
   }
@@ -394,8 +429,9 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
 template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const MainArgs a) {
-  fwd_block<D, DV, FP16>(tm_q, tm_k, tm_v, a, blockIdx.x, blockIdx.y);
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_y,
+                     const MainArgs a) {
+  fwd_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_y, a, blockIdx.x, blockIdx.y);
 }
 
 template <int D, int DV, bool FP16>
@@ -403,7 +439,7 @@ cudaError_t launch_fwd_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) 
   using C = FwdCfg<D, DV>;
   if (cudaError_t e = ensure_smem_limit<fabwd_fwd_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
   dim3 grid(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B);
-  fabwd_fwd_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, a);
+  fabwd_fwd_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dq, a);
   return cudaGetLastError();
 }
 
