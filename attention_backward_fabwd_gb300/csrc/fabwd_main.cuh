@@ -72,6 +72,7 @@ struct MainCfg {
   static_assert(D % 64 == 0 && DV % 64 == 0 && (D <= 128 || (D == 192 && DV <= 128)) && DV <= D, "head dims");
   static_assert(cDQ2 + (DQ2 ? 64 : 0) <= 512, "TMEM budget");
   static_assert(bytes <= 232448, "shared memory budget");
+  static_assert((D / 64 + DV / 64) * BC * 128 <= NS * (kQ + kdO), "dK/dV staging fits in the Q/dO ring");
 };
 
 // mbarrier indices
@@ -155,7 +156,8 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, vo
 // sequence) by; dK and dV into the outputs, dQᵀ reduced into the fp32 workspace accumulator.
 template <int D, int DV, bool FP16>
 __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                           const CUtensorMap& tm_do, const MainArgs& a, int bx, int by) {
+                                           const CUtensorMap& tm_do, const CUtensorMap& tm_dk, const CUtensorMap& tm_dv,
+                                           const MainArgs& a, int bx, int by) {
   using C = MainCfg<D, DV>;
   constexpr int BR = C::BR, BC = C::BC, NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -503,9 +505,47 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
         }
       }
     }
-    // ---- epilogue: dK = scale · acc, dV = acc; zeros when no query sees this block
+    // ---- epilogue: dK = scale · acc, dV = acc; zeros when no query sees this block.  Blocks
+    // inside their sequence are staged in the drained Q/dO ring and written by TMA stores, the
+    // last block of a TND sequence row by row (as in the separate mode's dK/dV CTAs).
     if (ok && T > 0) ok = wait_bar_warp(&bars[kAccDone], 0, abort_flag, a);
-    if (ok) {
+    const bool staged = !tnd || j0 + BC <= sq.span_k;  // the same in every thread of the CTA
+    if (staged) {
+      tc_fence_after();
+      uint8_t* stage = smem + C::oQ;  // D/64 dK tiles, then Dv/64 dV tiles, BC·128 bytes each
+#pragma unroll 1
+      for (int c = 0; ok && c < D / 64 + DV / 64; ++c) {
+        const bool kpart = c < D / 64;
+        const int col = kpart ? g * (D / 2) + c * 32 : g * (DV / 2) + (c - D / 64) * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + (kpart ? C::cDK : C::cDV) + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        const float s = kpart ? a.scale : 1.f;
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * s, __uint_as_float(r[e + 1]) * s) : 0u;
+        uint8_t* rowp = stage + ((kpart ? 0 : D / 64) + col / 64) * BC * 128 + row * 128;
+        const int unit0 = (col % 64) / 8;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          st_shared_v4(smem_u32(rowp + (((unit0 + v4) ^ (row & 7)) << 4)), o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2],
+                       o[4 * v4 + 3]);
+      }
+      fence_proxy_async_smem();
+      const bool all_ok = compute_warps_all(ok);  // every compute thread reaches this barrier
+      if (all_ok && warp == 0 && lane == 0) {
+#pragma unroll 1
+        for (int c = 0; c < D / 64 + DV / 64; ++c) {
+          const CUtensorMap* m = c < D / 64 ? &tm_dk : &tm_dv;
+          const int x = (c < D / 64 ? c : c - D / 64) * 64;
+          tma_store_4d(m, stage + c * BC * 128, x, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the tiles are read before the CTA's shared memory is released
+      }
+    } else if (ok) {
       tc_fence_after();
       const long long krow = row_index(a.layout, b, (long long)(tnd ? sq.k0 : 0) + (j_valid ? jr : 0), n2, a.N2, a.S2);
       uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * a.io_d;
@@ -570,8 +610,9 @@ template <int D, int DV, bool FP16>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                       const MainArgs a) {
-  main_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, a, blockIdx.x, blockIdx.y);
+  main_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, blockIdx.x, blockIdx.y);
 }
 
 template <int D, int DV, bool FP16>
@@ -581,7 +622,7 @@ cudaError_t launch_main_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks,
   // blockIdx.x = kv-block * N2 + kv-head: the heaviest kv-blocks (earliest keys under a causal
   // mask) of every head launch first.
   dim3 grid(n_kv_blocks * a.N2, a.B);
-  fabwd_main_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, a);
+  fabwd_main_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
   return cudaGetLastError();
 }
 
