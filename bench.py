@@ -448,7 +448,7 @@ def stage_table(pb, r, peak_tf, peak_hbm):
 
 # revision of each kernel's code that profiles/traffic.json must match
 KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v6", "fabwd_bwd_wide_kernel": "wide-v5", "fabwd_kv_kernel": "kv-v8",
-              "fabwd_dq_kernel": "dq-v9", "fabwd_main_kernel": "main-v5"}
+              "fabwd_dq_kernel": "dq-v9", "fabwd_main_kernel": "main-v6"}
 
 
 def max_over_ranks(values, world, device="cpu"):
