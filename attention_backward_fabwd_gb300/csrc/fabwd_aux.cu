@@ -46,14 +46,17 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
     if (bad) atomicOr(a.status, FABWD_DEV_BAD_SEQLENS);
   }
 
-  // Grid-stride over rows (b, n1, i), i over the padded length S1p: the order of the lse, lse2 and
-  // sfmg rows, so that a warp's 4-byte reads and writes of them are contiguous (a row's dout and
-  // attn_out, 2·Dv bytes each, are whole 128-byte lines in any order).  A warp takes RPI
-  // consecutive rows per iteration, UN groups of RPW rows with LPR lanes per row, whose dout,
-  // attn_out and lse loads are all issued before the arithmetic.  RPI divides S1p (a multiple of
-  // 128), so the rows of an iteration share (b, n1) and one 128-row block: the index split, the
-  // sequence bounds and the first row's addresses are worked out once per iteration and stepped
-  // per row.  SMALL: every row index fits 32 bits, so the split uses 32-bit division.
+  // Grid-stride over iterations of RPI consecutive rows (b, n1, i0 .. i0 + RPI - 1), i over the
+  // padded length S1p: the order of the lse, lse2 and sfmg rows, so that a warp's 4-byte reads
+  // and writes of them are contiguous (a row's dout and attn_out, 2·Dv bytes each, are whole
+  // 128-byte lines in any order).  Iterations go heads fastest, (b, i0, n1), so that the warps
+  // resident together read the rows of a few positions across all heads: in BSND and TND those
+  // are contiguous stretches of dout and attn_out.  An iteration is UN groups of RPW rows with
+  // LPR lanes per row, whose dout, attn_out and lse loads are all issued before the arithmetic.
+  // RPI divides S1p (a multiple of 128), so the rows of an iteration share (b, n1) and one
+  // 128-row block: the index split, the sequence bounds and the first row's addresses are worked
+  // out once per iteration and stepped per row.  SMALL: every row index fits 32 bits, so the
+  // split uses 32-bit division.
   // DV is the kernel's row width (64, 128 or 192); a.Dv (a multiple of 8, at most DV) the rows'
   // own length: chunks past it are not read.
   constexpr int CPL = DV == 192 ? 3 : 1;  // 16-byte chunks (8 elements) per lane and row
@@ -70,20 +73,23 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
   const bool tnd = a.layout == kTND;
   const long long rstep = a.layout == kBNSD ? 1 : a.N1;  // row_index step from row i to i + 1
   for (long long grp = gwarp; grp < ngroups; grp += nwarp) {
-    const long long base = grp * RPI;
     int b, n1;
     long long i0;
+    const int ipb = a.S1p / RPI;  // iterations per (b, n1)
     if (SMALL) {
-      const uint32_t w32 = (uint32_t)base, S1p = (uint32_t)a.S1p, N1 = (uint32_t)a.N1;
-      const uint32_t hq = w32 / S1p;
-      i0 = w32 - hq * S1p;
-      b = (int)(hq / N1);
-      n1 = (int)(hq - (uint32_t)b * N1);
+      const uint32_t g32 = (uint32_t)grp, N1 = (uint32_t)a.N1;
+      const uint32_t t = g32 / N1;
+      n1 = (int)(g32 - t * N1);
+      const uint32_t bb = t / (uint32_t)ipb;
+      b = (int)bb;
+      i0 = (long long)(t - bb * (uint32_t)ipb) * RPI;
     } else {
-      i0 = base % a.S1p;
-      n1 = (int)((base / a.S1p) % a.N1);
-      b = (int)(base / ((long long)a.S1p * a.N1));
+      n1 = (int)(grp % a.N1);
+      const long long t = grp / a.N1;
+      b = (int)(t / ipb);
+      i0 = (t % ipb) * RPI;
     }
+    const long long base = ((long long)b * a.N1 + n1) * a.S1p + i0;  // first lse2 / sfmg row
     long long q0 = 0, L1 = a.S1;
     if (tnd) {
       q0 = a.cu_q[b];

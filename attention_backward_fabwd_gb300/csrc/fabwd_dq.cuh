@@ -64,11 +64,12 @@ constexpr int kDqQdoFull = 0, kDqKFull = 1 /*+3*/, kDqKEmpty = 4 /*+3*/, kDqVFul
               kDqSFull = 11 /*+2*/, kDqDpFull = 13, kDqDsFull = 14, kDqAccDone = 15, kDqNever = 16, kDqDrain = 17,
               kDqNumBars = 18;
 
-// One CTA of the dQ kernel: query block (latest first) bx / N1 of q-head bx % N1, batch by.
+// One CTA of the dQ kernel: query block nqb - 1 - bx / N1 (latest first) of q-head bx % N1,
+// batch by; nqb counts the BM-row query blocks of the batch row (or sequence) that bx runs over.
 template <int D, int DV, bool FP16>
 __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                          const CUtensorMap& tm_do, const CUtensorMap& tm_dq, const MainArgs& a, int bx,
-                                         int by) {
+                                         int by, int nqb) {
   using C = DqCfg<D, DV>;
   constexpr int BM = C::BM, BN = C::BN, NK = C::NK, NV = C::NV, NC = C::NC;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -77,10 +78,9 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
   const int b = by;
   SeqRange sq;
   if (!seq_range(a, b, sq)) return;  // bad cu_seqlens: the preprocess kernel reports it
-  const int nqb_all = (a.S1 + BM - 1) / BM;
-  const int qb = nqb_all - 1 - bx / a.N1, n1 = bx % a.N1;  // latest query blocks first
+  const int qb = nqb - 1 - bx / a.N1, n1 = bx % a.N1;  // latest query blocks first
   const int i0 = qb * BM;
-  if (i0 >= sq.L1) return;
+  if (qb < 0 || i0 >= sq.L1) return;
   if ((smem_u32(smem) & 1023u) != 0) {
     griddep_wait();  // the preprocess clears the status word
     if (tid == 0) atomicOr(a.status, FABWD_DEV_INTERNAL);
@@ -413,21 +413,38 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
   }
 }
 
-template <int D, int DV, bool FP16>
+template <int D, int DV, bool FP16, bool FLAT>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq, const MainArgs a) {
-  dq_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dq, a, blockIdx.x, blockIdx.y);
+  using C = DqCfg<D, DV>;
+  if constexpr (FLAT) {  // varlen: the sequences' own query blocks back to back
+    int b, local, nqb;
+    bool kv;
+    if (!flat_unit(a, blockIdx.x, 0, C::BM, b, local, kv, nqb)) return;
+    dq_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dq, a, local, b, nqb);
+  } else {
+    dq_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dq, a, blockIdx.x, blockIdx.y, (a.S1 + C::BM - 1) / C::BM);
+  }
+}
+
+template <int D, int DV, bool FP16, bool FLAT>
+cudaError_t launch_dq_flat(const MainArgs& a, const MainMaps& m, dim3 grid, cudaStream_t st) {
+  using C = DqCfg<D, DV>;
+  if (cudaError_t e = ensure_smem_limit<fabwd_dq_kernel<D, DV, FP16, FLAT>>((int)C::bytes); e != cudaSuccess)
+    return e;
+  fabwd_dq_kernel<D, DV, FP16, FLAT><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, m.dq, a);
+  return cudaGetLastError();
 }
 
 template <int D, int DV, bool FP16>
 cudaError_t launch_dq_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) {
   using C = DqCfg<D, DV>;
-  if (cudaError_t e = ensure_smem_limit<fabwd_dq_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
-  dim3 grid(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B);
-  fabwd_dq_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, m.dq, a);
-  return cudaGetLastError();
+  if (a.layout == kTND)
+    return launch_dq_flat<D, DV, FP16, true>(
+        a, m, dim3((unsigned)(tnd_blocks_bound(a.B, a.S1, a.T1, C::BM) * a.N1), 1), st);
+  return launch_dq_flat<D, DV, FP16, false>(a, m, dim3(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B), st);
 }
 
 }  // namespace fabwd

@@ -54,10 +54,11 @@ struct FwdCfg {
 constexpr int kFwQFull = 0, kFwKFull = 1 /*+3*/, kFwKEmpty = 4 /*+3*/, kFwVFull = 7 /*+3*/, kFwVEmpty = 10 /*+3*/,
               kFwSFull = 13 /*+2*/, kFwPFull = 15, kFwOFull = 16, kFwNever = 17, kFwDrain = 18, kFwNumBars = 19;
 
-// One CTA of the forward: query block (latest first) bx / N1 of q-head bx % N1, batch (or sequence) by.
+// One CTA of the forward: query block nqb - 1 - bx / N1 (latest first) of q-head bx % N1, batch (or
+// sequence) by; nqb counts the BM-row query blocks of the batch row (or sequence) that bx runs over.
 template <int D, int DV, bool FP16>
 __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                          const CUtensorMap& tm_y, const MainArgs& a, int bx, int by) {
+                                          const CUtensorMap& tm_y, const MainArgs& a, int bx, int by, int nqb) {
   using C = FwdCfg<D, DV>;
   constexpr int BM = C::BM, BN = C::BN, NK = C::NK, NV = C::NV, NC = C::NC;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -69,10 +70,9 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
     if (tid == 0) atomicOr(a.status, FABWD_DEV_BAD_SEQLENS);
     return;
   }
-  const int nqb_all = (a.S1 + BM - 1) / BM;
-  const int qb = nqb_all - 1 - bx / a.N1, n1 = bx % a.N1;  // latest query blocks first
+  const int qb = nqb - 1 - bx / a.N1, n1 = bx % a.N1;  // latest query blocks first
   const int i0 = qb * BM;
-  if (i0 >= sq.L1) return;
+  if (qb < 0 || i0 >= sq.L1) return;
   if ((smem_u32(smem) & 1023u) != 0) {
     if (tid == 0) atomicOr(a.status, FABWD_DEV_INTERNAL);
     return;
@@ -426,21 +426,45 @@ __device__ __forceinline__ void fwd_block(const CUtensorMap& tm_q, const CUtenso
   }
 }
 
-template <int D, int DV, bool FP16>
+template <int D, int DV, bool FP16, bool FLAT>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_y,
                      const MainArgs a) {
-  fwd_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_y, a, blockIdx.x, blockIdx.y);
+  using C = FwdCfg<D, DV>;
+  if constexpr (FLAT) {  // varlen: the sequences' own query blocks back to back
+    if (blockIdx.x == 0) {
+      // a sequence with a negative span owns no CTA: its cu_seqlens are checked here
+      for (int s = threadIdx.x; s < a.B; s += blockDim.x) {
+        SeqRange r;
+        if (!seq_range(a, s, r)) atomicOr(a.status, FABWD_DEV_BAD_SEQLENS);
+      }
+    }
+    int b, local, nqb;
+    bool kv;
+    if (!flat_unit(a, blockIdx.x, 0, C::BM, b, local, kv, nqb)) return;
+    fwd_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_y, a, local, b, nqb);
+  } else {
+    fwd_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_y, a, blockIdx.x, blockIdx.y, (a.S1 + C::BM - 1) / C::BM);
+  }
+}
+
+template <int D, int DV, bool FP16, bool FLAT>
+cudaError_t launch_fwd_flat(const MainArgs& a, const MainMaps& m, dim3 grid, cudaStream_t st) {
+  using C = FwdCfg<D, DV>;
+  if (cudaError_t e = ensure_smem_limit<fabwd_fwd_kernel<D, DV, FP16, FLAT>>((int)C::bytes); e != cudaSuccess)
+    return e;
+  fabwd_fwd_kernel<D, DV, FP16, FLAT><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dq, a);
+  return cudaGetLastError();
 }
 
 template <int D, int DV, bool FP16>
 cudaError_t launch_fwd_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) {
   using C = FwdCfg<D, DV>;
-  if (cudaError_t e = ensure_smem_limit<fabwd_fwd_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
-  dim3 grid(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B);
-  fabwd_fwd_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dq, a);
-  return cudaGetLastError();
+  if (a.layout == kTND)
+    return launch_fwd_flat<D, DV, FP16, true>(
+        a, m, dim3((unsigned)(tnd_blocks_bound(a.B, a.S1, a.T1, C::BM) * a.N1), 1), st);
+  return launch_fwd_flat<D, DV, FP16, false>(a, m, dim3(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B), st);
 }
 
 }  // namespace fabwd

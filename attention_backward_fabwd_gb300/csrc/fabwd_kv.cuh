@@ -510,22 +510,38 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
   }
 }
 
-template <int D, int DV, bool FP16>
+template <int D, int DV, bool FP16, bool FLAT>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const MainArgs a) {
-  kv_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, blockIdx.x, blockIdx.y);
+  if constexpr (FLAT) {  // varlen: the sequences' own key blocks back to back
+    int b, local, nqb;
+    bool kv;
+    if (!flat_unit(a, blockIdx.x, KvCfg<D, DV>::BC, 0, b, local, kv, nqb)) return;
+    kv_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, local, b);
+  } else {
+    kv_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, blockIdx.x, blockIdx.y);
+  }
+}
+
+template <int D, int DV, bool FP16, bool FLAT>
+cudaError_t launch_kv_flat(const MainArgs& a, const MainMaps& m, dim3 grid, cudaStream_t st) {
+  using C = KvCfg<D, DV>;
+  if (cudaError_t e = ensure_smem_limit<fabwd_kv_kernel<D, DV, FP16, FLAT>>((int)C::bytes); e != cudaSuccess)
+    return e;
+  fabwd_kv_kernel<D, DV, FP16, FLAT><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
+  return cudaGetLastError();
 }
 
 template <int D, int DV, bool FP16>
 cudaError_t launch_kv_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
   using C = KvCfg<D, DV>;
-  if (cudaError_t e = ensure_smem_limit<fabwd_kv_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
-  dim3 grid(n_kv_blocks * a.N2, a.B);
-  fabwd_kv_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
-  return cudaGetLastError();
+  if (a.layout == kTND)
+    return launch_kv_flat<D, DV, FP16, true>(
+        a, m, dim3((unsigned)(tnd_blocks_bound(a.B, a.S2, a.T2, C::BC) * a.N2), 1), st);
+  return launch_kv_flat<D, DV, FP16, false>(a, m, dim3(n_kv_blocks * a.N2, a.B), st);
 }
 
 }  // namespace fabwd

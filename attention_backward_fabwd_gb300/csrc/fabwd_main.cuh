@@ -118,6 +118,51 @@ __device__ __forceinline__ bool seq_range(const MainArgs& a, int b, SeqRange& r)
   return true;
 }
 
+// Work unit f of a varlen grid.  Sequence b owns ceil(L2_b / kv_rows) · N2 dK/dV units (none
+// when kv_rows is 0) followed by ceil(L1_b / q_rows) · N1 dQ units (none when q_rows is 0), the
+// sequences back to back, L1_b / L2_b their cu_seqlens spans clamped to [0, max_seqlen].  Gives
+// the sequence, whether the unit is a dK/dV one, its index among that kind's units of the
+// sequence and the sequence's count of q_rows-row query blocks; false past the last unit.  Each
+// warp scans the sequences 32 at a time (lane = sequence), so every thread of the CTA gets the
+// result without shared memory; called by whole warps.
+__device__ __forceinline__ bool flat_unit(const MainArgs& a, long long f, int kv_rows, int q_rows, int& b,
+                                          int& local, bool& kv, int& nqb) {
+  const int lane = threadIdx.x & 31;
+  long long base = 0;  // units of the sequences before this group of 32
+  for (int c0 = 0; c0 < a.B; c0 += 32) {
+    const int s = c0 + lane;
+    long long lq = 0, lk = 0;
+    if (s < a.B) {
+      lq = (long long)a.cu_q[s + 1] - a.cu_q[s];
+      lk = (long long)a.cu_kv[s + 1] - a.cu_kv[s];
+      lq = lq < 0 ? 0 : (lq > a.S1 ? a.S1 : lq);
+      lk = lk < 0 ? 0 : (lk > a.S2 ? a.S2 : lk);
+    }
+    const long long nk = kv_rows > 0 ? (lk + kv_rows - 1) / kv_rows * a.N2 : 0;
+    const long long nq = q_rows > 0 ? (lq + q_rows - 1) / q_rows * a.N1 : 0;
+    long long incl = nk + nq;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const long long excl = incl - nk - nq;
+    const unsigned hit = __ballot_sync(0xffffffffu, f >= base + excl && f < base + incl);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      const long long r = f - base - __shfl_sync(0xffffffffu, excl, src);
+      const long long nks = __shfl_sync(0xffffffffu, nk, src);
+      b = c0 + src;
+      kv = r < nks;
+      local = (int)(kv ? r : r - nks);
+      nqb = q_rows > 0 ? (int)((__shfl_sync(0xffffffffu, lq, src) + q_rows - 1) / q_rows) : 0;
+      return true;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return false;
+}
+
 // Visible pairs satisfy lo <= j - i - (L2 - L1) <= hi.
 __device__ __forceinline__ void mask_bounds(const MainArgs& a, long long& lo, long long& hi) {
   const long long INF = 1ll << 40;
@@ -606,24 +651,39 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
   }
 }
 
-template <int D, int DV, bool FP16>
+template <int D, int DV, bool FP16, bool FLAT>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fabwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                       const MainArgs a) {
-  main_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, blockIdx.x, blockIdx.y);
+  if constexpr (FLAT) {  // varlen: the sequences' own key blocks back to back
+    int b, local, nqb;
+    bool kv;
+    if (!flat_unit(a, blockIdx.x, kBlockKV, 0, b, local, kv, nqb)) return;
+    main_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, local, b);
+  } else {
+    main_block<D, DV, FP16>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, blockIdx.x, blockIdx.y);
+  }
+}
+
+template <int D, int DV, bool FP16, bool FLAT>
+cudaError_t launch_main_flat(const MainArgs& a, const MainMaps& m, dim3 grid, cudaStream_t st) {
+  using C = MainCfg<D, DV>;
+  if (cudaError_t e = ensure_smem_limit<fabwd_main_kernel<D, DV, FP16, FLAT>>((int)C::bytes); e != cudaSuccess)
+    return e;
+  fabwd_main_kernel<D, DV, FP16, FLAT><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
+  return cudaGetLastError();
 }
 
 template <int D, int DV, bool FP16>
 cudaError_t launch_main_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
-  using C = MainCfg<D, DV>;
-  if (cudaError_t e = ensure_smem_limit<fabwd_main_kernel<D, DV, FP16>>((int)C::bytes); e != cudaSuccess) return e;
   // blockIdx.x = kv-block * N2 + kv-head: the heaviest kv-blocks (earliest keys under a causal
   // mask) of every head launch first.
-  dim3 grid(n_kv_blocks * a.N2, a.B);
-  fabwd_main_kernel<D, DV, FP16><<<grid, kMainThreads, C::bytes, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
-  return cudaGetLastError();
+  if (a.layout == kTND)
+    return launch_main_flat<D, DV, FP16, true>(
+        a, m, dim3((unsigned)(tnd_blocks_bound(a.B, a.S2, a.T2, kBlockKV) * a.N2), 1), st);
+  return launch_main_flat<D, DV, FP16, false>(a, m, dim3(n_kv_blocks * a.N2, a.B), st);
 }
 
 }  // namespace fabwd

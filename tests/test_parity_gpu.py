@@ -65,6 +65,10 @@ SMALL = [
                                         win_left=-1, win_right=-1), ([200, 33, 129], [90, 300, 129])),
     ("tnd_causal_unequal", inputs.sized(W["varlen_window_fp16_d128"], B=3, N1=2, N2=1, win_left=-1),
      ([200, 33, 300], [150, 60, 300])),
+    # more sequences than a warp has lanes (the varlen grid's unit scan runs over groups of 32),
+    # empty ones among them, q and kv lengths unequal
+    ("tnd_many_sequences", inputs.sized(W["varlen_window_fp16_d128"], B=37, N1=2, N2=1, win_left=64),
+     ([(i * 53) % 190 for i in range(37)], [(i * 71 + 5) % 160 for i in range(37)])),
     ("d192_dv128_causal", inputs.sized(W["causal_s8192_d192_dv128"], N1=2, N2=2, S1=300, S2=300), None),
     ("d192_dv128_gqa_fp16_band", inputs.sized(W["causal_s8192_d192_dv128"], dtype="fp16", N1=4, N2=2, S1=260,
                                               S2=390, mask_mode=2, win_left=100, win_right=30), None),
