@@ -63,6 +63,9 @@ def parse_args():
     ap.add_argument("--no-forward", action="store_true", help="skip the untimed pass that times fabwd_forward")
     ap.add_argument("--no-breakdown", action="store_true",
                     help="skip the untimed pass that launches the dK/dV and dQ kernels on their own")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="run the chosen BSND/BNSD workload at S1 = S2 = this length: a smaller case of the same "
+                         "kernels for profiler captures; the JSON line names the sized workload")
     ap.add_argument("--workloads", default="all",
                     help="comma-separated workloads whose step is timed beside the headline one, 'all' or 'none'")
     return ap.parse_args()
@@ -447,8 +450,8 @@ def stage_table(pb, r, peak_tf, peak_hbm):
 
 
 # revision of each kernel's code that profiles/traffic.json must match
-KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v6", "fabwd_bwd_wide_kernel": "wide-v5", "fabwd_kv_kernel": "kv-v8",
-              "fabwd_dq_kernel": "dq-v9", "fabwd_main_kernel": "main-v6"}
+KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v7", "fabwd_bwd_wide_kernel": "wide-v6", "fabwd_kv_kernel": "kv-v9",
+              "fabwd_dq_kernel": "dq-v10", "fabwd_main_kernel": "main-v7"}
 
 
 def max_over_ranks(values, world, device="cpu"):
@@ -466,6 +469,18 @@ def max_over_ranks(values, world, device="cpu"):
 def job_tflops(flops_per_rank, world, ms):
     """Whole-job throughput: every rank processed flops_per_rank in at most ms milliseconds."""
     return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
+def chosen_workload(args):
+    """The workload named by --workload, at S1 = S2 = --seq-len when that is given."""
+    from attention_backward_fabwd_gb300 import inputs
+
+    w = inputs.WORKLOADS[args.workload]
+    if args.seq_len:
+        if w.layout == "TND":
+            raise SystemExit("--seq-len applies to BSND/BNSD workloads")
+        w = inputs.sized(w, name=f"{w.name}@S{args.seq_len}", S1=args.seq_len, S2=args.seq_len)
+    return w
 
 
 def replica_workload(w, rank):
@@ -584,7 +599,7 @@ def gpu_arm(args, rank, world, local_rank):
     build.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = replica_workload(inputs.WORKLOADS[args.workload], rank)
+    w = replica_workload(chosen_workload(args), rank)
     c = prepare(w, dev, args.dq_mode)
     pb = c["pb"]
     q, k, v, dout, attn_out, lse = c["ins"]
@@ -697,7 +712,7 @@ def gpu_arm(args, rank, world, local_rank):
     names = list(inputs.WORKLOADS) if args.workloads == "all" else \
         ([] if args.workloads == "none" else [x for x in args.workloads.split(",") if x])
     for name in names:
-        if name == args.workload:
+        if name == args.workload and not args.seq_len:
             continue
         wo = replica_workload(inputs.WORKLOADS[name], rank)
         co = prepare(wo, dev, args.dq_mode)
@@ -802,7 +817,7 @@ def reference_arm(args, rank, world):
 
     if rank != 0:
         return None
-    w = inputs.WORKLOADS[args.workload]
+    w = chosen_workload(args)
     pb = inputs.make_problem(w)
     gen = oracle_head_sampler(pb)
     for _ in range(max(args.warmup, 0)):
