@@ -752,6 +752,26 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def oracle_head_sampler(pb):
     """Yields (seconds, flops_convention) of the fp64 oracle backward of one head at a time."""
     from attention_backward_fabwd_gb300 import inputs
@@ -807,8 +827,8 @@ def cpu_baseline(pb, budget_s):
         shape = shp
         if secs >= budget_s:
             break
-    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"fp64 numpy oracle backward of {heads} head(s) of the workload (S1xS2 {shape[0]}x{shape[1]}), "
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "cpu_model": cpu_model(),
+            "kind": "oracle", "sample": f"fp64 numpy oracle backward of {heads} head(s) of the workload (S1xS2 {shape[0]}x{shape[1]}), "
                       f"{secs:.1f} s of CPU time, same flop convention"}
 
 
@@ -841,7 +861,8 @@ def reference_arm(args, rank, world):
             "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": workload_config(pb, l2="n/a (CPU)"),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "cpu_model": cpu_model(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0, "wall_s": time.perf_counter() - t0}
 
