@@ -316,6 +316,27 @@ def test_bad_cu_seqlens_reported_not_faulted():
                         layout_out="TND", mask_mode=1, win_left=1024, win_right=0, check_status=True)
 
 
+def test_decreasing_cu_seqlens_reported_not_faulted():
+    # a sequence with a negative span owns no unit of the varlen grids: the backward's preprocess
+    # and the forward's first CTA still report it; the rows the other sequences cover stay in range
+    w = inputs.sized(W["varlen_window_fp16_d128"], B=3, N1=2, N2=2)
+    pb = inputs.make_problem(w, [100, 0, 60])
+    ref = tl.forward_inputs(pb)
+    dev = torch.device("cuda")
+    bad = torch.tensor([0, 100, 40, 160], dtype=torch.int32, device=dev)
+    args = [t.to(dev) for t in (pb.q, pb.k, pb.v, pb.dout, ref.attn_out, ref.lse)]
+    kw = dict(cu_seqlens_q=bad, cu_seqlens_kv=bad, max_seqlen_q=128, max_seqlen_kv=128)
+    with pytest.raises(F.FabwdError) as ei:
+        api.flash_attn_grad(*args, layout_q="TND", layout_kv="TND", layout_out="TND", check_status=True, **kw)
+    assert ei.value.status == F.FABWD_ERR_DEVICE
+    with pytest.raises(F.FabwdError) as ei:
+        api.flash_attn_forward(*args[:3], layout="TND", check_status=True, **kw)
+    assert ei.value.status == F.FABWD_ERR_DEVICE
+    # the context stays usable
+    cu = torch.from_numpy(pb.cu_seqlens_q).to(dev)
+    api.flash_attn_forward(*args[:3], cu_seqlens_q=cu, cu_seqlens_kv=cu, layout="TND", check_status=True)
+
+
 def test_timeout_injection_returns_status_and_context_survives():
     w = inputs.sized(W["gqa_causal_s4096_d128"], N1=4, N2=2, S1=256, S2=256, dout_std=1.0)
     pb = inputs.make_problem(w)
