@@ -71,8 +71,8 @@ fabwd_status plan_and_check(const fabwd_params* p, Plan* pl, bool check_ptrs) {
   // Each batch is one grid row of 128-row query blocks over N1 heads plus 128-row key blocks
   // over N2 heads; that count must fit a launch's x dimension (and the int the launches use).
   if ((p->S1 + 127) / 128 * p->N1 + (p->S2 + 127) / 128 * p->N2 > 0x7fffffffll) return FABWD_ERR_UNSUPPORTED;
-  // Varlen grids run over every sequence's units in one x dimension.
-  if (tnd && tnd_blocks_bound(p->B, p->S1, p->T1, 128) * p->N1 + tnd_blocks_bound(p->B, p->S2, p->T2, 128) * p->N2 >
+  // Flat varlen grids run over every sequence's units in one x dimension.
+  if (flat_grid(p->layout, p->B) && tnd_blocks_bound(p->B, p->S1, p->T1, 128) * p->N1 + tnd_blocks_bound(p->B, p->S2, p->T2, 128) * p->N2 >
                  0x7fffffffll)
     return FABWD_ERR_UNSUPPORTED;
 

@@ -441,7 +441,7 @@ cudaError_t launch_dq_flat(const MainArgs& a, const MainMaps& m, dim3 grid, cuda
 template <int D, int DV, bool FP16>
 cudaError_t launch_dq_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) {
   using C = DqCfg<D, DV>;
-  if (a.layout == kTND)
+  if (flat_grid(a.layout, a.B))
     return launch_dq_flat<D, DV, FP16, true>(
         a, m, dim3((unsigned)(tnd_blocks_bound(a.B, a.S1, a.T1, C::BM) * a.N1), 1), st);
   return launch_dq_flat<D, DV, FP16, false>(a, m, dim3(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B), st);

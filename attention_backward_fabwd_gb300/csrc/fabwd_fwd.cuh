@@ -461,7 +461,7 @@ cudaError_t launch_fwd_flat(const MainArgs& a, const MainMaps& m, dim3 grid, cud
 template <int D, int DV, bool FP16>
 cudaError_t launch_fwd_t(const MainArgs& a, const MainMaps& m, cudaStream_t st) {
   using C = FwdCfg<D, DV>;
-  if (a.layout == kTND)
+  if (flat_grid(a.layout, a.B))
     return launch_fwd_flat<D, DV, FP16, true>(
         a, m, dim3((unsigned)(tnd_blocks_bound(a.B, a.S1, a.T1, C::BM) * a.N1), 1), st);
   return launch_fwd_flat<D, DV, FP16, false>(a, m, dim3(((a.S1 + C::BM - 1) / C::BM) * a.N1, a.B), st);

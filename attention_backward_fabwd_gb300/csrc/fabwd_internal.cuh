@@ -40,10 +40,15 @@ constexpr int dq_block_kv(int D, int DV) { return D > 128 ? (DV > 128 ? 64 : 96)
 
 enum Layout : int { kBSND = 0, kTND = 1, kBNSD = 2 };
 
-// Varlen (TND) grids run over the sequences' own work units back to back instead of B times the
-// units of the longest sequence.  Upper bound of sum over sequences of ceil(L_b / blk) for B
-// sequences of at most S rows and T rows in all: each term is at most (L_b + blk - 1) / blk and
-// at most ceil(S / blk).
+// Varlen (TND) grids of up to kFlatMaxSeqs sequences run over the sequences' own work units back
+// to back instead of B times the units of the longest sequence.  Each CTA finds its unit with a
+// warp scan of the cu_seqlens spans, 32 sequences per round, each round about one cu_seqlens
+// round trip (what an empty CTA of the B-by-units grid costs): kept to two rounds, more
+// sequences keep that grid.
+constexpr int kFlatMaxSeqs = 64;
+inline bool flat_grid(int layout, long long B) { return layout == kTND && B <= kFlatMaxSeqs; }
+// Upper bound of sum over sequences of ceil(L_b / blk) for B sequences of at most S rows and T
+// rows in all: each term is at most (L_b + blk - 1) / blk and at most ceil(S / blk).
 inline long long tnd_blocks_bound(long long B, long long S, long long T, int blk) {
   const long long by_max = B * ((S + blk - 1) / blk), by_total = (T + (long long)(blk - 1) * B) / blk;
   return by_max < by_total ? by_max : by_total;

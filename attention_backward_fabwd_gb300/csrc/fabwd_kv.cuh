@@ -538,7 +538,7 @@ cudaError_t launch_kv_flat(const MainArgs& a, const MainMaps& m, dim3 grid, cuda
 template <int D, int DV, bool FP16>
 cudaError_t launch_kv_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
   using C = KvCfg<D, DV>;
-  if (a.layout == kTND)
+  if (flat_grid(a.layout, a.B))
     return launch_kv_flat<D, DV, FP16, true>(
         a, m, dim3((unsigned)(tnd_blocks_bound(a.B, a.S2, a.T2, C::BC) * a.N2), 1), st);
   return launch_kv_flat<D, DV, FP16, false>(a, m, dim3(n_kv_blocks * a.N2, a.B), st);

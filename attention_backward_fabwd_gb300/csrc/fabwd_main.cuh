@@ -680,7 +680,7 @@ template <int D, int DV, bool FP16>
 cudaError_t launch_main_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
   // blockIdx.x = kv-block * N2 + kv-head: the heaviest kv-blocks (earliest keys under a causal
   // mask) of every head launch first.
-  if (a.layout == kTND)
+  if (flat_grid(a.layout, a.B))
     return launch_main_flat<D, DV, FP16, true>(
         a, m, dim3((unsigned)(tnd_blocks_bound(a.B, a.S2, a.T2, kBlockKV) * a.N2), 1), st);
   return launch_main_flat<D, DV, FP16, false>(a, m, dim3(n_kv_blocks * a.N2, a.B), st);

@@ -28,10 +28,10 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, int threads, uint32_t smem, cuda
   return cfg;
 }
 
-// Which CTA kind and unit blockIdx stands for.  BSND / BNSD: grid (kv_ctas + dQ units, B), the
-// dK/dV units first.  Varlen (FLAT): a flat grid over every sequence's dK/dV units and then its
-// dQ units, the sequences back to back (flat_unit), so that short sequences leave no CTAs that
-// only exit; CTAs past the last unit return.
+// Which CTA kind and unit blockIdx stands for.  BSND / BNSD (and varlen with many sequences):
+// grid (kv_ctas + dQ units, B), the dK/dV units first.  Varlen (FLAT): a flat grid over every
+// sequence's dK/dV units and then its dQ units, the sequences back to back (flat_unit), so that
+// short sequences leave no CTAs that only exit; CTAs past the last unit return.
 struct GridUnit {
   int b, local, nqb;
   bool kv;
@@ -51,7 +51,7 @@ __device__ __forceinline__ bool grid_unit(const MainArgs& a, int kv_ctas, int kv
 
 // Grid of the one-grid launch: (dK/dV units + dQ units, B), or the flat varlen grid's bound.
 inline dim3 one_grid(const MainArgs& a, int n_kv_blocks, int kv_rows, int q_rows) {
-  if (a.layout == kTND)
+  if (flat_grid(a.layout, a.B))
     return dim3((unsigned)(tnd_blocks_bound(a.B, a.S2, a.T2, kv_rows) * a.N2 +
                            tnd_blocks_bound(a.B, a.S1, a.T1, q_rows) * a.N1),
                 1);
@@ -88,7 +88,7 @@ cudaError_t launch_bwd_flat(const MainArgs& a, const MainMaps& m, int n_kv_block
 
 template <int D, int DV, bool FP16>
 cudaError_t launch_bwd_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
-  return a.layout == kTND ? launch_bwd_flat<D, DV, FP16, true>(a, m, n_kv_blocks, st)
+  return flat_grid(a.layout, a.B) ? launch_bwd_flat<D, DV, FP16, true>(a, m, n_kv_blocks, st)
                           : launch_bwd_flat<D, DV, FP16, false>(a, m, n_kv_blocks, st);
 }
 
@@ -129,7 +129,7 @@ cudaError_t launch_bwd_wide_flat(const MainArgs& a, const MainMaps& mkv, const M
 template <int D, int DV, bool FP16>
 cudaError_t launch_bwd_wide_t(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int n_kv_blocks,
                               cudaStream_t st) {
-  return a.layout == kTND ? launch_bwd_wide_flat<D, DV, FP16, true>(a, mkv, mdq, n_kv_blocks, st)
+  return flat_grid(a.layout, a.B) ? launch_bwd_wide_flat<D, DV, FP16, true>(a, mkv, mdq, n_kv_blocks, st)
                           : launch_bwd_wide_flat<D, DV, FP16, false>(a, mkv, mdq, n_kv_blocks, st);
 }
 

@@ -69,6 +69,9 @@ SMALL = [
     # empty ones among them, q and kv lengths unequal
     ("tnd_many_sequences", inputs.sized(W["varlen_window_fp16_d128"], B=37, N1=2, N2=1, win_left=64),
      ([(i * 53) % 190 for i in range(37)], [(i * 71 + 5) % 160 for i in range(37)])),
+    # more sequences than the flat varlen grid takes: the (units, B) grid, empty CTAs included
+    ("tnd_70_sequences", inputs.sized(W["varlen_window_fp16_d128"], B=70, N1=2, N2=2, win_left=-1),
+     ([(i * 37) % 150 for i in range(70)], None)),
     ("d192_dv128_causal", inputs.sized(W["causal_s8192_d192_dv128"], N1=2, N2=2, S1=300, S2=300), None),
     ("d192_dv128_gqa_fp16_band", inputs.sized(W["causal_s8192_d192_dv128"], dtype="fp16", N1=4, N2=2, S1=260,
                                               S2=390, mask_mode=2, win_left=100, win_right=30), None),
