@@ -52,7 +52,8 @@ struct KvCfg {
   static constexpr uint32_t cDK = 0, cDV = D, cS = D + DV, cP = cS + BR;
   static_assert(D % 64 == 0 && DV % 64 == 0 && DV <= D && D <= 192, "head dims");
   static_assert(cP + BR <= 512, "TMEM budget");
-  static_assert((D / 64 + DV / 64) * BC * 128 <= NQ * kQ + NO * kdO, "dK/dV staging fits in the Q and dO rings");
+  static_assert(DV / 64 * BC * 128 <= NO * kdO, "dV staging fits in the dO ring");
+  static_assert(D / 64 * BC * 128 <= NQ * kQ, "dK staging fits in the Q ring");
   static_assert(bytes <= 232448, "shared memory budget");
 };
 
@@ -394,36 +395,25 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
       }
     }
     // ---- epilogue: dK = scale · acc, dV = acc; zeros when no query sees this block
-    if (ok && T > 0) ok = wait_bar_warp(&bars[kKvAccDone], 0, abort_flag, a);
     // A block whose 128 rows lie inside its sequence is staged in shared memory (the drained
     // Q/dO rings) as 128-byte-swizzled 64-column tiles and written by TMA stores, one per tile;
     // the last block of a TND sequence, whose box would reach into the next sequence's rows,
     // is written row by row.  A thread's 16-byte stores to rows 2 KB or more apart would
-    // otherwise take one request each.
+    // otherwise take one request each.  dV is final once the last dV product has completed
+    // (the commit on its dO stage, which also frees the dO ring): its tiles are staged in the dO
+    // ring and stored while the last dK product still runs; dK follows through the Q ring.
     const bool staged = !tnd || j0 + BC <= sq.span_k;  // the same in every thread of the CTA
     if (staged) {
-      tc_fence_after();
-      uint8_t* stage = smem + C::oQ;  // D/64 dK tiles, then Dv/64 dV tiles, BC·128 bytes each
-      auto put = [&](int tile, int unit0, const uint32_t (&o)[16]) {
+      auto put = [&](uint8_t* stage, int tile, int unit0, const uint32_t (&o)[16]) {
         uint8_t* rowp = stage + tile * BC * 128 + row * 128;
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4)
           st_shared_v4(smem_u32(rowp + (((unit0 + v4) ^ (row & 7)) << 4)), o[4 * v4], o[4 * v4 + 1], o[4 * v4 + 2],
                        o[4 * v4 + 3]);
       };
-#pragma unroll 1
-      for (int c = 0; ok && c < D / 64; ++c) {
-        const int col = g * (D / 2) + c * 32;
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::cDK + col, r);
-        tmem_wait_ld();
-        reg_fence(r);
-        uint32_t o[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * -a.scale, __uint_as_float(r[e + 1]) * -a.scale) : 0u;
-        put(col / 64, (col % 64) / 8, o);
-      }
+      if (ok && T > 0) ok = wait_bar_warp(&bars[kKvOEmpty + (T - 1) % NO], ((T - 1) / NO) & 1, abort_flag, a);
+      tc_fence_after();
+      uint8_t* vstage = smem + C::odO;  // Dv/64 dV tiles, BC·128 bytes each
 #pragma unroll 1
       for (int c = 0; ok && c < DV / 64; ++c) {
         const int col = g * (DV / 2) + c * 32;
@@ -435,23 +425,46 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
           o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]), __uint_as_float(r[e + 1])) : 0u;
-        put(D / 64 + col / 64, (col % 64) / 8, o);
+        put(vstage, col / 64, (col % 64) / 8, o);
       }
       fence_proxy_async_smem();
-      // every compute thread reaches this barrier (staged is CTA-uniform); the tiles are stored
+      // every compute thread reaches these barriers (staged is CTA-uniform); tiles are stored
       // only if every warp wrote its part
-      const bool all_ok = compute_warps_all(ok);
-      if (all_ok && warp == 0 && lane == 0) {
+      const bool v_ok = compute_warps_all(ok);
+      if (v_ok && warp == 0 && lane == 0) {
 #pragma unroll 1
-        for (int c = 0; c < D / 64 + DV / 64; ++c) {
-          const CUtensorMap* m = c < D / 64 ? &tm_dk : &tm_dv;
-          const int x = (c < D / 64 ? c : c - D / 64) * 64;
-          tma_store_4d(m, stage + c * BC * 128, x, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
-        }
+        for (int c = 0; c < DV / 64; ++c)
+          tma_store_4d(&tm_dv, vstage + c * BC * 128, c * 64, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
         bulk_commit_group();
+      }
+      if (ok && T > 0) ok = wait_bar_warp(&bars[kKvAccDone], 0, abort_flag, a);
+      tc_fence_after();
+      uint8_t* kstage = smem + C::oQ;  // D/64 dK tiles
+#pragma unroll 1
+      for (int c = 0; ok && c < D / 64; ++c) {
+        const int col = g * (D / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::cDK + col, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          o[e >> 1] = T > 0 ? pack2<FP16>(__uint_as_float(r[e]) * -a.scale, __uint_as_float(r[e + 1]) * -a.scale) : 0u;
+        put(kstage, col / 64, (col % 64) / 8, o);
+      }
+      fence_proxy_async_smem();
+      const bool k_ok = compute_warps_all(ok);
+      if (warp == 0 && lane == 0) {
+        if (k_ok) {
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c)
+            tma_store_4d(&tm_dk, kstage + c * BC * 128, c * 64, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
+          bulk_commit_group();
+        }
         bulk_wait_group_read0();  // the tiles are read before the CTA's shared memory is released
       }
-    } else if (ok) {
+    } else if (ok && (T == 0 || (ok = wait_bar_warp(&bars[kKvAccDone], 0, abort_flag, a)))) {
       tc_fence_after();
       const long long krow = row_index(a.layout, b, (long long)(tnd ? sq.k0 : 0) + (j_valid ? jr : 0), n2, a.N2, a.S2);
       uint16_t* dk = static_cast<uint16_t*>(a.dk) + krow * a.io_d;

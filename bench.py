@@ -450,7 +450,7 @@ def stage_table(pb, r, peak_tf, peak_hbm):
 
 
 # revision of each kernel's code that profiles/traffic.json must match
-KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v7", "fabwd_bwd_wide_kernel": "wide-v6", "fabwd_kv_kernel": "kv-v9",
+KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v8", "fabwd_bwd_wide_kernel": "wide-v7", "fabwd_kv_kernel": "kv-v10",
               "fabwd_dq_kernel": "dq-v10", "fabwd_main_kernel": "main-v7"}
 
 
