@@ -370,7 +370,6 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
         for (int c = 0; c < D / 64; ++c)
           tma_store_4d(&tm_dq, stage + c * BM * 128, c * 64, bnsd ? q_row : n1, bnsd ? n1 : q_row, bcoord);
         bulk_commit_group();
-        bulk_wait_group_read0();  // the tiles are read before the CTA's shared memory is released
       }
     } else if (ok) {
       tc_fence_after();
@@ -411,6 +410,9 @@ __device__ __forceinline__ void dq_block(const CUtensorMap& tm_q, const CUtensor
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // the TMA stores issued in the epilogue read their tiles before the CTA's shared memory is
+  // released; that drain overlaps the tensor-memory release above
+  if (warp == 0 && lane == 0) bulk_wait_group_read0();
 }
 
 template <int D, int DV, bool FP16, bool FLAT>

@@ -455,14 +455,11 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
       }
       fence_proxy_async_smem();
       const bool k_ok = compute_warps_all(ok);
-      if (warp == 0 && lane == 0) {
-        if (k_ok) {
+      if (k_ok && warp == 0 && lane == 0) {
 #pragma unroll 1
-          for (int c = 0; c < D / 64; ++c)
-            tma_store_4d(&tm_dk, kstage + c * BC * 128, c * 64, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
-          bulk_commit_group();
-        }
-        bulk_wait_group_read0();  // the tiles are read before the CTA's shared memory is released
+        for (int c = 0; c < D / 64; ++c)
+          tma_store_4d(&tm_dk, kstage + c * BC * 128, c * 64, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
+        bulk_commit_group();
       }
     } else if (ok && (T == 0 || (ok = wait_bar_warp(&bars[kKvAccDone], 0, abort_flag, a)))) {
       tc_fence_after();
@@ -521,6 +518,9 @@ __device__ __forceinline__ void kv_block(const CUtensorMap& tm_q, const CUtensor
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // the TMA stores issued in the epilogue read their tiles before the CTA's shared memory is
+  // released; that drain overlaps the tensor-memory release above
+  if (warp == 0 && lane == 0) bulk_wait_group_read0();
 }
 
 template <int D, int DV, bool FP16, bool FLAT>

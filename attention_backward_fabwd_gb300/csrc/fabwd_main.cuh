@@ -588,7 +588,6 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
           tma_store_4d(m, stage + c * BC * 128, x, bnsd ? kv_row0 : n2, bnsd ? n2 : kv_row0, bcoord);
         }
         bulk_commit_group();
-        bulk_wait_group_read0();  // the tiles are read before the CTA's shared memory is released
       }
     } else if (ok) {
       tc_fence_after();
@@ -649,6 +648,9 @@ __device__ __forceinline__ void main_block(const CUtensorMap& tm_q, const CUtens
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // the TMA stores issued in the epilogue read their tiles before the CTA's shared memory is
+  // released; that drain overlaps the tensor-memory release above
+  if (warp == 0 && lane == 0) bulk_wait_group_read0();
 }
 
 template <int D, int DV, bool FP16, bool FLAT>

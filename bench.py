@@ -450,8 +450,8 @@ def stage_table(pb, r, peak_tf, peak_hbm):
 
 
 # revision of each kernel's code that profiles/traffic.json must match
-KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v8", "fabwd_bwd_wide_kernel": "wide-v7", "fabwd_kv_kernel": "kv-v10",
-              "fabwd_dq_kernel": "dq-v10", "fabwd_main_kernel": "main-v7"}
+KERNEL_REV = {"fabwd_bwd_kernel": "bwd-v9", "fabwd_bwd_wide_kernel": "wide-v8", "fabwd_kv_kernel": "kv-v11",
+              "fabwd_dq_kernel": "dq-v11", "fabwd_main_kernel": "main-v8"}
 
 
 def max_over_ranks(values, world, device="cpu"):
