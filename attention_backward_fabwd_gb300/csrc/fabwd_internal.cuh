@@ -42,8 +42,8 @@ enum Layout : int { kBSND = 0, kTND = 1, kBNSD = 2 };
 
 // Varlen (TND) grids of up to kFlatMaxSeqs sequences run over the sequences' own work units back
 // to back instead of B times the units of the longest sequence.  Each CTA finds its unit with a
-// warp scan of the cu_seqlens spans, 32 sequences per round, each round about one cu_seqlens
-// round trip (what an empty CTA of the B-by-units grid costs): kept to two rounds, more
+// warp scan of the cu_seqlens spans, 32 sequences per pass, each pass about one cu_seqlens
+// load latency (what an empty CTA of the B-by-units grid costs): kept to two passes, more
 // sequences keep that grid.
 constexpr int kFlatMaxSeqs = 64;
 inline bool flat_grid(int layout, long long B) { return layout == kTND && B <= kFlatMaxSeqs; }
