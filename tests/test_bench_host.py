@@ -84,3 +84,26 @@ def test_nvml_sampler_without_a_gpu_is_unavailable():
     c = bench.NvmlClocks("00000000:00:00.0")
     if not c.available:
         assert c.summary() is None
+
+
+def test_seq_len_sizes_the_chosen_workload():
+    # --seq-len runs a BSND/BNSD workload at S1 = S2 = N under its own name; varlen is refused
+    import argparse
+    import bench
+
+    args = argparse.Namespace(workload="causal_s8192_d192_dv128", seq_len=512)
+    w = bench.chosen_workload(args)
+    base = inputs.WORKLOADS["causal_s8192_d192_dv128"]
+    assert (w.S1, w.S2, w.name) == (512, 512, "causal_s8192_d192_dv128@S512")
+    assert (w.D, w.Dv, w.N1, w.N2, w.mask_mode, w.dtype) == (base.D, base.Dv, base.N1, base.N2, base.mask_mode,
+                                                             base.dtype)
+    args.seq_len = 0
+    assert bench.chosen_workload(args) is base
+    with pytest.raises(SystemExit):
+        bench.chosen_workload(argparse.Namespace(workload="varlen_window_fp16_d128", seq_len=512))
+
+
+def test_cpu_model_is_named():
+    import bench
+    name = bench.cpu_model()
+    assert isinstance(name, str) and name
