@@ -89,7 +89,7 @@ cudaError_t launch_bwd_flat(const MainArgs& a, const MainMaps& m, int n_kv_block
 template <int D, int DV, bool FP16>
 cudaError_t launch_bwd_t(const MainArgs& a, const MainMaps& m, int n_kv_blocks, cudaStream_t st) {
   return flat_grid(a.layout, a.B) ? launch_bwd_flat<D, DV, FP16, true>(a, m, n_kv_blocks, st)
-                          : launch_bwd_flat<D, DV, FP16, false>(a, m, n_kv_blocks, st);
+                                  : launch_bwd_flat<D, DV, FP16, false>(a, m, n_kv_blocks, st);
 }
 
 // D > 128: the two CTA kinds take different tensor-map boxes (the dK/dV CTAs stream 64-row query
@@ -130,7 +130,7 @@ template <int D, int DV, bool FP16>
 cudaError_t launch_bwd_wide_t(const MainArgs& a, const MainMaps& mkv, const MainMaps& mdq, int n_kv_blocks,
                               cudaStream_t st) {
   return flat_grid(a.layout, a.B) ? launch_bwd_wide_flat<D, DV, FP16, true>(a, mkv, mdq, n_kv_blocks, st)
-                          : launch_bwd_wide_flat<D, DV, FP16, false>(a, mkv, mdq, n_kv_blocks, st);
+                                  : launch_bwd_wide_flat<D, DV, FP16, false>(a, mkv, mdq, n_kv_blocks, st);
 }
 
 }  // namespace fabwd
