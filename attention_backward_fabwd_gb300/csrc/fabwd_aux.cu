@@ -65,18 +65,49 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
   constexpr int UN = 4;                   // row groups per iteration
   constexpr int RPI = RPW * UN;           // rows per warp iteration
   static_assert(kRowPad % RPI == 0, "an iteration's rows stay within one padded row block");
-  const long long ngroups = (long long)a.B * a.N1 * a.S1p / RPI;
+  long long ngroups = (long long)a.B * a.N1 * a.S1p / RPI;
   const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, part = lane % LPR;
   const bool tnd = a.layout == kTND;
   const long long rstep = a.layout == kBNSD ? 1 : a.N1;  // row_index step from row i to i + 1
+  // Varlen with up to 32 sequences: the iterations run over each sequence's own rows up to its
+  // last 128-row block only (lane s of every warp holds sequence s's count of iterations and
+  // their running sum), instead of max_seqlen rows per sequence of which the excess is skipped.
+  const bool compact = tnd && a.B <= 32;
+  long long cnt = 0, incl = 0;
+  if (compact) {
+    if (lane < a.B) {
+      const long long s0 = a.cu_q[lane];
+      long long L = (long long)a.cu_q[lane + 1] - s0;
+      if (s0 < 0 || s0 > a.T1) L = 0;
+      L = L < 0 ? 0 : (L > a.S1 ? a.S1 : L);
+      if (s0 + L > a.T1) L = a.T1 - s0 < 0 ? 0 : a.T1 - s0;
+      if (a.used_q) {
+        const long long us = a.used_q[lane];
+        L = us < 0 ? 0 : (us < L ? us : L);
+      }
+      cnt = (L + 127) / 128 * (128 / RPI) * a.N1;
+    }
+    incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    ngroups = __shfl_sync(0xffffffffu, incl, 31);
+  }
   for (long long grp = gwarp; grp < ngroups; grp += nwarp) {
     int b, n1;
     long long i0;
     const int ipb = a.S1p / RPI;  // iterations per (b, n1)
-    if (SMALL) {
+    if (compact) {
+      b = __popc(__ballot_sync(0xffffffffu, incl <= grp));  // the sequences that end at or before grp
+      const long long local = grp - (__shfl_sync(0xffffffffu, incl, b) - __shfl_sync(0xffffffffu, cnt, b));
+      n1 = (int)(local % a.N1);
+      i0 = (local / a.N1) * RPI;
+    } else if (SMALL) {
       const uint32_t g32 = (uint32_t)grp, N1 = (uint32_t)a.N1;
       const uint32_t t = g32 / N1;
       n1 = (int)(g32 - t * N1);
