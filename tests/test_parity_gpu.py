@@ -69,6 +69,9 @@ SMALL = [
     # empty ones among them, q and kv lengths unequal
     ("tnd_many_sequences", inputs.sized(W["varlen_window_fp16_d128"], B=37, N1=2, N2=1, win_left=64),
      ([(i * 53) % 190 for i in range(37)], [(i * 71 + 5) % 160 for i in range(37)])),
+    # exactly one warp's worth of sequences (every lane of the varlen scans holds one)
+    ("tnd_32_sequences", inputs.sized(W["varlen_window_fp16_d128"], dtype="bf16", B=32, N1=4, N2=2, win_left=40),
+     ([(i * 29) % 140 for i in range(32)], [(i * 43 + 7) % 150 for i in range(32)])),
     # more sequences than the flat varlen grid takes: the (units, B) grid, empty CTAs included
     ("tnd_70_sequences", inputs.sized(W["varlen_window_fp16_d128"], B=70, N1=2, N2=2, win_left=-1),
      ([(i * 37) % 150 for i in range(70)], None)),
