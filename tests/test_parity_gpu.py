@@ -384,6 +384,18 @@ def test_full_size_elementwise(name, dq_mode, parity_report):
     parity_report(f"{name} [{dq_mode}]", errs)
 
 
+def test_long_sequence_elementwise(parity_report):
+    # twice the longest measured sequence (128 key and query blocks per head, GQA G = 2, causal):
+    # every element against the oracle
+    w = inputs.sized(W["causal_b2_s2048_d128"], B=1, N1=2, N2=1, S1=16384, S2=16384, D=64, Dv=64)
+    pb = inputs.make_problem(w)
+    ref = tl.full_reference_parallel(pb)
+    dq, dk, dv, sf = tl.run_gpu(pb, ref)
+    errs = check_all(pb, ref, dq, dk, dv, sf)
+    errs["sfmg"] = tl.errors(sf, ref.sfmg)
+    parity_report("causal S=16384 D=64 G=2 [auto]", errs)
+
+
 def test_head_dim_not_multiple_of_8_is_unsupported():
     q = torch.zeros(1, 256, 2, 100, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(F.FabwdError) as ei:
