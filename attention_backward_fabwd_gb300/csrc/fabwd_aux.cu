@@ -72,39 +72,52 @@ __global__ void __launch_bounds__(256) preprocess_kernel(PreArgs a) {
   const int sub = lane / LPR, part = lane % LPR;
   const bool tnd = a.layout == kTND;
   const long long rstep = a.layout == kBNSD ? 1 : a.N1;  // row_index step from row i to i + 1
-  // Varlen with up to 32 sequences: the iterations run over each sequence's own rows up to its
-  // last 128-row block only (lane s of every warp holds sequence s's count of iterations and
-  // their running sum), instead of max_seqlen rows per sequence of which the excess is skipped.
-  const bool compact = tnd && a.B <= 32;
-  long long cnt = 0, incl = 0;
+  // Varlen with up to 64 sequences: the iterations run over each sequence's own rows up to its
+  // last 128-row block only (lanes s and s + 32 of every warp hold sequences s and s + 32: their
+  // counts of iterations and running sums), instead of max_seqlen rows per sequence of which the
+  // excess is skipped.
+  const bool compact = tnd && a.B <= 64;
+  long long cnt0 = 0, cnt1 = 0, incl0 = 0, incl1 = 0;
   if (compact) {
-    if (lane < a.B) {
-      const long long s0 = a.cu_q[lane];
-      long long L = (long long)a.cu_q[lane + 1] - s0;
+    auto count = [&](int s) -> long long {  // iterations of sequence s (0 past the last one)
+      if (s >= a.B) return 0;
+      const long long s0 = a.cu_q[s];
+      long long L = (long long)a.cu_q[s + 1] - s0;
       if (s0 < 0 || s0 > a.T1) L = 0;
       L = L < 0 ? 0 : (L > a.S1 ? a.S1 : L);
       if (s0 + L > a.T1) L = a.T1 - s0 < 0 ? 0 : a.T1 - s0;
       if (a.used_q) {
-        const long long us = a.used_q[lane];
+        const long long us = a.used_q[s];
         L = us < 0 ? 0 : (us < L ? us : L);
       }
-      cnt = (L + 127) / 128 * (128 / RPI) * a.N1;
-    }
-    incl = cnt;
+      return (L + 127) / 128 * (128 / RPI) * a.N1;
+    };
+    cnt0 = count(lane);
+    cnt1 = count(lane + 32);
+    incl0 = cnt0;
+    incl1 = cnt1;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+      const long long v0 = __shfl_up_sync(0xffffffffu, incl0, o), v1 = __shfl_up_sync(0xffffffffu, incl1, o);
+      if (lane >= o) {
+        incl0 += v0;
+        incl1 += v1;
+      }
     }
-    ngroups = __shfl_sync(0xffffffffu, incl, 31);
+    incl1 += __shfl_sync(0xffffffffu, incl0, 31);
+    ngroups = __shfl_sync(0xffffffffu, incl1, 31);
   }
   for (long long grp = gwarp; grp < ngroups; grp += nwarp) {
     int b, n1;
     long long i0;
     const int ipb = a.S1p / RPI;  // iterations per (b, n1)
     if (compact) {
-      b = __popc(__ballot_sync(0xffffffffu, incl <= grp));  // the sequences that end at or before grp
-      const long long local = grp - (__shfl_sync(0xffffffffu, incl, b) - __shfl_sync(0xffffffffu, cnt, b));
+      // the sequences that end at or before grp
+      b = __popc(__ballot_sync(0xffffffffu, incl0 <= grp)) + __popc(__ballot_sync(0xffffffffu, incl1 <= grp));
+      const int src = b & 31;
+      const long long ib = b < 32 ? __shfl_sync(0xffffffffu, incl0, src) : __shfl_sync(0xffffffffu, incl1, src);
+      const long long cb = b < 32 ? __shfl_sync(0xffffffffu, cnt0, src) : __shfl_sync(0xffffffffu, cnt1, src);
+      const long long local = grp - (ib - cb);
       n1 = (int)(local % a.N1);
       i0 = (local / a.N1) * RPI;
     } else if (SMALL) {
